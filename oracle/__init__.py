@@ -1,0 +1,40 @@
+"""Reference oracle for fused exact attention — TEST INFRASTRUCTURE ONLY.
+
+This package is a plain, slow, fp64 CPU restatement of what the GPU path
+computes.  It exists so that tests, the package smoke check and the bench's
+CPU-baseline leg have something independent to compare against.  Nothing in
+the product path (the CUDA library and its Python binding) may import it, and
+it imports nothing from the product path: the two share no code.
+
+Sources (web pages about FlashAttention, Dao et al. 2022):
+  * "FlashAttention: Cơ chế Attention chính xác, nhanh và tối ưu bộ nhớ với
+    nhận thức IO" (xyznot.com/vi/paper/2205.14135) — online-softmax
+    statistics, block-sparse mask, stored (l, m) statistics.
+  * "3.3 Hiểu sâu cơ chế Self-Attention" (infra-guide-du8.pages.dev) — the
+    scaled dot-product definition (§3, §4), safe softmax (§7.2), causal mask
+    (§10.2), tiling (§12.2).
+  * "FlashAttention: انتباه دقيق وسريع وموفِّر للذاكرة" (azimuth.plus/paper/
+    flashattention) — the step-by-step algorithm and the online-softmax update.
+
+Modules
+  attention  -- the plain definition: masked scaled scores, softmax, dropout,
+                O and the per-row logsumexp L, and the chain-rule gradients.
+  philox     -- Philox4x32-10 counter-based generator (Salmon et al., SC'11),
+                a vectorised numpy version and an independent scalar one.
+  blockwise  -- the pages' tiled online-softmax recurrence, restated; used
+                only to pin the direct definition in tests.
+
+Parity status: the Philox constants are not pinned to published known-answer
+vectors (none are available here); "parity partly unpinned" for `philox`.
+Everything else is pinned by tests under tests/test_oracle_*.py.
+"""
+
+from .attention import (  # noqa: F401
+    allowed_mask,
+    attention_forward,
+    attention_backward,
+    forward_rows,
+    backward_keys,
+    dropout_threshold,
+    keep_mask,
+)

@@ -1,0 +1,436 @@
+"""Pins of the fp64 oracle against facts fixed by the pages and by mathematics.
+
+None of these tests needs a GPU.  Each checks the oracle against something
+other than itself: a value printed on the pages (tests/golden/), a closed form,
+an invariant, a library routine on a special case, a brute-force scalar loop
+on tiny inputs, or finite differences.
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+from oracle import attention as A
+from oracle.blockwise import blockwise_forward
+from oracle.philox import philox4x32_10, philox4x32_10_scalar
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+def _rand(shape, seed, std=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * std
+
+
+def _fwd(q, k, v, **kw):
+    """Forward on a single head given as [N, d] arrays."""
+    O, L = A.attention_forward(q[None, None], k[None, None], v[None, None], **kw)
+    return O[0, 0], L[0, 0]
+
+
+def _bwd(q, k, v, do, **kw):
+    O, L, dQ, dK, dV = A.attention_backward(q[None, None], k[None, None],
+                                            v[None, None], do[None, None], **kw)
+    return O[0, 0], L[0, 0], dQ[0, 0], dK[0, 0], dV[0, 0]
+
+
+# ---------------------------------------------------------------- masks ----
+
+def test_causal_mask_matches_printed_example():
+    gold = np.array([[int(x) for x in r] for r in _golden_rows("causal_mask_4x4.txt")],
+                    dtype=bool)
+    got = A.allowed_mask(np.arange(4), np.arange(4), causal=True)
+    assert np.array_equal(got, gold)
+
+
+def test_block_mask_granularity_and_partial_blocks():
+    N = 300                                   # 3 blocks, the last one partial
+    bm = np.array([[1, 0, 1], [0, 1, 0], [1, 1, 0]], dtype=np.uint8)
+    got = A.allowed_mask(np.arange(N), np.arange(N), block_mask=bm)
+    for i in range(0, N, 7):
+        for j in range(0, N, 5):
+            assert got[i, j] == bool(bm[i // 128, j // 128])
+
+
+def test_block_mask_equals_key_truncation():
+    # A row whose only kept block is (0, 0) attends exactly keys 0..127:
+    # identical to running the definition on the truncated key set.
+    N, d = 260, 8
+    q, k, v = _rand((N, d), 1), _rand((N, d), 2), _rand((N, d), 3)
+    bm = np.zeros((3, 3), dtype=np.uint8)
+    bm[0, 0] = 1
+    bm[1, :] = 1
+    bm[2, 2] = 1
+    O, L = _fwd(q, k, v, scale=0.3, block_mask=bm)
+    Ot, Lt = _fwd(q[:128], k[:128], v[:128], scale=0.3)
+    np.testing.assert_allclose(O[:128], Ot, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(L[:128], Lt, rtol=1e-12, atol=1e-12)
+    # last block row attends only keys 256..259
+    O2, L2 = _fwd(q[256:], k[256:], v[256:], scale=0.3)
+    np.testing.assert_allclose(O[256:], O2, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------- softmax / forward --
+
+def test_probability_rows_sum_to_one():
+    N, d = 37, 16
+    q, k, v = _rand((N, d), 4), _rand((N, d), 5), _rand((N, d), 6)
+    for kw in (dict(), dict(causal=True), dict(key_len=20)):
+        hd = A._Head(q, k, v, 0.25, kw.get("causal", False), kw.get("key_len"),
+                     None, 0.0, 0, 0, 0)
+        _, P, _, _ = hd.chunk(np.arange(N))
+        np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-13)
+
+
+def test_constant_values_give_constant_output():
+    N, d = 29, 8
+    q, k = _rand((N, d), 7), _rand((N, d), 8)
+    v = np.tile(np.linspace(-2, 3, d), (N, 1))
+    for causal in (False, True):
+        O, _ = _fwd(q, k, v, scale=0.5, causal=causal)
+        np.testing.assert_allclose(O, v, rtol=0, atol=1e-13)
+
+
+def test_single_key_output_is_value():
+    d = 5
+    q, k, v = _rand((1, d), 9), _rand((1, d), 10), _rand((1, d), 11)
+    O, L = _fwd(q, k, v, scale=0.7)
+    np.testing.assert_allclose(O, v, atol=1e-15)
+    c = float(np.float32(0.7))
+    assert L[0] == pytest.approx(c * float(q[0] @ k[0]), abs=1e-14)
+
+
+def test_two_keys_closed_form():
+    # softmax over two scores is a logistic function of their difference
+    d = 3
+    q, k, v = _rand((2, d), 12), _rand((2, d), 13), _rand((2, d), 14)
+    c = float(np.float32(0.5))
+    O, L = _fwd(q, k, v, scale=0.5)
+    for i in range(2):
+        s0 = c * sum(q[i, t] * k[0, t] for t in range(d))
+        s1 = c * sum(q[i, t] * k[1, t] for t in range(d))
+        w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+        w1 = 1.0 / (1.0 + math.exp(s0 - s1))
+        for t in range(d):
+            assert O[i, t] == pytest.approx(w0 * v[0, t] + w1 * v[1, t], abs=1e-14)
+        hi = max(s0, s1)
+        assert L[i] == pytest.approx(hi + math.log1p(math.exp(-abs(s0 - s1))), abs=1e-14)
+
+
+def test_causal_first_row_is_first_value():
+    N, d = 9, 4
+    q, k, v = _rand((N, d), 15), _rand((N, d), 16), _rand((N, d), 17)
+    O, L = _fwd(q, k, v, scale=1.0, causal=True)
+    np.testing.assert_allclose(O[0], v[0], atol=1e-15)
+    assert L[0] == pytest.approx(float(q[0] @ k[0]), abs=1e-13)
+
+
+def test_library_softmax_and_logsumexp():
+    N, d = 23, 7
+    q, k, v = _rand((N, d), 18), _rand((N, d), 19), _rand((N, d), 20)
+    c = float(np.float32(0.3))
+    S = c * (q @ k.T)
+    O, L = _fwd(q, k, v, scale=0.3)
+    np.testing.assert_allclose(L, scipy.special.logsumexp(S, axis=1), rtol=1e-13)
+    np.testing.assert_allclose(O, scipy.special.softmax(S, axis=1) @ v, atol=1e-13)
+
+
+def test_shift_invariance_of_scores():
+    # adding u to every key adds c*q.u to each row's scores: O is unchanged,
+    # L moves by exactly that amount
+    N, d = 19, 6
+    q, k, v = _rand((N, d), 21), _rand((N, d), 22), _rand((N, d), 23)
+    u = _rand((d,), 24) * 3.0
+    c = float(np.float32(0.4))
+    O1, L1 = _fwd(q, k, v, scale=0.4)
+    O2, L2 = _fwd(q, k + u, v, scale=0.4)
+    np.testing.assert_allclose(O1, O2, atol=1e-12)
+    np.testing.assert_allclose(L2 - L1, c * (q @ u), atol=1e-12)
+
+
+def test_key_permutation_equivariance():
+    N, d = 17, 5
+    q, k, v = _rand((N, d), 25), _rand((N, d), 26), _rand((N, d), 27)
+    perm = np.random.default_rng(28).permutation(N)
+    O1, L1 = _fwd(q, k, v, scale=0.6)
+    O2, L2 = _fwd(q, k[perm], v[perm], scale=0.6)
+    np.testing.assert_allclose(O1, O2, atol=1e-13)
+    np.testing.assert_allclose(L1, L2, atol=1e-13)
+
+
+def _brute_force(q, k, v, c, causal, key_len, p, seed, offset, bh):
+    """Scalar-loop restatement of the definition on a tiny head."""
+    N, d = len(q), len(q[0])
+    T = A.dropout_threshold(p)
+    O = [[0.0] * len(v[0]) for _ in range(N)]
+    L = [0.0] * N
+    for i in range(N):
+        s = []
+        for j in range(N):
+            ok = (not causal or j <= i) and (key_len is None or j < key_len)
+            s.append(c * sum(q[i][t] * k[j][t] for t in range(d)) if ok else None)
+        live = [x for x in s if x is not None]
+        if not live:
+            L[i] = -math.inf
+            continue
+        mx = max(live)
+        tot = sum(math.exp(x - mx) for x in live)
+        L[i] = mx + math.log(tot)
+        for j in range(N):
+            if s[j] is None:
+                continue
+            pij = math.exp(s[j] - L[i])
+            if T:
+                w = philox4x32_10_scalar((j // 4, i, bh, offset),
+                                         (seed & 0xFFFFFFFF, seed >> 32))[j % 4]
+                pij = 0.0 if w < T else pij / (1.0 - float(np.float32(p)))
+            for t in range(len(v[0])):
+                O[i][t] += pij * v[j][t]
+    return np.array(O), np.array(L)
+
+
+@pytest.mark.parametrize("causal,key_len,p", [(False, None, 0.0), (True, None, 0.0),
+                                              (False, 4, 0.0), (True, 5, 0.35),
+                                              (False, None, 0.5)])
+def test_matches_brute_force_loops(causal, key_len, p):
+    N, d = 7, 3
+    q, k, v = _rand((N, d), 30), _rand((N, d), 31), _rand((N, d), 32)
+    seed, offset = 0x1234_5678_9ABC_DEF0, 77
+    O, L = _fwd(q, k, v, scale=0.8, causal=causal,
+                key_lens=None if key_len is None else [key_len],
+                dropout_p=p, seed=seed, offset=offset)
+    Ob, Lb = _brute_force(q.tolist(), k.tolist(), v.tolist(),
+                          float(np.float32(0.8)), causal, key_len, p, seed, offset, 0)
+    np.testing.assert_allclose(O, Ob, atol=1e-13)
+    np.testing.assert_allclose(L, Lb, atol=1e-13)
+
+
+def test_blockwise_recurrence_matches_direct_statistics():
+    # the pages' tiled online softmax reaches the direct row max and exp-sum
+    # for every block size (the blockwise result equals the full softmax)
+    for N in (1, 5, 17, 40):
+        d = 4
+        q, k, v = _rand((N, d), 40 + N), _rand((N, d), 41 + N), _rand((N, d), 42 + N)
+        c = float(np.float32(0.45))
+        O, L = _fwd(q, k, v, scale=0.45)
+        S = c * (q @ k.T)
+        for br in sorted({1, 2, 3, N // 2 or 1, N}):
+            for bc in sorted({1, 4, N}):
+                Ob, m, l = blockwise_forward(q, k, v, c, br, bc)
+                np.testing.assert_allclose(m, S.max(axis=1), rtol=0, atol=1e-14)
+                np.testing.assert_allclose(m + np.log(l), L, atol=1e-12)
+                np.testing.assert_allclose(Ob, O, atol=1e-12)
+
+
+def test_fully_masked_row_is_zero():
+    N, d = 6, 4
+    q, k, v, do = (_rand((N, d), s) for s in (50, 51, 52, 53))
+    O, L, dQ, dK, dV = _bwd(q, k, v, do, scale=0.5, key_lens=[0])
+    assert np.all(O == 0) and np.all(np.isneginf(L))
+    assert np.all(dQ == 0) and np.all(dK == 0) and np.all(dV == 0)
+
+
+def test_shape_walkthrough():
+    g = {r[0]: [float(x) for x in r[1:]] for r in _golden_rows("shape_walkthrough.txt")}
+    B, H, N, d = (int(x) for x in g["q_heads"])
+    rng = np.random.default_rng(54)
+    q, k, v = (rng.standard_normal((B, H, N, d)) for _ in range(3))
+    scale = 1.0 / g["scale_divisor"][0]
+    assert math.sqrt(d) == g["scale_divisor"][0]
+    O, L = A.attention_forward(q, k, v, scale)
+    assert list(O.shape) == [int(x) for x in g["context_heads"]]
+    assert list(L.shape) == [int(x) for x in g["scores"][:3]]
+    hd = A._Head(q[0, 0], k[0, 0], v[0, 0], scale, False, None, None, 0.0, 0, 0, 0)
+    _, P, _, _ = hd.chunk(np.arange(N))
+    assert list(P.shape) == [int(x) for x in g["scores"][2:]]
+    np.testing.assert_allclose(P.sum(axis=1), g["softmax_row_sum"][0], atol=1e-14)
+
+
+def test_dot_product_standard_deviation_of_inputs():
+    import torch
+    import workloads
+    for d_s, std_s in _golden_rows("dot_product_std.txt"):
+        d, std = int(d_s), float(std_s)
+        q, k, _, _ = workloads.random_case(1, 1, 20000, d, seed=d, dtype=torch.float32)
+        dots = (q[0, 0].double() * k[0, 0].double()).sum(-1).numpy()
+        assert abs(dots.std() - std) / std < 0.03
+
+
+# ---------------------------------------------------------------- backward --
+
+def _fd_check(kw, N=6, d=3, seed=60):
+    q, k, v, do = (_rand((N, d), seed + i) for i in range(4))
+    _, _, dQ, dK, dV = _bwd(q, k, v, do, **kw)
+
+    def f(qq, kk, vv):
+        O, _ = _fwd(qq, kk, vv, **kw)
+        return float((O * do).sum())
+
+    h = 1e-6
+    for name, X, G in (("q", q, dQ), ("k", k, dK), ("v", v, dV)):
+        num = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += h
+            Xm[idx] -= h
+            args = {"q": q, "k": k, "v": v}
+            args[name] = Xp
+            fp = f(args["q"], args["k"], args["v"])
+            args[name] = Xm
+            fm = f(args["q"], args["k"], args["v"])
+            num[idx] = (fp - fm) / (2 * h)
+        err = np.linalg.norm(num - G) / max(np.linalg.norm(G), 1e-30)
+        assert err < 1e-6, (name, err)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(scale=0.5),
+    dict(scale=0.7, causal=True),
+    dict(scale=0.3, key_lens=[4]),
+    dict(scale=0.9, causal=True, key_lens=[5], dropout_p=0.3, seed=99, offset=3),
+    dict(scale=0.4, dropout_p=0.5, seed=7),
+])
+def test_gradients_match_finite_differences(kw):
+    _fd_check(kw)
+
+
+def test_gradient_with_block_mask_finite_differences():
+    # N spans two mask blocks so the block mask matters; only a few inputs
+    # are perturbed to keep it quick
+    N, d = 130, 2
+    bm = np.array([[1, 0], [1, 1]], dtype=np.uint8)
+    kw = dict(scale=0.5, block_mask=bm)
+    q, k, v, do = (_rand((N, d), 70 + i) for i in range(4))
+    _, _, dQ, dK, dV = _bwd(q, k, v, do, **kw)
+    h = 1e-6
+    rng = np.random.default_rng(75)
+    for name, X, G in (("q", q, dQ), ("k", k, dK), ("v", v, dV)):
+        for _ in range(6):
+            idx = (int(rng.integers(N)), int(rng.integers(d)))
+            args = {"q": q.copy(), "k": k.copy(), "v": v.copy()}
+            args[name][idx] += h
+            fp = float((_fwd(args["q"], args["k"], args["v"], **kw)[0] * do).sum())
+            args[name][idx] -= 2 * h
+            fm = float((_fwd(args["q"], args["k"], args["v"], **kw)[0] * do).sum())
+            assert (fp - fm) / (2 * h) == pytest.approx(G[idx], rel=1e-5, abs=1e-8)
+
+
+def test_D_identity_with_dropout():
+    N, d = 33, 8
+    q, k, v, do = (_rand((N, d), 80 + i) for i in range(4))
+    hd = A._Head(q, k, v, 0.35, True, 30, None, 0.2, 5, 9, 3)
+    rows = np.arange(N)
+    cols, P, Zs, L = hd.chunk(rows)
+    O = (P * Zs) @ v[cols]
+    dP = (do @ v[cols].T) * Zs
+    np.testing.assert_allclose((do * O).sum(1), (P * dP).sum(1), atol=1e-12)
+
+
+def test_padded_keys_have_zero_gradients():
+    N, d = 20, 4
+    q, k, v, do = (_rand((N, d), 90 + i) for i in range(4))
+    _, _, _, dK, dV = _bwd(q, k, v, do, scale=0.5, key_lens=[13], dropout_p=0.1, seed=1)
+    assert np.all(dK[13:] == 0) and np.all(dV[13:] == 0)
+    assert np.all(np.abs(dK[:13]).sum(1) > 0)
+
+
+def test_sampled_helpers_match_full_evaluation():
+    B, H, N, d = 2, 2, 300, 8
+    rng = np.random.default_rng(100)
+    q, k, v, do = (rng.standard_normal((B, H, N, d)) for _ in range(4))
+    kw = dict(scale=0.35, causal=True, key_lens=[250, 300], dropout_p=0.1, seed=3,
+              offset=2)
+    O, L, dQ, dK, dV = A.attention_backward(q, k, v, do, **kw)
+    rows = np.array([0, 5, 129, 299])
+    Or, Lr = A.forward_rows(q, k, v, 1, 0, rows, **kw)
+    np.testing.assert_allclose(Or, O[1, 0, rows], atol=1e-13)
+    np.testing.assert_allclose(Lr, L[1, 0, rows], atol=1e-13)
+    keys = np.array([0, 127, 128, 249, 260])
+    dKs, dVs = A.backward_keys(q, k, v, do, 0, 1, keys, **kw)
+    np.testing.assert_allclose(dKs, dK[0, 1, keys], atol=1e-12)
+    np.testing.assert_allclose(dVs, dV[0, 1, keys], atol=1e-12)
+
+
+# ----------------------------------------------------------------- dropout --
+
+def test_dropout_threshold_values():
+    assert A.dropout_threshold(0.0) == 0
+    assert A.dropout_threshold(0.5) == 2 ** 31
+    assert A.dropout_threshold(0.25) == 2 ** 30
+    p32 = float(np.float32(0.1))
+    assert A.dropout_threshold(0.1) == math.floor(p32 * 2 ** 32)
+
+
+def test_keep_mask_uses_counter_word_layout():
+    rows = np.array([0, 3, 511])
+    cols = np.array([0, 1, 2, 3, 4, 9, 510])
+    seed, offset, bh = (5 << 32) | 17, 11, 6
+    Z = A.keep_mask(rows, cols, bh, seed, offset, 0.5)
+    for a, i in enumerate(rows):
+        for b, j in enumerate(cols):
+            w = philox4x32_10_scalar((j // 4, i, bh, offset), (17, 5))[j % 4]
+            assert Z[a, b] == (w >= 2 ** 31)
+
+
+def test_keep_fraction_within_binomial_band():
+    p = 0.1
+    Z = A.keep_mask(np.arange(512), np.arange(512), 3, 0, 0, p)
+    n = Z.size
+    keep = Z.mean()
+    sigma = math.sqrt(p * (1 - p) / n)
+    assert abs(keep - (1 - p)) < 5 * sigma
+    assert A.keep_mask(np.arange(4), np.arange(4), 0, 0, 0, 0.0).all()
+
+
+def test_inverted_dropout_is_unbiased():
+    N, d = 12, 3
+    q, k, v = _rand((N, d), 110), _rand((N, d), 111), _rand((N, d), 112)
+    p = 0.3
+    O0, _ = _fwd(q, k, v, scale=0.5)
+    n_seeds = 1500
+    acc = np.zeros_like(O0)
+    for s in range(n_seeds):
+        acc += _fwd(q, k, v, scale=0.5, dropout_p=p, seed=s)[0]
+    mean = acc / n_seeds
+    hd = A._Head(q, k, v, 0.5, False, None, None, 0.0, 0, 0, 0)
+    _, P, _, _ = hd.chunk(np.arange(N))
+    pp = float(np.float32(p))
+    var = (P ** 2) @ (v ** 2) * pp / (1 - pp)           # per-seed variance
+    sigma = np.sqrt(var / n_seeds)
+    assert np.all(np.abs(mean - O0) < 6 * sigma + 1e-12)
+
+
+# ------------------------------------------------------------------ philox --
+
+def test_philox_vector_matches_scalar():
+    rng = np.random.default_rng(120)
+    ctr = rng.integers(0, 2 ** 32, size=(64, 4), dtype=np.uint64)
+    keys = rng.integers(0, 2 ** 32, size=(64, 2), dtype=np.uint64)
+    for c, kk in zip(ctr, keys):
+        vec = philox4x32_10(c[0], c[1], c[2], c[3], int(kk[0]), int(kk[1]))
+        sca = philox4x32_10_scalar(c.tolist(), kk.tolist())
+        assert tuple(int(x) for x in vec) == sca
+
+
+def test_philox_output_bits_are_balanced():
+    n = 1 << 14
+    words = philox4x32_10(np.arange(n), 0, 0, 0, 0x1234, 0x5678)
+    bits = np.unpackbits(np.stack(words).view(np.uint8))
+    assert abs(bits.mean() - 0.5) < 5 * math.sqrt(0.25 / bits.size)
+    # neighbouring counters differ in about half of their bits
+    x = words[0][1:] ^ words[0][:-1]
+    flips = np.unpackbits(x.view(np.uint8)).mean()
+    assert abs(flips - 0.5) < 0.01

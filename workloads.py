@@ -1,0 +1,145 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module only draws random numbers and builds masks; it holds none of the
+attention arithmetic.  Tests (GPU path and oracle alike) and bench.py take
+their inputs from here, so both sides always see the same values.
+
+Workloads (shapes of the pages' benchmarks, data synthetic):
+  single-head-fp32    B=1,  H=1,  N=256,  d=64,  fp32, forward only
+  bert-large          B=16, H=16, N=512,  d=64,  bf16, key padding
+                      lengths ~ U{256..512} (seed 1), dropout p=0.1
+                      (Philox seed 0, offset 0), non-causal
+  gpt2-1k             B=8,  H=12, N=1024, d=64,  bf16, causal
+  gpt2-4k             B=2,  H=12, N=4096, d=64,  bf16, causal
+  long-causal-<N>     B=1,  H=16, d=128, N in {512..16384}, entries
+                      N(0, 0.5^2), causal
+  block-sparse-64k    B=1,  H=8,  N=65536, d=64, 128x128 block mask with
+                      the diagonal and block column 0 kept and the other
+                      blocks kept with Bernoulli(q) so the density is ~0.1
+
+Q, K, V, dO are i.i.d. normal fp32 draws from a CPU torch.Generator seeded
+with 0, in the order Q, K, V, dO, scaled by the workload's std and rounded to
+the workload's dtype.
+"""
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional
+
+import torch
+
+BLOCK = 128
+LONG_SWEEP = (512, 1024, 2048, 4096, 8192, 16384)
+
+
+@dataclass
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    dtype: str = "bf16"          # "bf16" or "fp32"
+    causal: bool = False
+    std: float = 1.0
+    key_len_range: Optional[tuple] = None   # (lo, hi) inclusive, seed 1
+    dropout_p: float = 0.0
+    philox_seed: int = 0
+    philox_offset: int = 0
+    block_density: Optional[float] = None   # block-sparse target density
+    fwd_only: bool = False
+    seed: int = 0
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def scale(self):
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "fp32" else torch.bfloat16
+
+
+def _all():
+    w = {
+        "single-head-fp32": Workload("single-head-fp32", 1, 1, 256, 64,
+                                     dtype="fp32", fwd_only=True),
+        "bert-large": Workload("bert-large", 16, 16, 512, 64,
+                               key_len_range=(256, 512), dropout_p=0.1),
+        "gpt2-1k": Workload("gpt2-1k", 8, 12, 1024, 64, causal=True),
+        "gpt2-4k": Workload("gpt2-4k", 2, 12, 4096, 64, causal=True),
+        "block-sparse-64k": Workload("block-sparse-64k", 1, 8, 65536, 64,
+                                     block_density=0.1),
+    }
+    for n in LONG_SWEEP:
+        name = f"long-causal-{n}"
+        w[name] = Workload(name, 1, 16, n, 128, causal=True, std=0.5)
+    return w
+
+
+WORKLOADS = _all()
+
+
+def get(name, **overrides):
+    """A workload by name, optionally with fields replaced (e.g. a smaller N)."""
+    base = WORKLOADS[name]
+    if not overrides:
+        return base
+    kw = dict(base.__dict__)
+    kw.update(overrides)
+    return Workload(**kw)
+
+
+def make_block_mask(nb, density, seed=0):
+    """uint8 [nb, nb]: diagonal and block column 0 kept, the rest Bernoulli(q).
+
+    q is chosen so that the expected fraction of kept blocks is `density`:
+    q = (density*nb^2 - (2nb - 1)) / (nb^2 - (2nb - 1)).
+    """
+    g = torch.Generator().manual_seed(seed)
+    forced = 2 * nb - 1 if nb > 1 else 1
+    total = nb * nb
+    q = max(0.0, (density * total - forced) / max(1, total - forced))
+    m = (torch.rand((nb, nb), generator=g) < q)
+    m |= torch.eye(nb, dtype=torch.bool)
+    m[:, 0] = True
+    return m.to(torch.uint8)
+
+
+def make_inputs(w: Workload):
+    """Draw the workload's tensors on the CPU.
+
+    Returns a dict with q, k, v, do ([B, H, N, d] in the workload dtype; do is
+    None for forward-only workloads), key_lens (int32 [B] or None),
+    block_mask (uint8 [nb, nb] or None) and the scalar settings.
+    """
+    g = torch.Generator().manual_seed(w.seed)
+    shape = (w.B, w.H, w.N, w.d)
+
+    def draw():
+        return (torch.randn(shape, generator=g, dtype=torch.float32) * w.std
+                ).to(w.torch_dtype)
+
+    q, k, v = draw(), draw(), draw()
+    do = None if w.fwd_only else draw()
+    key_lens = None
+    if w.key_len_range is not None:
+        lo, hi = w.key_len_range
+        gl = torch.Generator().manual_seed(1)
+        key_lens = torch.randint(lo, hi + 1, (w.B,), generator=gl,
+                                 dtype=torch.int64).to(torch.int32)
+    block_mask = None
+    if w.block_density is not None:
+        nb = (w.N + BLOCK - 1) // BLOCK
+        block_mask = make_block_mask(nb, w.block_density, seed=0)
+    return dict(q=q, k=k, v=v, do=do, key_lens=key_lens,
+                block_mask=block_mask, scale=w.scale, causal=w.causal,
+                dropout_p=w.dropout_p, seed=w.philox_seed,
+                offset=w.philox_offset)
+
+
+def random_case(B, H, N, d, seed, dtype=torch.bfloat16, std=1.0):
+    """Small i.i.d. normal q, k, v, do for edge-case tests."""
+    g = torch.Generator().manual_seed(seed)
+    shape = (B, H, N, d)
+    return [(torch.randn(shape, generator=g) * std).to(dtype) for _ in range(4)]
