@@ -1,0 +1,460 @@
+"""Benchmark: attention forward + backward TFLOPS on GB300.
+
+One step = the whole hot path on one batch: the fused forward (O, L) and the
+backward (D preprocess, fused recomputing backward, dQ conversion), plus the
+block-mask compaction when the workload has a mask.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...     (the fp64 CPU oracle, timed)
+
+With N > 1 (launched by torch.distributed.run, one rank per GPU) every rank
+runs its own replica of the workload (weak scaling; attention over
+independent heads needs no exchange), the ranks meet at a barrier around the
+timed region and the slowest rank's time counts.
+"""
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "attention fwd+bwd TFLOPS (bf16, causal/non-causal) & % of GB300 dense BF16 peak"
+SPEC_BF16_TFLOPS = 2250.0
+L2_BYTES = 129 * 2 ** 20
+SECONDARY = ("long-causal-16384",)
+# DRAM bytes per launch of the backward main kernel, from the ncu capture in
+# profiles/ (None until a capture of the current kernel exists)
+BWD_MAIN_TRAFFIC = {}
+
+
+# ----------------------------------------------------------------- FLOPs --
+
+def fwd_flops(w, key_lens=None, block_mask=None):
+    """Algorithmic forward FLOPs: 4 d per allowed (query, key) pair.
+
+    Causal counts N^2/2 per head, key padding N*len_b, block-sparse the kept
+    128x128 blocks (clipped to N).
+    """
+    N, d = w.N, w.d
+    if block_mask is not None:
+        nb = block_mask.shape[-1]
+        sizes = torch.full((nb,), 128.0)
+        sizes[-1] = N - 128 * (nb - 1)
+        bm = block_mask.double()
+        pairs = float((sizes[:, None] * sizes[None, :] * bm).sum()) * w.B * w.H
+    elif key_lens is not None:
+        pairs = float(N * key_lens.double().sum()) * w.H
+    elif w.causal:
+        pairs = N * N / 2.0 * w.B * w.H
+    else:
+        pairs = float(N) * N * w.B * w.H
+    return 4.0 * d * pairs
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p["bf16_tflops"], p["bf16_tflops_sustained"], p["hbm_gbs"], "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- GPU arm --
+
+class Step:
+    """One forward + backward through the C interface, stage by stage."""
+
+    def __init__(self, ea, inp, dev):
+        from exact_attention_12_gb300 import _abi
+        self.abi = _abi
+        self.lib = _abi.lib()
+        self.dev = dev
+        self.q, self.k, self.v, self.do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+        self.key_lens = None if inp["key_lens"] is None else inp["key_lens"].to(dev)
+        self.block_mask = None if inp["block_mask"] is None else inp["block_mask"].to(dev)
+        self.p = ea.make_params(self.q, scale=inp["scale"], causal=inp["causal"],
+                                key_lens=self.key_lens, dropout_p=inp["dropout_p"],
+                                seed=inp["seed"], offset=inp["offset"],
+                                block_mask=self.block_mask)
+        B, H, N, d = self.q.shape
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        nbytes = max(ea.workspace_size(self.p, True), ea.workspace_size(self.p, False))
+        self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        self.launches = 1 + 3 + (2 if self.block_mask is not None else 0)
+
+    def run(self, stream, ev=None):
+        """Enqueue the step; `ev` = 4 events around fwd / preprocess / main / dq."""
+        lib, P, s = self.lib, ctypes.byref(self.p), ctypes.c_void_p(stream.cuda_stream)
+        wsp, wsn = self.ws.data_ptr(), self.ws.numel()
+        if ev:
+            ev[0].record(stream)
+        st = lib.attn_fwd(P, self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
+                          self.o.data_ptr(), self.lse.data_ptr(), wsp, wsn, s)
+        self.abi.check_status(st, "attn_fwd")
+        if ev:
+            ev[1].record(stream)
+        st = lib.attn_bwd_preprocess(P, self.o.data_ptr(), self.do.data_ptr(), wsp, wsn, s)
+        self.abi.check_status(st, "attn_bwd_preprocess")
+        if ev:
+            ev[2].record(stream)
+        st = lib.attn_bwd_main(P, self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
+                               self.lse.data_ptr(), self.do.data_ptr(), self.dk.data_ptr(),
+                               self.dv.data_ptr(), wsp, wsn, s)
+        self.abi.check_status(st, "attn_bwd_main")
+        if ev:
+            ev[3].record(stream)
+        st = lib.attn_bwd_dq(P, self.dq.data_ptr(), wsp, wsn, s)
+        self.abi.check_status(st, "attn_bwd_dq")
+        if ev:
+            ev[4].record(stream)
+
+    def bytes_resident(self):
+        t = [self.q, self.k, self.v, self.do, self.o, self.lse, self.dq, self.dk, self.dv, self.ws]
+        return sum(x.numel() * x.element_size() for x in t)
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def _max_over_ranks(dist, x, dev):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measure_device(ea, w, dev, steps, warmup, dist=None, sample_clocks=True):
+    """Device-resident timing of `steps` steps; returns a dict of results."""
+    inp = workloads.make_inputs(w)
+    first = Step(ea, inp, dev)
+    # rotate input sets so consecutive steps do not find their data in L2
+    nsets = max(1, min(8, math.ceil(2 * L2_BYTES / max(1, first.bytes_resident()))))
+    sets = [first] + [Step(ea, inp, dev) for _ in range(nsets - 1)]
+    stream = torch.cuda.current_stream(dev)
+    for i in range(warmup):
+        sets[i % nsets].run(stream)
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    _barrier(dist)
+    torch.cuda.synchronize(dev)
+    if sample_clocks:
+        sampler.__enter__()
+        time.sleep(0.3)       # let the sampler start before the timed region
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        sets[i % nsets].run(stream, evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    _barrier(dist)
+    if sample_clocks:
+        sampler.__exit__()
+    ea.check(first.ws, dev)
+    total_ms = _max_over_ranks(dist, start.elapsed_time(end), dev)
+    stage = [sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
+             for j in range(4)]
+    flops_f = fwd_flops(w, inp["key_lens"], inp["block_mask"])
+    return dict(inp=inp, total_ms=total_ms, ms_per_step=total_ms / steps, stage_ms=stage,
+                fwd_flops=flops_f, bwd_flops=2.5 * flops_f, nsets=nsets,
+                resident_bytes=first.bytes_resident(), launches=first.launches * steps,
+                clocks=sampler.summary() if sample_clocks else None)
+
+
+def measure_e2e(ea, w, dev, steps, warmup):
+    """Same metric through the Python API with host (pinned) inputs and outputs."""
+    inp = workloads.make_inputs(w)
+    host = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
+    kl = None if inp["key_lens"] is None else inp["key_lens"].to(dev)
+    bm = None if inp["block_mask"] is None else inp["block_mask"].to(dev)
+    kw = dict(scale=inp["scale"], causal=inp["causal"], key_lens=kl, dropout_p=inp["dropout_p"],
+              seed=inp["seed"], offset=inp["offset"], block_mask=bm)
+    outs = [torch.empty(inp["q"].shape, dtype=inp["q"].dtype).pin_memory() for _ in range(3)]
+
+    def step():
+        q, k, v, do = (host[n].to(dev, non_blocking=True) for n in ("q", "k", "v", "do"))
+        o, lse = ea.attention_fwd(q, k, v, **kw)
+        dq, dk, dv = ea.attention_bwd(do, q, k, v, o, lse, **kw)
+        for dst, src in zip(outs, (dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize(dev)
+    dt = (time.perf_counter() - t0) / steps
+    flops = 3.5 * fwd_flops(w, inp["key_lens"], inp["block_mask"])
+    h2d = sum(host[n].numel() * host[n].element_size() for n in host)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
+
+
+# ---------------------------------------------------------- oracle (CPU) --
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else os.cpu_count()
+    except ImportError:
+        return os.cpu_count()
+
+
+def oracle_sample(w, inp, budget_s, max_heads=None):
+    """Time the oracle's fwd+bwd on (b, h) heads until `budget_s` has passed."""
+    import numpy as np
+    from oracle import attention as oracle
+    q, k, v, do = (inp[n] for n in ("q", "k", "v", "do"))
+    kl = inp["key_lens"]
+    bm = inp["block_mask"]
+    kw = dict(scale=inp["scale"], causal=inp["causal"],
+              key_lens=None if kl is None else kl.numpy(),
+              block_mask=None if bm is None else bm.numpy(),
+              dropout_p=inp["dropout_p"], seed=inp["seed"], offset=inp["offset"])
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    done, flops = 0, 0.0
+    t0 = time.perf_counter()
+    for b, h in heads:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        qs, ks, vs, dos = (x[sl].double().numpy() for x in (q, k, v, do))
+        kws = dict(kw)
+        if kl is not None:
+            kws["key_lens"] = np.asarray(kw["key_lens"])[b:b + 1]
+        oracle.attention_backward(qs, ks, vs, dos, **kws)
+        done += 1
+        wh = workloads.get(w.name, B=1, H=1)
+        flops += 3.5 * fwd_flops(wh, None if kl is None else kl[b:b + 1],
+                                 None if bm is None else bm)
+        if time.perf_counter() - t0 > budget_s or (max_heads and done >= max_heads):
+            break
+    dt = time.perf_counter() - t0
+    return flops, dt, done
+
+
+def run_reference(args, w):
+    """The reference arm: the fp64 CPU oracle, as it stands, on host cores."""
+    inp = workloads.make_inputs(w)
+    for _ in range(args.warmup):
+        oracle_sample(w, inp, 0.0, max_heads=1)
+    times, flops = [], 0.0
+    for _ in range(args.steps):
+        f, dt, _ = oracle_sample(w, inp, 0.0, max_heads=1)
+        times.append(dt)
+        flops = f
+    per = sum(times) / len(times)
+    value = flops / per / 1e12
+    cores = _blas_threads()
+    sample = f"one (b, h) head of {w.name} per step, fp64 numpy fwd+bwd"
+    line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(w), "parallelism": "none (host cores)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def describe(w):
+    parts = [f"{w.name}: B={w.B} H={w.H} N={w.N} d={w.d} {w.dtype}"]
+    parts.append("causal" if w.causal else "non-causal")
+    if w.key_len_range:
+        parts.append(f"key lengths U{{{w.key_len_range[0]}..{w.key_len_range[1]}}}")
+    if w.dropout_p:
+        parts.append(f"dropout p={w.dropout_p}")
+    if w.block_density:
+        parts.append(f"block-sparse 128x128, density ~{w.block_density}")
+    return ", ".join(parts)
+
+
+# -------------------------------------------------------------------- main --
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="bert-large")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing")
+    args = ap.parse_args()
+    w = workloads.get(args.workload)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w)
+        return
+
+    # the oracle is timed before any GPU work so that its BLAS threads start
+    # in a process that has not touched CUDA yet
+    cpu = None
+    if rank == 0 and world == 1:
+        inp_cpu = workloads.make_inputs(w)
+        f, dt, heads = oracle_sample(w, inp_cpu, args.cpu_budget)
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOPS", "cores": _blas_threads(),
+               "kind": "oracle",
+               "sample": f"{heads} of {w.B * w.H} (b, h) heads of {w.name}, fp64 numpy fwd+bwd, "
+                         f"{dt:.1f} s"}
+        del inp_cpu
+
+    dist = None
+    if world > 1:
+        import torch.distributed as td
+        td.init_process_group("nccl")
+        dist = td
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    import exact_attention_12_gb300 as ea
+    from exact_attention_12_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if dist is not None:
+        dist.barrier()
+
+    r = measure_device(ea, w, dev, args.steps, args.warmup, dist)
+    ms = r["ms_per_step"]
+    flops_step = r["fwd_flops"] + r["bwd_flops"]
+    value = world * flops_step / (ms * 1e-3) / 1e12
+    burst, sustained, hbm, src = peaks()
+    fwd_ms, pre_ms, main_ms, dq_ms = r["stage_ms"]
+    main_tflops = r["bwd_flops"] / (main_ms * 1e-3) / 1e12
+    traffic = BWD_MAIN_TRAFFIC.get(w.name)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": describe(w), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "dropout_p": w.dropout_p,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs rotate over {r['nsets']} resident sets of "
+                         f"{r['resident_bytes'] / 2**20:.0f} MiB (> 2x the 129 MB L2)"},
+        "fwd_tflops": r["fwd_flops"] / (fwd_ms * 1e-3) / 1e12,
+        "bwd_tflops": r["bwd_flops"] / ((pre_ms + main_ms + dq_ms) * 1e-3) / 1e12,
+        "stage_ms": {"fwd": fwd_ms, "bwd_preprocess": pre_ms, "bwd_main": main_ms,
+                     "bwd_dq": dq_ms},
+        "pct_of_peak": {"of_measured_sustained": 100 * value / world / sustained,
+                        "of_spec_2250": 100 * value / world / SPEC_BF16_TFLOPS},
+        "roofline": {"kernel": "bwd_bf16_kernel", "bound": "tensor", "achieved": main_tflops,
+                     "peak": sustained, "unit": "TFLOP/s", "frac": main_tflops / sustained,
+                     "peak_source": f"bf16_tflops_sustained ({src})", "traffic": traffic},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    line["e2e"] = measure_e2e(ea, w, dev, max(3, min(args.steps, 100)), 3)
+    if not args.no_secondary and world == 1:
+        sec = []
+        for name in SECONDARY:
+            ws = workloads.get(name)
+            rs = measure_device(ea, ws, dev, max(10, args.steps // 20), 5, None,
+                                sample_clocks=False)
+            f_ms, p_ms, m_ms, d_ms = rs["stage_ms"]
+            tot = rs["fwd_flops"] + rs["bwd_flops"]
+            sec.append({"workload": describe(ws),
+                        "fwd_bwd_tflops": tot / (rs["ms_per_step"] * 1e-3) / 1e12,
+                        "fwd_tflops": rs["fwd_flops"] / (f_ms * 1e-3) / 1e12,
+                        "bwd_tflops": rs["bwd_flops"] / ((p_ms + m_ms + d_ms) * 1e-3) / 1e12,
+                        "ms_per_step": rs["ms_per_step"]})
+        line["secondary"] = sec
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,146 @@
+"""Python binding of the C interface: argument marshalling only.
+
+Every step of the computation runs in the CUDA library; this module checks
+tensor shapes/devices, fills `attn_params`, allocates outputs and the
+workspace with torch, and calls `attn_fwd` / `attn_bwd` on the current
+stream.
+"""
+
+import ctypes
+import math
+
+import torch
+
+from . import _abi
+from ._abi import AttnParams, check_status, lib
+
+_DTYPES = {torch.bfloat16: _abi.ATTN_BF16, torch.float32: _abi.ATTN_FP32}
+_workspaces = {}
+
+
+def workspace(device, nbytes):
+    """A zero-initialised device workspace of at least `nbytes`, cached per device.
+
+    The cached buffer is shared by every call on that device that does not
+    pass its own workspace, so calls that overlap on different streams must
+    pass separate workspaces.
+    """
+    key = torch.device(device).index
+    t = _workspaces.get(key)
+    if t is None or t.numel() < nbytes:
+        t = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+        _workspaces[key] = t
+    return t
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def make_params(q, *, scale=None, causal=False, key_lens=None, dropout_p=0.0, seed=0,
+                offset=0, block_mask=None):
+    """Fill `attn_params` from the query tensor and the options."""
+    if q.dim() != 4:
+        raise ValueError("tensors must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    if q.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    p = AttnParams()
+    p.B, p.H, p.N, p.d = B, H, N, d
+    p.dtype = _DTYPES[q.dtype]
+    p.scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    p.causal = 1 if causal else 0
+    p.dropout_p = float(dropout_p)
+    p.philox_seed = int(seed) & 0xFFFFFFFFFFFFFFFF
+    p.philox_offset = int(offset)
+    sb, sh, sn, sd = q.stride()
+    if sd != 1 and d > 1:
+        raise ValueError("the head dimension must be contiguous")
+    p.stride_b, p.stride_h, p.stride_n = sb, sh, sn
+    if key_lens is not None:
+        if key_lens.dtype != torch.int32 or key_lens.device != q.device or key_lens.numel() != B:
+            raise ValueError("key_lens must be an int32 tensor [B] on the tensors' device")
+        p.key_lens = key_lens.data_ptr()
+    if block_mask is not None:
+        nb = (N + 127) // 128
+        if block_mask.dtype != torch.uint8 or block_mask.device != q.device:
+            raise ValueError("block_mask must be uint8 on the tensors' device")
+        if not block_mask.is_contiguous():
+            raise ValueError("block_mask must be contiguous")
+        if tuple(block_mask.shape) == (nb, nb):
+            p.block_mask_head_stride = 0
+        elif tuple(block_mask.shape) == (B, H, nb, nb):
+            p.block_mask_head_stride = nb * nb
+        else:
+            raise ValueError(f"block_mask must be [{nb}, {nb}] or [B, H, {nb}, {nb}]")
+        p.block_mask = block_mask.data_ptr()
+    return p
+
+
+def _same_layout(ref, *ts):
+    for t in ts:
+        if t.shape != ref.shape or t.stride() != ref.stride() or t.device != ref.device \
+                or t.dtype != ref.dtype:
+            raise ValueError("all attention tensors must share shape, strides, dtype and device")
+
+
+def _like(t):
+    return torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, device=t.device)
+
+
+def workspace_size(params, backward):
+    n = lib().attn_workspace_size(ctypes.byref(params), 1 if backward else 0)
+    if n == 0:
+        check_status(_abi.ATTN_ERR_INVALID_ARG, "attn_workspace_size")
+    return n
+
+
+def attention_fwd(q, k, v, *, scale=None, causal=False, key_lens=None, dropout_p=0.0, seed=0,
+                  offset=0, block_mask=None, out=None, lse=None, ws=None):
+    """O and the per-row logsumexp L of exact attention (see include/attn.h).
+
+    q, k, v: [B, H, N, d] CUDA tensors (bf16 or fp32) with identical strides.
+    Returns (o, lse) with o like q and lse fp32 [B, H, N].
+    """
+    _same_layout(q, k, v)
+    p = make_params(q, scale=scale, causal=causal, key_lens=key_lens, dropout_p=dropout_p,
+                    seed=seed, offset=offset, block_mask=block_mask)
+    o = _like(q) if out is None else out
+    _same_layout(q, o)
+    B, H, N, _ = q.shape
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    w = workspace(q.device, workspace_size(p, False)) if ws is None else ws
+    st = lib().attn_fwd(ctypes.byref(p), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                        lse.data_ptr(), w.data_ptr(), w.numel() * w.element_size(),
+                        _stream(q.device))
+    check_status(st, "attn_fwd")
+    return o, lse
+
+
+def attention_bwd(dout, q, k, v, o, lse, *, scale=None, causal=False, key_lens=None,
+                  dropout_p=0.0, seed=0, offset=0, block_mask=None, dq=None, dk=None, dv=None,
+                  ws=None):
+    """dQ, dK, dV of exact attention given the forward's o and lse (bf16)."""
+    _same_layout(q, k, v, o, dout)
+    p = make_params(q, scale=scale, causal=causal, key_lens=key_lens, dropout_p=dropout_p,
+                    seed=seed, offset=offset, block_mask=block_mask)
+    dq = _like(q) if dq is None else dq
+    dk = _like(q) if dk is None else dk
+    dv = _like(q) if dv is None else dv
+    _same_layout(q, dq, dk, dv)
+    w = workspace(q.device, workspace_size(p, True)) if ws is None else ws
+    st = lib().attn_bwd(ctypes.byref(p), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                        lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                        dv.data_ptr(), w.data_ptr(), w.numel() * w.element_size(),
+                        _stream(q.device))
+    check_status(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def check(ws=None, device=None):
+    """Synchronise the current stream and raise if a kernel recorded a time-out."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    w = workspace(dev, 256) if ws is None else ws
+    st = lib().attn_check(w.data_ptr(), _stream(dev))
+    check_status(st, "attn_check")

@@ -1,0 +1,392 @@
+// Host side of the C interface declared in include/attn.h: argument
+// validation, workspace layout, TMA tensor-map encoding and kernel launches.
+// Nothing here allocates device memory.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "attn.h"
+#include "attn_kernels.cuh"
+
+namespace {
+
+using attn::kTile;
+
+thread_local std::string g_last_error;
+
+attn_status fail(attn_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+attn_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr size_t kHeaderBytes = 256;   // status words
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+  size_t list_cnt = 0, list_idx = 0;   // compacted block mask (0 = none)
+  size_t dsum = 0, dq_acc = 0;         // backward only
+  size_t total = 0;
+};
+
+int num_masks(const attn_params* p) {
+  return p->block_mask_head_stride != 0 ? p->B * p->H : 1;
+}
+
+WsLayout layout(const attn_params* p, bool bwd) {
+  WsLayout L;
+  size_t off = kHeaderBytes;
+  const size_t nb = (static_cast<size_t>(p->N) + kTile - 1) / kTile;
+  const size_t bhn = static_cast<size_t>(p->B) * p->H * p->N;
+  if (p->block_mask != nullptr && p->dtype == ATTN_BF16) {
+    const size_t masks = static_cast<size_t>(num_masks(p));
+    L.list_cnt = off;
+    off = round_up(off + masks * nb * sizeof(int32_t), 256);
+    L.list_idx = off;
+    off = round_up(off + masks * nb * nb * sizeof(uint16_t), 256);
+  }
+  if (bwd) {
+    L.dsum = off;
+    off = round_up(off + bhn * sizeof(float), 256);
+    L.dq_acc = off;
+    off = round_up(off + bhn * p->d * sizeof(float), 256);
+  }
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+attn_status validate(const attn_params* p, bool bwd) {
+  if (p == nullptr) return fail(ATTN_ERR_INVALID_ARG, "params is NULL");
+  if (p->B < 0 || p->H < 0 || p->N < 0)
+    return fail(ATTN_ERR_INVALID_ARG, "negative shape B=%d H=%d N=%d", p->B, p->H, p->N);
+  if (p->d != 64 && p->d != 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", p->d);
+  if (p->dtype != ATTN_BF16 && p->dtype != ATTN_FP32)
+    return fail(ATTN_ERR_INVALID_ARG, "dtype %d", p->dtype);
+  if (bwd && p->dtype != ATTN_BF16)
+    return fail(ATTN_ERR_UNSUPPORTED, "backward is implemented for bf16 only");
+  if (!std::isfinite(p->scale) || !(p->scale > 0.f))
+    return fail(ATTN_ERR_INVALID_ARG, "scale must be positive and finite (got %g)", p->scale);
+  if (!(p->dropout_p >= 0.f && p->dropout_p < 1.f))
+    return fail(ATTN_ERR_INVALID_ARG, "dropout_p must be in [0, 1) (got %g)", p->dropout_p);
+  if (p->philox_offset >= (1ull << 32))
+    return fail(ATTN_ERR_INVALID_ARG, "philox_offset must be < 2^32");
+  if (static_cast<int64_t>(p->N) > (int64_t{1} << 30))
+    return fail(ATTN_ERR_UNSUPPORTED, "N=%d too large", p->N);
+  if (p->block_mask != nullptr) {
+    if (p->block_mask_head_stride < 0)
+      return fail(ATTN_ERR_INVALID_ARG, "negative block_mask_head_stride");
+    if ((p->N + kTile - 1) / kTile > 65535)
+      return fail(ATTN_ERR_UNSUPPORTED, "block mask with more than 65535 blocks per side");
+    if (num_masks(p) > 65535)
+      return fail(ATTN_ERR_UNSUPPORTED, "more than 65535 per-head block masks");
+  }
+  const int64_t align = p->dtype == ATTN_BF16 ? 8 : 4;   // elements per 16 bytes
+  const int64_t st[3] = {p->stride_b, p->stride_h, p->stride_n};
+  for (int i = 0; i < 3; ++i) {
+    if (st[i] <= 0 || st[i] % align != 0)
+      return fail(ATTN_ERR_INVALID_ARG,
+                  "strides must be positive multiples of %lld elements (b=%lld h=%lld n=%lld)",
+                  static_cast<long long>(align), static_cast<long long>(p->stride_b),
+                  static_cast<long long>(p->stride_h), static_cast<long long>(p->stride_n));
+  }
+  if (p->stride_n < p->d) return fail(ATTN_ERR_INVALID_ARG, "stride_n < d");
+  return ATTN_OK;
+}
+
+attn_status check_ptrs(std::initializer_list<const void*> ptrs) {
+  int i = 0;
+  for (const void* ptr : ptrs) {
+    if (ptr == nullptr) return fail(ATTN_ERR_INVALID_ARG, "tensor argument %d is NULL", i);
+    if (!aligned16(ptr)) return fail(ATTN_ERR_INVALID_ARG, "tensor argument %d is not 16-byte aligned", i);
+    ++i;
+  }
+  return ATTN_OK;
+}
+
+attn_status check_ws(const attn_params* p, bool bwd, const void* ws, size_t ws_bytes) {
+  const size_t need = layout(p, bwd).total;
+  if (ws == nullptr) return fail(ATTN_ERR_WORKSPACE, "workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(ATTN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  return ATTN_OK;
+}
+
+// ------------------------------------------------------------ tensor maps --
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// [B, H, N, d] tensor with element strides; boxes of `box_cols` x 128 rows.
+attn_status make_map(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, int elem_bytes,
+                     int B, int H, int N, int d, int64_t sb, int64_t sh, int64_t sn, int box_cols,
+                     CUtensorMapSwizzle swz) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(sn * elem_bytes),
+                                 static_cast<cuuint64_t>(sh * elem_bytes),
+                                 static_cast<cuuint64_t>(sb * elem_bytes)};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(kTile), 1, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = enc(map, dt, 4, const_cast<void*>(ptr), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return ATTN_OK;
+}
+
+attn_status make_bf16_map(CUtensorMap* map, const void* ptr, const attn_params* p) {
+  return make_map(map, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->B, p->H, p->N, p->d,
+                  p->stride_b, p->stride_h, p->stride_n, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+attn::MaskArgs mask_args(const attn_params* p, const WsLayout& L, char* ws, bool by_column) {
+  attn::MaskArgs m{};
+  m.B = p->B;
+  m.H = p->H;
+  m.N = p->N;
+  m.causal = p->causal != 0;
+  m.key_lens = p->key_lens;
+  m.nb = (p->N + kTile - 1) / kTile;
+  m.block_mask = p->block_mask;
+  m.block_mask_head_stride = p->block_mask_head_stride;
+  m.mask_per_head = p->block_mask_head_stride != 0;
+  if (L.list_idx != 0) {
+    m.list_cnt = reinterpret_cast<const int32_t*>(ws + L.list_cnt);
+    m.list_idx = reinterpret_cast<const uint16_t*>(ws + L.list_idx);
+  }
+  (void)by_column;
+  const double p32 = static_cast<double>(p->dropout_p);
+  uint32_t T = 0;
+  if (p32 > 0.0) {
+    const double t = std::floor(p32 * 4294967296.0);
+    T = t >= 4294967295.0 ? 0xFFFFFFFFu : static_cast<uint32_t>(t);
+  }
+  m.drop_threshold = T;
+  m.drop_scale = p32 > 0.0 ? static_cast<float>(1.0 / (1.0 - p32)) : 1.0f;
+  m.seed_lo = static_cast<uint32_t>(p->philox_seed & 0xFFFFFFFFull);
+  m.seed_hi = static_cast<uint32_t>(p->philox_seed >> 32);
+  m.offset = static_cast<uint32_t>(p->philox_offset);
+  return m;
+}
+
+bool empty_problem(const attn_params* p) { return p->B == 0 || p->H == 0 || p->N == 0; }
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_workspace_size(const attn_params* p, int for_backward) {
+  if (validate(p, for_backward != 0) != ATTN_OK) return 0;
+  return layout(p, for_backward != 0).total;
+}
+
+attn_status attn_fwd(const attn_params* p, const void* q, const void* k, const void* v, void* o,
+                     float* lse, void* ws, size_t ws_bytes, void* stream) {
+  attn_status st = validate(p, false);
+  if (st != ATTN_OK) return st;
+  if ((st = check_ws(p, false, ws, ws_bytes)) != ATTN_OK) return st;
+  if (empty_problem(p)) return ATTN_OK;
+  if ((st = check_ptrs({q, k, v, o, lse})) != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  const WsLayout L = layout(p, false);
+
+  attn::FwdArgs a{};
+  a.m = mask_args(p, L, w, false);
+  a.d = p->d;
+  a.scale = p->scale;
+  a.scale_log2 = p->scale * kLog2e;
+  a.o = o;
+  a.lse = lse;
+  a.stride_b = p->stride_b;
+  a.stride_h = p->stride_h;
+  a.stride_n = p->stride_n;
+  a.status = reinterpret_cast<int*>(w);
+  a.timeout_ns = kTimeoutNs;
+
+  cudaError_t e;
+  if (p->dtype == ATTN_FP32) {
+    e = attn::launch_fwd_fp32(static_cast<const float*>(q), static_cast<const float*>(k),
+                              static_cast<const float*>(v), a, s);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "forward (fp32) launch");
+  }
+  attn::TensorMaps tm{};
+  if ((st = make_bf16_map(&tm.q, q, p)) != ATTN_OK) return st;
+  if ((st = make_bf16_map(&tm.k, k, p)) != ATTN_OK) return st;
+  if ((st = make_bf16_map(&tm.v, v, p)) != ATTN_OK) return st;
+  if (p->block_mask != nullptr) {
+    e = attn::launch_compact_mask(p->block_mask, p->block_mask_head_stride, num_masks(p), a.m.nb,
+                                  0, reinterpret_cast<int32_t*>(w + L.list_cnt),
+                                  reinterpret_cast<uint16_t*>(w + L.list_idx), s);
+    if (e != cudaSuccess) return cuda_fail(e, "block-mask compaction launch");
+  }
+  e = attn::launch_fwd_bf16(tm, a, s);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "forward launch");
+}
+
+}  // extern "C"
+
+namespace {
+
+// Validation and argument block shared by the backward entry points.
+attn_status bwd_setup(const attn_params* p, void* ws, size_t ws_bytes, attn::BwdArgs* a,
+                      WsLayout* L) {
+  attn_status st = validate(p, true);
+  if (st != ATTN_OK) return st;
+  if ((st = check_ws(p, true, ws, ws_bytes)) != ATTN_OK) return st;
+  char* w = static_cast<char*>(ws);
+  *L = layout(p, true);
+  *a = attn::BwdArgs{};
+  a->m = mask_args(p, *L, w, true);
+  a->d = p->d;
+  a->scale = p->scale;
+  a->scale_log2 = p->scale * kLog2e;
+  a->Dsum = reinterpret_cast<const float*>(w + L->dsum);
+  a->dq_acc = reinterpret_cast<float*>(w + L->dq_acc);
+  a->stride_b = p->stride_b;
+  a->stride_h = p->stride_h;
+  a->stride_n = p->stride_n;
+  a->status = reinterpret_cast<int*>(w);
+  a->timeout_ns = kTimeoutNs;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_bwd_preprocess(const attn_params* p, const void* o, const void* dout, void* ws,
+                                size_t ws_bytes, void* stream) {
+  attn::BwdArgs a;
+  WsLayout L;
+  attn_status st = bwd_setup(p, ws, ws_bytes, &a, &L);
+  if (st != ATTN_OK) return st;
+  if (empty_problem(p)) return ATTN_OK;
+  if ((st = check_ptrs({o, dout})) != ATTN_OK) return st;
+  const cudaError_t e = attn::launch_bwd_preprocess(o, dout, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "backward preprocess launch");
+}
+
+attn_status attn_bwd_main(const attn_params* p, const void* q, const void* k, const void* v,
+                          const float* lse, const void* dout, void* dk, void* dv, void* ws,
+                          size_t ws_bytes, void* stream) {
+  attn::BwdArgs a;
+  WsLayout L;
+  attn_status st = bwd_setup(p, ws, ws_bytes, &a, &L);
+  if (st != ATTN_OK) return st;
+  if (empty_problem(p)) return ATTN_OK;
+  if ((st = check_ptrs({q, k, v, lse, dout, dk, dv})) != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  a.lse = lse;
+  a.dk = dk;
+  a.dv = dv;
+  attn::TensorMaps tm{};
+  if ((st = make_bf16_map(&tm.q, q, p)) != ATTN_OK) return st;
+  if ((st = make_bf16_map(&tm.k, k, p)) != ATTN_OK) return st;
+  if ((st = make_bf16_map(&tm.v, v, p)) != ATTN_OK) return st;
+  if ((st = make_bf16_map(&tm.dout, dout, p)) != ATTN_OK) return st;
+  cudaError_t e;
+  if (p->block_mask != nullptr) {
+    e = attn::launch_compact_mask(p->block_mask, p->block_mask_head_stride, num_masks(p), a.m.nb,
+                                  1, reinterpret_cast<int32_t*>(w + L.list_cnt),
+                                  reinterpret_cast<uint16_t*>(w + L.list_idx), s);
+    if (e != cudaSuccess) return cuda_fail(e, "block-mask compaction launch");
+  }
+  e = attn::launch_bwd_bf16(tm, a, s);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "backward launch");
+}
+
+attn_status attn_bwd_dq(const attn_params* p, void* dq, void* ws, size_t ws_bytes, void* stream) {
+  attn::BwdArgs a;
+  WsLayout L;
+  attn_status st = bwd_setup(p, ws, ws_bytes, &a, &L);
+  if (st != ATTN_OK) return st;
+  if (empty_problem(p)) return ATTN_OK;
+  if ((st = check_ptrs({dq})) != ATTN_OK) return st;
+  const cudaError_t e = attn::launch_dq_convert(dq, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "dQ conversion launch");
+}
+
+attn_status attn_bwd(const attn_params* p, const void* q, const void* k, const void* v,
+                     const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                     void* dv, void* ws, size_t ws_bytes, void* stream) {
+  attn::BwdArgs a;
+  WsLayout L;
+  attn_status st = bwd_setup(p, ws, ws_bytes, &a, &L);
+  if (st != ATTN_OK) return st;
+  if (empty_problem(p)) return ATTN_OK;
+  if ((st = check_ptrs({q, k, v, o, lse, dout, dq, dk, dv})) != ATTN_OK) return st;
+  if ((st = attn_bwd_preprocess(p, o, dout, ws, ws_bytes, stream)) != ATTN_OK) return st;
+  if ((st = attn_bwd_main(p, q, k, v, lse, dout, dk, dv, ws, ws_bytes, stream)) != ATTN_OK)
+    return st;
+  return attn_bwd_dq(p, dq, ws, ws_bytes, stream);
+}
+
+attn_status attn_check(void* ws, void* stream) {
+  if (ws == nullptr) return fail(ATTN_ERR_WORKSPACE, "workspace is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int words[2] = {0, 0};
+  if ((e = cudaMemcpy(words, ws, sizeof(words), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "status read");
+  if (words[0] == 0) return ATTN_OK;
+  if ((e = cudaMemset(ws, 0, sizeof(words))) != cudaSuccess) return cuda_fail(e, "status clear");
+  return fail(static_cast<attn_status>(words[0]), "device status %d at wait site %d", words[0],
+              words[1]);
+}
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device wait timed out";
+    case ATTN_ERR_WORKSPACE: return "bad workspace";
+  }
+  return "unknown status";
+}
+
+const char* attn_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

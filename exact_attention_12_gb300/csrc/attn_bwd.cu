@@ -1,0 +1,593 @@
+// Fused attention backward, bf16, tcgen05 tensor cores.
+//
+// The pages state the idea (FlashAttention paper summary, "Tính toán lại
+// trong lượt lan truyền ngược": store only O and the softmax statistics and
+// recompute S and P block by block on chip in the backward pass); the
+// gradients are the chain rule of the forward definition:
+//   D = rowsum(dO * O), P = exp(S - L), dV = P~^T dO, dP = (dO V^T) * Z/(1-p),
+//   dS = P * (dP - D), dQ = c dS K, dK = c dS^T Q.
+//
+// Kernels:
+//   bwd_preprocess   D = rowsum(dO * O) per query row; zeroes the fp32 dQ
+//                    accumulator.  Memory-bound.
+//   bwd_kernel       one CTA per 128-row key/value tile K_j, V_j of one
+//                    (b, h); loops over the query tiles Q_i that may attend
+//                    it (all, the causal suffix i >= j, or the block mask's
+//                    column list).  Per query tile, five MMAs:
+//                      S^T  = K_j Q_i^T      (TMEM)
+//                      dP^T = V_j dO_i^T     (TMEM)
+//                      dV  += P~^T dO_i      (A = P~^T in TMEM, bf16)
+//                      dK  += dS^T Q_i       (A = dS^T in shared memory)
+//                      dQ_i = dS K_j         (A = the same dS^T buffer read
+//                                             as an MN-major operand)
+//                    dK and dV stay in TMEM for the whole loop; dQ_i is
+//                    drained by four warps into the fp32 accumulator with
+//                    vector atomics.
+//   dq_convert       dQ = c * accumulator -> bf16.
+//
+// Warp roles of bwd_kernel (320 threads):
+//   warps 0-3  "softmax": thread t owns key row t (TMEM lane t): P^T row,
+//              dropout mask, dS^T row; epilogue writes dK, dV.
+//   warps 4-7  dQ drain: thread t owns query row t of the dQ tile.
+//   warp 8     TMA producer (K_j, V_j once; Q_i, dO_i per query tile).
+//   warp 9     MMA issuer, TMEM owner.
+// TMEM columns: S^T [0,128) (P~^T as bf16 over [0,64) once S^T is read),
+//   dP^T [128,256), dV [256,256+d), dK [256+d,256+2d), dQ [384,448) for
+//   d = 64 and over the dP^T columns for d = 128.
+#include <cuda_bf16.h>
+
+#include "attn_kernels.cuh"
+#include "philox.cuh"
+#include "sm103.cuh"
+
+namespace attn {
+using namespace sm103;
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kBoxBytes = kTile * 128;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStages = (D == 64) ? 2 : 1;          // Q_i / dO_i stages
+  static constexpr int kDsBytes = kTile * kTile * 2;          // dS^T tile, bf16
+  static constexpr int kSmem = 1024 + 2 * kTileBytes + 2 * kStages * kTileBytes + kDsBytes;
+  static constexpr uint32_t kSCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 256 + D;
+  static constexpr uint32_t kDQCol = (D == 64) ? 384 : 128;
+  static constexpr bool kDqAliasesDp = (D == 128);
+  static constexpr int kThreads = 320;
+};
+
+template <int ST>
+struct BwdCtl {
+  uint64_t kvfull;
+  uint64_t qfull[ST], qempty[ST];
+  uint64_t sfull, dpfull, pfull, dsfull, dsfree, dqfull, dqfree, done;
+  uint64_t final_bar;
+  float sL[4][kTile];     // per softmax warp: L_i * log2(e) of the query tile
+                          // (+inf: the row contributes nothing)
+  float sD[4][kTile];     // per softmax warp: D_i of the query tile
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct QList {
+  const uint16_t* idx;   // block-mask column list, or null (dense)
+  int first, n;
+  __device__ __forceinline__ int operator[](int t) const {
+    return idx ? int(idx[first + t]) : first + t;
+  }
+};
+
+__device__ __forceinline__ QList bwd_tiles(const MaskArgs& m, int kt, int bh, int limit) {
+  QList t{nullptr, 0, 0};
+  if (kt * kTile >= limit) return t;   // every key of the tile is masked
+  const int first = m.causal ? kt : 0;
+  if (m.list_idx == nullptr) {
+    t.first = first;
+    t.n = m.nb - first;
+    return t;
+  }
+  const size_t col = static_cast<size_t>(m.mask_per_head ? bh : 0) * m.nb + kt;
+  const uint16_t* p = m.list_idx + col * m.nb;
+  const int cnt = m.list_cnt[col];
+  int lo = 0, hi = cnt;   // first entry >= first (the list is sorted)
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (int(p[mid]) < first) lo = mid + 1; else hi = mid;
+  }
+  t.idx = p;
+  t.first = lo;
+  t.n = cnt - lo;
+  return t;
+}
+
+__device__ __forceinline__ int key_limit(const MaskArgs& m, int b) {
+  int limit = m.N;
+  if (m.key_lens != nullptr) limit = min(max(m.key_lens[b], 0), m.N);
+  return limit;
+}
+
+// 16-byte chunk `chunk` (8 bf16) of row `r` in a [128][128] bf16 tile stored
+// as two 64-column boxes with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t ds_offset(int r, int chunk) {
+  const int half = chunk >> 3, c = chunk & 7;
+  return half * (kTile * 128) + r * 128 + ((c ^ (r & 7)) << 4);
+}
+
+template <int D, bool DROPOUT>
+__global__ void __launch_bounds__(320, 1)
+    bwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                    const BwdArgs a) {
+  using C = BwdCfg<D>;
+  constexpr int ST = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = sK + C::kTileBytes;
+  uint8_t* sQ = sV + C::kTileBytes;                 // ST tiles
+  uint8_t* sdO = sQ + ST * C::kTileBytes;           // ST tiles
+  uint8_t* sDS = sdO + ST * C::kTileBytes;          // dS^T [kv][q]
+  __shared__ BwdCtl<ST> ctl;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const MaskArgs& m = a.m;
+  const int BH = m.B * m.H;
+  const int kt = static_cast<int>(blockIdx.x / BH);   // heaviest (earliest) key tiles first
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int b = bh / m.H, h = bh - b * m.H;
+  const int k0 = kt * kTile;
+  const int limit = key_limit(m, b);
+  const QList tiles = bwd_tiles(m, kt, bh, limit);
+  const int n = tiles.n;
+
+  if (threadIdx.x == 0) {
+    ctl.abort_flag = 0;
+    mbar_init(&ctl.kvfull, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&ctl.qfull[s], 1);
+      mbar_init(&ctl.qempty[s], 1);
+    }
+    mbar_init(&ctl.sfull, 1);
+    mbar_init(&ctl.dpfull, 1);
+    mbar_init(&ctl.pfull, 4);
+    mbar_init(&ctl.dsfull, 4);
+    mbar_init(&ctl.dsfree, 1);
+    mbar_init(&ctl.dqfull, 1);
+    mbar_init(&ctl.dqfree, 4);
+    mbar_init(&ctl.done, 1);
+    mbar_init(&ctl.final_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&ctl.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  const WaitCtx wc{&ctl.abort_flag, a.status, a.timeout_ns};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n > 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      tma_prefetch_desc(&tdo);
+      mbar_arrive_expect_tx(&ctl.kvfull, 2 * C::kTileBytes);
+#pragma unroll
+      for (int x = 0; x < C::kBoxes; ++x) {
+        tma_load_4d(sK + x * C::kBoxBytes, &tk, &ctl.kvfull, x * 64, k0, h, b);
+        tma_load_4d(sV + x * C::kBoxBytes, &tv, &ctl.kvfull, x * 64, k0, h, b);
+      }
+      int i = 0;
+      for (; i < n; ++i) {
+        const int s = i % ST;
+        if (i >= ST && !mbar_wait(&ctl.qempty[s], ((i / ST) - 1) & 1, wc, kSiteBwdEmpty)) break;
+        const int q0 = tiles[i] * kTile;
+        mbar_arrive_expect_tx(&ctl.qfull[s], 2 * C::kTileBytes);
+#pragma unroll
+        for (int x = 0; x < C::kBoxes; ++x) {
+          tma_load_4d(sQ + s * C::kTileBytes + x * C::kBoxBytes, &tq, &ctl.qfull[s], x * 64, q0,
+                      h, b);
+          tma_load_4d(sdO + s * C::kTileBytes + x * C::kBoxBytes, &tdo, &ctl.qfull[s], x * 64,
+                      q0, h, b);
+        }
+      }
+      if (ctl.abort_flag) {   // let issued copies land before the CTA exits
+        mbar_wait_drain(&ctl.kvfull, 0, a.timeout_ns);
+        for (int ii = max(0, i - ST); ii < i; ++ii)
+          mbar_wait_drain(&ctl.qfull[ii % ST], (ii / ST) & 1, a.timeout_ns);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------- MMA issue
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);   // K-major x K-major
+      constexpr uint32_t kIdKN = idesc_bf16(128, D, false, true);      // K-major A, MN-major B
+      constexpr uint32_t kIdNN = idesc_bf16(128, D, true, true);       // MN-major A and B
+      const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), ds_base = smem_u32(sDS);
+      bool ok = mbar_wait(&ctl.kvfull, 0, wc, kSiteBwdKV);
+      for (int i = 0; ok && i < n; ++i) {
+        const int s = i % ST;
+        const uint32_t ph = i & 1;
+        const uint32_t q_base = smem_u32(sQ + s * C::kTileBytes);
+        const uint32_t do_base = smem_u32(sdO + s * C::kTileBytes);
+        ok = mbar_wait(&ctl.qfull[s], (i / ST) & 1, wc, kSiteBwdQ);
+        if (!ok) break;
+        tc_fence_after();
+        // S^T = K_j Q_i^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+          mma_ss(tmem + C::kSCol, smem_desc(k_base + off, 16, 1024),
+                 smem_desc(q_base + off, 16, 1024), kIdSS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&ctl.sfull);
+        if (C::kDqAliasesDp && i >= 1) {   // dQ_{i-1} shares the dP^T columns
+          ok = mbar_wait(&ctl.dqfree, (i - 1) & 1, wc, kSiteBwdMma);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // dP^T = V_j dO_i^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+          mma_ss(tmem + C::kDPCol, smem_desc(v_base + off, 16, 1024),
+                 smem_desc(do_base + off, 16, 1024), kIdSS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&ctl.dpfull);
+        // dV += P~^T dO_i
+        ok = mbar_wait(&ctl.pfull, ph, wc, kSiteBwdMma);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + C::kDVCol, tmem + C::kSCol + kk * 8,
+                 smem_desc(do_base + kk * 2048, C::kBoxBytes, 1024), kIdKN,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q_i
+        ok = mbar_wait(&ctl.dsfull, ph, wc, kSiteBwdMma);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+          mma_ss(tmem + C::kDKCol, smem_desc(ds_base + off, 16, 1024),
+                 smem_desc(q_base + kk * 2048, C::kBoxBytes, 1024), kIdKN,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!C::kDqAliasesDp && i >= 1) {
+          ok = mbar_wait(&ctl.dqfree, (i - 1) & 1, wc, kSiteBwdMma);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // dQ_i = dS K_j
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ss(tmem + C::kDQCol, smem_desc(ds_base + kk * 2048, C::kBoxBytes, 1024),
+                 smem_desc(k_base + kk * 2048, C::kBoxBytes, 1024), kIdNN, kk > 0 ? 1u : 0u);
+        mma_commit(&ctl.dqfull);
+        mma_commit(&ctl.dsfree);
+        mma_commit(&ctl.qempty[s]);
+      }
+      if (ok) mma_commit(&ctl.done);
+      mma_commit(&ctl.final_bar);
+      mbar_wait_drain(&ctl.final_bar, 0, a.timeout_ns);
+    }
+  } else if (warp < 4) {
+    // -------------------------------------------- P^T, dS^T; dK/dV epilogue
+    const int r = threadIdx.x;             // key row within the tile == TMEM lane
+    const int kj = k0 + r;                 // global key index
+    const bool key_ok = kj < limit;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float c2 = a.scale_log2;
+    const float ds = m.drop_scale;
+    const float* lse = a.lse + static_cast<int64_t>(bh) * m.N;
+    const float* dsum = a.Dsum + static_cast<int64_t>(bh) * m.N;
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      const uint32_t ph = i & 1;
+      const int qtile = tiles[i];
+      const int q0 = qtile * kTile;
+      {   // each warp stages L (log2 units) and D of the query tile for itself
+        __syncwarp();   // the previous tile's values have been read
+#pragma unroll
+        for (int u = 0; u < kTile / 32; ++u) {
+          const int qq = q0 + u * 32 + lane;
+          float l2 = INFINITY, dv = 0.f;
+          if (qq < m.N) {
+            const float L = lse[qq];
+            l2 = (L == -INFINITY) ? INFINITY : L * kLog2e;
+            dv = dsum[qq];
+          }
+          ctl.sL[warp][u * 32 + lane] = l2;
+          ctl.sD[warp][u * 32 + lane] = dv;
+        }
+        __syncwarp();
+      }
+      const bool diag = m.causal && qtile == kt;   // query q < key: masked
+
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.sfull, ph, wc, kSiteBwdSoft));
+      if (!ok) break;
+      tc_fence_after();
+      // P^T row (bf16 pairs kept for dS), P~^T into TMEM columns [0, 64)
+      uint32_t pp[64];
+      uint32_t keepbits[4];
+#pragma unroll
+      for (int c = 0; c < kTile; c += 32) {
+        uint32_t sr[32];
+        tmem_ld32(tl + C::kSCol + c, sr);
+        tmem_wait_ld();
+        uint32_t keep = 0xffffffffu;
+        if constexpr (DROPOUT) {
+          // element (query q, key kj): word kj mod 4 of the counter (kj/4, q, bh, offset)
+          keep = 0;
+#pragma unroll 4
+          for (int t = 0; t < 32; ++t) {
+            const uint32_t w4 = dropout_keep4(static_cast<uint32_t>(kj >> 2),
+                                              static_cast<uint32_t>(q0 + c + t),
+                                              static_cast<uint32_t>(bh), m.offset, m.seed_lo,
+                                              m.seed_hi, m.drop_threshold);
+            keep |= ((w4 >> (kj & 3)) & 1u) << t;
+          }
+        }
+        keepbits[c / 32] = keep;
+        uint32_t pk[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          const int qa = c + t, qb = c + t + 1;
+          float p0 = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -ctl.sL[warp][qa]));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sr[t + 1]), c2, -ctl.sL[warp][qb]));
+          if (!key_ok || (diag && qa < r)) p0 = 0.f;
+          if (!key_ok || (diag && qb < r)) p1 = 0.f;
+          pp[(c + t) / 2] = pack_bf16x2(p0, p1);
+          if constexpr (DROPOUT) {
+            p0 = ((keep >> t) & 1u) ? p0 * ds : 0.f;
+            p1 = ((keep >> (t + 1)) & 1u) ? p1 * ds : 0.f;
+            pk[t / 2] = pack_bf16x2(p0, p1);
+          } else {
+            pk[t / 2] = pp[(c + t) / 2];
+          }
+        }
+        tmem_st16(tl + C::kSCol + c / 2, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.pfull);
+
+      // dS^T = P * (dP~ * Z/(1-p) - D)
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dpfull, ph, wc, kSiteBwdSoft));
+      if (!ok) break;
+      tc_fence_after();
+      if (i >= 1) {   // dS^T buffer was last read by dQ_{i-1}
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dsfree, (i - 1) & 1, wc, kSiteBwdSoft));
+        if (!ok) break;
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int c = 0; c < kTile; c += 32) {
+        uint32_t dr[32];
+        tmem_ld32(tl + C::kDPCol + c, dr);
+        tmem_wait_ld();
+        const uint32_t keep = keepbits[c / 32];
+        uint32_t pk[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[(c + t) / 2]));
+          float d0 = __uint_as_float(dr[t]), d1 = __uint_as_float(dr[t + 1]);
+          if constexpr (DROPOUT) {
+            d0 = ((keep >> t) & 1u) ? d0 * ds : 0.f;
+            d1 = ((keep >> (t + 1)) & 1u) ? d1 * ds : 0.f;
+          }
+          const float s0 = p.x * (d0 - ctl.sD[warp][c + t]);
+          const float s1 = p.y * (d1 - ctl.sD[warp][c + t + 1]);
+          pk[t / 2] = pack_bf16x2(s0, s1);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t off = ds_offset(r, (c >> 3) + u);
+          *reinterpret_cast<uint4*>(sDS + off) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.dsfull);
+    }
+
+    // epilogue: dV and c*dK rows of this key tile
+    if (ok && n > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.done, 0, wc, kSiteBwdSoft));
+      if (ok) tc_fence_after();
+    }
+    if (ok) {
+      const int64_t row_off = b * a.stride_b + h * a.stride_h + static_cast<int64_t>(kj) * a.stride_n;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(which ? a.dk : a.dv) + row_off;
+        const float mul = which ? a.scale : 1.f;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          if (n > 0) {
+            tmem_ld32(tl + (which ? C::kDKCol : C::kDVCol) + c, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) o[t] = 0u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int t = 0; t < 32; t += 2)
+            pk[t / 2] = pack_bf16x2(key_ok ? __uint_as_float(o[t]) * mul : 0.f,
+                                    key_ok ? __uint_as_float(o[t + 1]) * mul : 0.f);
+          if (kj < m.N) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              d4[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------- dQ drain (4-7)
+    const int r = threadIdx.x - 128;       // query row within the tile == TMEM lane
+    const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    float* acc_head = a.dq_acc + static_cast<int64_t>(bh) * m.N * D;
+    for (int i = 0; i < n; ++i) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dqfull, i & 1, wc, kSiteBwdDq));
+      if (!ok) break;
+      tc_fence_after();
+      const int qq = tiles[i] * kTile + r;
+      float4* dst = reinterpret_cast<float4*>(acc_head + static_cast<int64_t>(qq) * D);
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tl + C::kDQCol + c, v);
+        tmem_wait_ld();
+        if (c + 32 >= D) {   // last chunk read: the MMA may reuse the columns
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.dqfree);
+        }
+        if (qq < m.N) {
+#pragma unroll
+          for (int t = 0; t < 32; t += 4)
+            atomicAdd(dst + (c + t) / 4,
+                      make_float4(__uint_as_float(v[t]), __uint_as_float(v[t + 1]),
+                                  __uint_as_float(v[t + 2]), __uint_as_float(v[t + 3])));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// D = rowsum(dO * O) (one row per group of d/8 lanes) and dQacc = 0.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
+                                                            const __nv_bfloat16* __restrict__ dout,
+                                                            const BwdArgs a) {
+  constexpr int kLanes = D / 8;                 // lanes per row
+  const int64_t rows = static_cast<int64_t>(a.m.B) * a.m.H * a.m.N;
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = gtid / kLanes;
+  const int part = static_cast<int>(gtid % kLanes);
+  float s = 0.f;
+  if (row < rows) {
+    const int64_t n = row % a.m.N;
+    const int64_t bh = row / a.m.N;
+    const int64_t b = bh / a.m.H, h = bh % a.m.H;
+    const int64_t off = b * a.stride_b + h * a.stride_h + n * a.stride_n + part * 8;
+    const uint4 ov = *reinterpret_cast<const uint4*>(o + off);
+    const uint4 gv = *reinterpret_cast<const uint4*>(dout + off);
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float2 x = __bfloat1622float2(o2[t]), y = __bfloat1622float2(g2[t]);
+      s = fmaf(x.x, y.x, s);
+      s = fmaf(x.y, y.y, s);
+    }
+  }
+#pragma unroll
+  for (int w = kLanes / 2; w > 0; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
+  if (row < rows && part == 0) const_cast<float*>(a.Dsum)[row] = s;
+  // zero the dQ accumulator
+  const int64_t n4 = rows * D / 4;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  float4* acc = reinterpret_cast<float4*>(a.dq_acc);
+  for (int64_t e = gtid; e < n4; e += stride) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) dq_convert_kernel(__nv_bfloat16* __restrict__ dq,
+                                                        const BwdArgs a) {
+  const int64_t rows = static_cast<int64_t>(a.m.B) * a.m.H * a.m.N;
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = gtid / (D / 8);
+  const int part = static_cast<int>(gtid % (D / 8));
+  if (row >= rows) return;
+  const int64_t n = row % a.m.N;
+  const int64_t bh = row / a.m.N;
+  const int64_t b = bh / a.m.H, h = bh % a.m.H;
+  const float4* src = reinterpret_cast<const float4*>(a.dq_acc + row * D + part * 8);
+  const float4 x = src[0], y = src[1];
+  const float c = a.scale;
+  uint4 out;
+  out.x = pack_bf16x2(x.x * c, x.y * c);
+  out.y = pack_bf16x2(x.z * c, x.w * c);
+  out.z = pack_bf16x2(y.x * c, y.y * c);
+  out.w = pack_bf16x2(y.z * c, y.w * c);
+  *reinterpret_cast<uint4*>(dq + b * a.stride_b + h * a.stride_h + n * a.stride_n + part * 8) = out;
+}
+
+template <int D, bool DROP>
+cudaError_t launch_main(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s) {
+  using C = BwdCfg<D>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_bf16_kernel<D, DROP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const unsigned grid = static_cast<unsigned>(a.m.nb) * a.m.B * a.m.H;
+  bwd_bf16_kernel<D, DROP><<<grid, C::kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, tm.dout, a);
+  return cudaGetLastError();
+}
+
+unsigned blocks_for(int64_t threads) {
+  const int64_t b = (threads + 255) / 256;
+  return static_cast<unsigned>(b < 1 ? 1 : (b > 2147483647 ? 2147483647 : b));
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const BwdArgs& a,
+                                  cudaStream_t s) {
+  const int64_t rows = static_cast<int64_t>(a.m.B) * a.m.H * a.m.N;
+  const unsigned grid = blocks_for(rows * (a.d / 8));
+  if (a.d == 64)
+    bwd_preprocess_kernel<64><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
+                                                   static_cast<const __nv_bfloat16*>(dout), a);
+  else
+    bwd_preprocess_kernel<128><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
+                                                    static_cast<const __nv_bfloat16*>(dout), a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_bf16(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s) {
+  const bool drop = a.m.drop_threshold != 0;
+  if (a.d == 64) return drop ? launch_main<64, true>(tm, a, s) : launch_main<64, false>(tm, a, s);
+  return drop ? launch_main<128, true>(tm, a, s) : launch_main<128, false>(tm, a, s);
+}
+
+cudaError_t launch_dq_convert(void* dq, const BwdArgs& a, cudaStream_t s) {
+  const int64_t rows = static_cast<int64_t>(a.m.B) * a.m.H * a.m.N;
+  const unsigned grid = blocks_for(rows * (a.d / 8));
+  if (a.d == 64)
+    dq_convert_kernel<64><<<grid, 256, 0, s>>>(static_cast<__nv_bfloat16*>(dq), a);
+  else
+    dq_convert_kernel<128><<<grid, 256, 0, s>>>(static_cast<__nv_bfloat16*>(dq), a);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,84 @@
+// Kernel argument blocks and launcher declarations shared by the host API
+// (attn_api.cu) and the kernel translation units.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+constexpr int kTile = 128;            // query/key tile rows == block-mask granularity
+constexpr float kRescaleTau = 8.0f;   // lazy-rescale threshold, log2 units
+
+// Where a kernel gave up waiting (recorded next to the status code).
+enum WaitSite : int {
+  kSiteFwdQ = 1, kSiteFwdK, kSiteFwdV, kSiteFwdKvEmpty, kSiteFwdSFull, kSiteFwdSFree,
+  kSiteFwdPFull, kSiteFwdPvDone,
+  kSiteBwdLoad = 20, kSiteBwdKV, kSiteBwdQ, kSiteBwdMma, kSiteBwdSoft, kSiteBwdDq,
+  kSiteBwdEmpty, kSiteBwdFree
+};
+
+// Per-call mask/dropout settings common to every kernel.
+struct MaskArgs {
+  int B, H, N;
+  int causal;
+  const int32_t* key_lens;        // [B] or null
+  // block mask, compacted: for mask m and tile t, cnt[m * nb + t] sorted
+  // tile indices in idx[(m * nb + t) * nb + ...]; null when dense
+  const int32_t* list_cnt;
+  const uint16_t* list_idx;
+  int nb;                         // ceil(N / 128)
+  int mask_per_head;              // 0: one mask for all (b, h)
+  // dense block mask (read by the fp32 kernel directly)
+  const uint8_t* block_mask;
+  int64_t block_mask_head_stride;
+  // dropout
+  uint32_t drop_threshold;        // 0 = no dropout
+  float drop_scale;               // 1 / (1 - p)
+  uint32_t seed_lo, seed_hi, offset;
+};
+
+struct FwdArgs {
+  MaskArgs m;
+  int d;
+  float scale;                    // c
+  float scale_log2;               // c * log2(e)
+  void* o;                        // [B,H,N,d]
+  float* lse;                     // [B,H,N]
+  int64_t stride_b, stride_h, stride_n;
+  int* status;                    // workspace status words
+  uint64_t timeout_ns;
+};
+
+struct BwdArgs {
+  MaskArgs m;
+  int d;
+  float scale;
+  float scale_log2;
+  const float* lse;               // [B,H,N]
+  const float* Dsum;              // [B,H,N] rowsum(dO * O)
+  float* dq_acc;                  // [B,H,N,d] fp32, zeroed by the preprocess
+  void* dk;
+  void* dv;
+  int64_t stride_b, stride_h, stride_n;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+// Tensor maps: 4-D {d, N, H, B}, 64-element x 128-row boxes, 128-byte swizzle.
+struct TensorMaps {
+  CUtensorMap q, k, v, o, dout, dq_acc;
+};
+
+// Launchers (return the cudaGetLastError() of their launches).
+cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_fwd_fp32(const float* q, const float* k, const float* v, const FwdArgs& a,
+                            cudaStream_t s);
+cudaError_t launch_compact_mask(const uint8_t* mask, int64_t head_stride, int masks, int nb,
+                                int by_column, int32_t* cnt, uint16_t* idx, cudaStream_t s);
+cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const BwdArgs& a,
+                                  cudaStream_t s);
+cudaError_t launch_bwd_bf16(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_dq_convert(void* dq, const BwdArgs& a, cudaStream_t s);
+
+}  // namespace attn

@@ -1,0 +1,45 @@
+// Philox4x32-10 counter-based generator, device side.
+//
+// From the definition in Salmon, Moraes, Dror, Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3" (SC'11): four 32-bit counter words, two key
+// words; each round multiplies words 0 and 2 by fixed odd constants, takes
+// the 64-bit products apart into high and low halves, mixes the high halves
+// with the other two words and the key, and the key advances by the Weyl
+// increments between rounds.  Ten rounds.
+#pragma once
+#include <cstdint>
+
+namespace attn {
+
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u;
+constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
+constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += kPhiloxW0;
+      k1 += kPhiloxW1;
+    }
+    const uint64_t p0 = static_cast<uint64_t>(kPhiloxM0) * c.x;
+    const uint64_t p1 = static_cast<uint64_t>(kPhiloxM1) * c.z;
+    const uint32_t hi0 = static_cast<uint32_t>(p0 >> 32), lo0 = static_cast<uint32_t>(p0);
+    const uint32_t hi1 = static_cast<uint32_t>(p1 >> 32), lo1 = static_cast<uint32_t>(p1);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// Keep bits of four consecutive keys j = 4g .. 4g+3 of query row i:
+// bit t of the result is 1 iff key 4g+t is kept (word t >= threshold).
+__device__ __forceinline__ uint32_t dropout_keep4(uint32_t g, uint32_t i, uint32_t bh,
+                                                  uint32_t offset, uint32_t seed_lo,
+                                                  uint32_t seed_hi, uint32_t threshold) {
+  const uint4 u = philox4x32_10(make_uint4(g, i, bh, offset), seed_lo, seed_hi);
+  return (u.x >= threshold ? 1u : 0u) | (u.y >= threshold ? 2u : 0u) |
+         (u.z >= threshold ? 4u : 0u) | (u.w >= threshold ? 8u : 0u);
+}
+
+}  // namespace attn

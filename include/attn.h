@@ -1,0 +1,149 @@
+/*
+ * exact_attention_12_gb300 — fused exact scaled dot-product attention for
+ * NVIDIA GB300 (sm_103a).  C interface.
+ *
+ * The operation (FlashAttention: Fast and Memory-Efficient Exact Attention
+ * with IO-Awareness, Dao et al. 2022, as summarised on the pages
+ * "FlashAttention: Cơ chế Attention chính xác, nhanh và tối ưu bộ nhớ với
+ * nhận thức IO" (xyznot.com, "Phương pháp"), "3.3 Hiểu sâu cơ chế
+ * Self-Attention" (§3 Scaled Dot-Product Attention, §10 Causal Mask, §12
+ * FlashAttention) and the azimuth.plus FlashAttention explainer
+ * ("الخوارزمية خطوة بخطوة", the step-by-step algorithm)):
+ *
+ *   S = scale * Q K^T, with S_ij = -inf where key j is not allowed for query i
+ *   L_i = logsumexp_j S_ij               (natural log, fp32)
+ *   P = exp(S - L),  P~ = P * Z / (1 - p)  (Z: Philox dropout keep mask)
+ *   O = P~ V
+ *
+ * Allowed(i, j) = (!causal || j <= i) && j < key_lens[b] &&
+ *                 block_mask[i / 128][j / 128] != 0.
+ * A row with no allowed key gets O_i = 0 and L_i = -inf.
+ *
+ * Backward (chain rule of the above; the pages state only that S and P are
+ * recomputed from Q, K, V and the stored statistics):
+ *   D = rowsum(dO * O),  dV = P~^T dO,  dP = (dO V^T) * Z / (1 - p),
+ *   dS = P * (dP - D),   dQ = scale * dS K,  dK = scale * dS^T Q.
+ *
+ * Dropout keep mask: for element (b, h, i, j) the 32-bit word j mod 4 of
+ * Philox4x32-10 (Salmon et al., SC'11) at counter
+ * (floor(j / 4), i, b * H + h, philox_offset) under key
+ * (low 32 bits of philox_seed, high 32 bits) is u; the element is dropped
+ * iff u < T, T = min(2^32 - 1, floor(dropout_p * 2^32)) computed in fp64
+ * from the float dropout_p.  The backward call regenerates the same mask.
+ *
+ * Layout: Q, K, V, O, dO, dQ, dK, dV are logical [B, H, N, d] arrays with
+ * unit stride along d and the element strides stride_b, stride_h, stride_n
+ * (shared by all eight tensors).  lse is a contiguous fp32 [B, H, N].
+ * Every device pointer must be 16-byte aligned; strides must be multiples
+ * of 8 elements (bf16) or 4 elements (fp32).
+ *
+ * Ownership: the caller allocates and owns every buffer, including the
+ * workspace `ws` (device memory, at least attn_workspace_size() bytes).  The
+ * library allocates nothing and keeps no state between calls.  The first
+ * 256 bytes of a workspace hold a device status word and must be zero before
+ * the workspace is first used; attn_check() reads and clears it.
+ *
+ * Streams: every call only enqueues work on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and returns.  Argument errors are detected on
+ * the host before anything is enqueued.  Launch failures return
+ * ATTN_ERR_CUDA.  A kernel that stops making progress gives up after a
+ * bounded wait and records ATTN_ERR_TIMEOUT in the workspace status word,
+ * which attn_check() returns.
+ *
+ * Thread safety: calls on different workspaces may run concurrently; two
+ * calls in flight on the same workspace race.
+ */
+#ifndef EXACT_ATTENTION_12_GB300_ATTN_H
+#define EXACT_ATTENTION_12_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,   /* bad shape, stride, pointer, scale, p, ... */
+  ATTN_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. fp32 bwd) */
+  ATTN_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+  ATTN_ERR_TIMEOUT = 4,       /* a kernel wait gave up (device status) */
+  ATTN_ERR_WORKSPACE = 5      /* workspace missing, misaligned or too small */
+} attn_status;
+
+typedef enum { ATTN_BF16 = 0, ATTN_FP32 = 1 } attn_dtype;
+
+typedef struct attn_params {
+  int32_t B, H, N, d;        /* batch, heads, sequence length, head dim.
+                                d in {64, 128}.  B, H or N = 0: no work. */
+  int32_t dtype;             /* attn_dtype.  bf16: forward and backward;
+                                fp32: forward only. */
+  float scale;               /* score scale, e.g. 1/sqrt(d); finite */
+  int32_t causal;            /* nonzero: keep j <= i (top-left aligned) */
+  float dropout_p;           /* drop probability in [0, 1); 0 = no dropout */
+  uint64_t philox_seed;      /* Philox key */
+  uint64_t philox_offset;    /* Philox counter word 3; must be < 2^32 */
+  const int32_t* key_lens;   /* device [B]: keys j >= key_lens[b] masked;
+                                NULL = all N keys valid.  Values are
+                                clamped to [0, N]. */
+  const uint8_t* block_mask; /* device uint8 [nb][nb], nb = ceil(N / 128),
+                                row-major; nonzero = 128x128 block kept;
+                                NULL = dense.  bf16 only. */
+  int64_t block_mask_head_stride; /* bytes between the masks of consecutive
+                                (b * H + h); 0 = one mask for all heads */
+  int64_t stride_b, stride_h, stride_n; /* element strides of the tensors */
+} attn_params;
+
+/* Bytes of device workspace a forward (for_backward = 0) or backward
+ * (for_backward != 0) call needs.  Returns 0 if the parameters are invalid
+ * (the call itself then reports why). */
+size_t attn_workspace_size(const attn_params* p, int for_backward);
+
+/* Forward: O [B,H,N,d] (same dtype as q) and lse [B,H,N] fp32. */
+attn_status attn_fwd(const attn_params* p, const void* q, const void* k,
+                     const void* v, void* o, float* lse, void* ws,
+                     size_t ws_bytes, void* stream);
+
+/* Backward (bf16): needs o and lse from attn_fwd with the same parameters
+ * (dropout seed and offset included).  Writes dq, dk, dv [B,H,N,d] bf16. */
+attn_status attn_bwd(const attn_params* p, const void* q, const void* k,
+                     const void* v, const void* o, const float* lse,
+                     const void* dout, void* dq, void* dk, void* dv, void* ws,
+                     size_t ws_bytes, void* stream);
+
+/* The three stages attn_bwd runs, callable one by one on the same workspace
+ * (for callers that schedule or time them separately):
+ *   attn_bwd_preprocess  D = rowsum(dO * O) into the workspace; zeroes the
+ *                        workspace's fp32 dQ accumulator.
+ *   attn_bwd_main        the fused recomputing backward: dK, dV written,
+ *                        dQ accumulated into the workspace.  Needs the
+ *                        preprocess of the same call sequence.
+ *   attn_bwd_dq          dQ = scale * accumulator, converted to bf16.
+ * Arguments mean the same as for attn_bwd; the workspace must be the same
+ * and at least attn_workspace_size(p, 1) bytes. */
+attn_status attn_bwd_preprocess(const attn_params* p, const void* o,
+                                const void* dout, void* ws, size_t ws_bytes,
+                                void* stream);
+attn_status attn_bwd_main(const attn_params* p, const void* q, const void* k,
+                          const void* v, const float* lse, const void* dout,
+                          void* dk, void* dv, void* ws, size_t ws_bytes,
+                          void* stream);
+attn_status attn_bwd_dq(const attn_params* p, void* dq, void* ws,
+                        size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, returns the workspace's device status (ATTN_OK or
+ * ATTN_ERR_TIMEOUT) and clears it. */
+attn_status attn_check(void* ws, void* stream);
+
+/* Static description of a status code. */
+const char* attn_status_string(attn_status s);
+
+/* Detail message of the last non-OK status returned on the calling thread. */
+const char* attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTENTION_12_GB300_ATTN_H */

@@ -35,6 +35,7 @@ from .attention import (  # noqa: F401
     attention_backward,
     forward_rows,
     backward_keys,
+    backward_rows,
     dropout_threshold,
     keep_mask,
 )

@@ -218,6 +218,16 @@ def backward_keys(q, k, v, do, b, h, keys, scale, causal=False, key_lens=None,
     return dK[keys], dV[keys]
 
 
+def backward_rows(q, k, v, do, b, h, rows, scale, causal=False, key_lens=None,
+                  block_mask=None, dropout_p=0.0, seed=0, offset=0):
+    """dQ[b, h, rows] for sampled query rows of one head (each row in full)."""
+    hd = _head(q, k, v, b, h, scale, causal, key_lens, block_mask, dropout_p,
+               seed, offset)
+    dob = np.asarray(do[b, h], dtype=np.float64)
+    out = [hd.backward(r, dob[r])[2] for r in _chunks(rows)]
+    return np.concatenate(out) if out else np.zeros((0, hd.q.shape[1]))
+
+
 def attention_forward(q, k, v, scale, causal=False, key_lens=None,
                       block_mask=None, dropout_p=0.0, seed=0, offset=0):
     """Full forward.  q, k, v: [B, H, N, d].  Returns O [B,H,N,d], L [B,H,N] (fp64).

@@ -1,0 +1,74 @@
+"""Shared helpers for the GPU parity tests: tolerances, conversions, oracle calls."""
+
+import numpy as np
+import torch
+
+# Tolerances of the parity bar (bf16 I/O, fp32 accumulation):
+O_MAX_ABS = 1e-2      # forward output: max |O_gpu - O_oracle| beyond the output's
+                      # own bf16 rounding (see o_err)
+BF16_HALF_ULP_REL = 2.0 ** -8   # one round-to-nearest into bf16, relative
+L_MAX_ABS = 1e-3      # logsumexp, max |L_gpu - L_oracle|
+GRAD_REL_L2 = 1e-2    # dQ, dK, dV: ||g_gpu - g_oracle|| / ||g_oracle||
+
+
+def np64(t):
+    """Exact fp64 copy of a (bf16/fp32) tensor as numpy."""
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def to_dev(x, device="cuda"):
+    return None if x is None else x.to(device)
+
+
+def max_abs(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    if a.size == 0:
+        return 0.0
+    with np.errstate(invalid="ignore"):
+        both_inf = np.isinf(a) & np.isinf(b) & (np.sign(a) == np.sign(b))
+        d = np.where(both_inf, 0.0, np.abs(a - b))
+    return float(np.nanmax(np.where(np.isnan(d), np.inf, d)))
+
+
+def o_err(got, want, out_bf16=True):
+    """Max |got - want| beyond the output's own rounding.
+
+    A bf16 output cannot be closer to the exact value than half a bf16 ulp
+    (<= 2^-8 |want|), so that much is subtracted per element before taking
+    the max; for fp32 outputs nothing is subtracted.
+    """
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    if got.size == 0:
+        return 0.0
+    slack = BF16_HALF_ULP_REL * np.abs(want) if out_bf16 else 0.0
+    d = np.abs(got - want) - slack
+    return float(np.max(np.where(np.isnan(d), np.inf, d)))
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    nb = np.linalg.norm(b)
+    if nb == 0:
+        return float(np.linalg.norm(a))
+    return float(np.linalg.norm(a - b) / nb)
+
+
+def oracle_kwargs(inp):
+    """Translate a workloads.make_inputs dict into oracle keyword arguments."""
+    kl = inp.get("key_lens")
+    bm = inp.get("block_mask")
+    return dict(scale=inp["scale"], causal=inp["causal"],
+                key_lens=None if kl is None else kl.numpy(),
+                block_mask=None if bm is None else bm.numpy(),
+                dropout_p=inp["dropout_p"], seed=inp["seed"], offset=inp["offset"])
+
+
+def api_kwargs(inp, device="cuda"):
+    """Translate a workloads.make_inputs dict into API keyword arguments."""
+    return dict(scale=inp["scale"], causal=inp["causal"],
+                key_lens=to_dev(inp.get("key_lens"), device),
+                block_mask=to_dev(inp.get("block_mask"), device),
+                dropout_p=inp["dropout_p"], seed=inp["seed"], offset=inp["offset"])

@@ -1,0 +1,121 @@
+"""The C library's host side, without a GPU: symbols, struct layout, argument checks.
+
+Every call here fails validation before anything touches the CUDA runtime,
+so none of these tests needs a device.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def abi():
+    from exact_attention_12_gb300 import build, _abi
+    if not os.path.exists(build.LIB_PATH):
+        build.build()
+    return _abi
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function(abi):
+    lib = abi.lib()
+    declared = _declared_functions()
+    assert declared, "no functions found in include/attn.h"
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(declared) == sorted(abi.EXPORTS), (declared, sorted(abi.EXPORTS))
+
+
+def test_params_struct_layout(abi):
+    p = abi.AttnParams
+    assert ctypes.sizeof(p) == 96
+    assert p.philox_seed.offset == 32 and p.key_lens.offset == 48
+    assert p.stride_n.offset == 88
+
+
+def _params(abi, **kw):
+    p = abi.AttnParams()
+    p.B, p.H, p.N, p.d = 2, 3, 256, 64
+    p.dtype = abi.ATTN_BF16
+    p.scale = 0.125
+    p.stride_b, p.stride_h, p.stride_n = 3 * 256 * 64, 256 * 64, 64
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("d", 96, 2), ("d", 32, 2), ("B", -1, 1), ("scale", 0.0, 1), ("scale", -1.0, 1),
+    ("scale", float("inf"), 1), ("dropout_p", 1.0, 1), ("dropout_p", -0.1, 1),
+    ("philox_offset", 1 << 32, 1), ("stride_n", 60, 1), ("stride_h", 0, 1), ("dtype", 7, 1),
+])
+def test_invalid_arguments_are_rejected_on_the_host(abi, field, value, status):
+    lib = abi.lib()
+    p = _params(abi, **{field: value})
+    assert lib.attn_workspace_size(ctypes.byref(p), 0) == 0
+    fake = ctypes.c_void_p(0x1000)
+    st = lib.attn_fwd(ctypes.byref(p), fake, fake, fake, fake, fake, fake, 1 << 20, None)
+    assert st == status, lib.attn_last_error()
+    assert lib.attn_last_error()
+
+
+def test_fp32_backward_is_unsupported(abi):
+    lib = abi.lib()
+    p = _params(abi, dtype=abi.ATTN_FP32)
+    fake = ctypes.c_void_p(0x1000)
+    st = lib.attn_bwd(ctypes.byref(p), *([fake] * 10), 1 << 30, None)
+    assert st == abi.ATTN_ERR_UNSUPPORTED
+
+
+def test_workspace_size_and_checks(abi):
+    lib = abi.lib()
+    p = _params(abi)
+    fwd = lib.attn_workspace_size(ctypes.byref(p), 0)
+    bwd = lib.attn_workspace_size(ctypes.byref(p), 1)
+    B, H, N, d = 2, 3, 256, 64
+    assert fwd == 256
+    assert bwd >= 256 + B * H * N * 4 + B * H * N * d * 4
+    fake = ctypes.c_void_p(0x1000)
+    assert lib.attn_fwd(ctypes.byref(p), fake, fake, fake, fake, fake, None, 0, None) == \
+        abi.ATTN_ERR_WORKSPACE
+    assert lib.attn_fwd(ctypes.byref(p), fake, fake, fake, fake, fake, ctypes.c_void_p(0x1010),
+                        4096, None) == abi.ATTN_ERR_WORKSPACE          # misaligned
+    assert lib.attn_bwd(ctypes.byref(p), *([fake] * 10), bwd - 1, None) == abi.ATTN_ERR_WORKSPACE
+    # block masks add the compacted lists
+    p2 = _params(abi, block_mask=0x2000, block_mask_head_stride=4)
+    assert lib.attn_workspace_size(ctypes.byref(p2), 0) > fwd
+
+
+def test_misaligned_tensor_is_rejected(abi):
+    lib = abi.lib()
+    p = _params(abi)
+    ok = ctypes.c_void_p(0x1000)
+    bad = ctypes.c_void_p(0x1008)
+    st = lib.attn_fwd(ctypes.byref(p), ok, bad, ok, ok, ok, ok, 4096, None)
+    assert st == abi.ATTN_ERR_INVALID_ARG
+
+
+def test_empty_problem_is_a_no_op(abi):
+    lib = abi.lib()
+    for f in ("N", "B", "H"):
+        p = _params(abi, **{f: 0})
+        st = lib.attn_fwd(ctypes.byref(p), None, None, None, None, None, ctypes.c_void_p(0x1000),
+                          256, None)
+        assert st == abi.ATTN_OK, (f, lib.attn_last_error())
+
+
+def test_status_strings(abi):
+    lib = abi.lib()
+    for s in range(6):
+        assert lib.attn_status_string(s)
+    assert lib.attn_status_string(99) == b"unknown status"

@@ -1,0 +1,195 @@
+"""Forward parity: the CUDA library against the fp64 oracle, element by element."""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import attention as oracle
+from tests.helpers import (L_MAX_ABS, O_MAX_ABS, api_kwargs, max_abs, np64, o_err,
+                           oracle_kwargs)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ea():
+    import exact_attention_12_gb300 as ea
+    from exact_attention_12_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+    return ea
+
+
+def _run_fwd(ea, inp):
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    o, lse = ea.attention_fwd(q, k, v, **api_kwargs(inp))
+    torch.cuda.synchronize()
+    ea.check()
+    return o.cpu(), lse.cpu()
+
+
+def _inputs(B, H, N, d, seed, dtype=torch.bfloat16, causal=False, key_lens=None,
+            block_mask=None, dropout_p=0.0, std=1.0, scale=None):
+    q, k, v, do = workloads.random_case(B, H, N, d, seed, dtype=dtype, std=std)
+    return dict(q=q, k=k, v=v, do=do,
+                key_lens=None if key_lens is None else torch.tensor(key_lens, dtype=torch.int32),
+                block_mask=block_mask, scale=scale if scale is not None else d ** -0.5,
+                causal=causal, dropout_p=dropout_p, seed=1234, offset=5)
+
+
+def _check_full(ea, inp):
+    o, lse = _run_fwd(ea, inp)
+    O, L = oracle.attention_forward(np64(inp["q"]), np64(inp["k"]), np64(inp["v"]),
+                                    **oracle_kwargs(inp))
+    eo = o_err(np64(o), O, out_bf16=o.dtype == torch.bfloat16)
+    el = max_abs(lse.numpy(), L)
+    assert eo <= O_MAX_ABS and el <= L_MAX_ABS, (eo, el)
+    return eo, el
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 7, 127, 128, 129, 300])
+@pytest.mark.parametrize("causal", [False, True])
+def test_small_shapes(ea, d, N, causal):
+    _check_full(ea, _inputs(2, 3, N, d, seed=N * 7 + d, causal=causal))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_key_padding_and_dropout(ea, d):
+    _check_full(ea, _inputs(3, 2, 390, d, seed=11, key_lens=[390, 200, 129], dropout_p=0.1))
+
+
+def test_padding_with_empty_and_short_rows(ea):
+    # key_lens 0: every row is empty (O = 0, L = -inf); 1: one key
+    _check_full(ea, _inputs(3, 1, 260, 64, seed=12, key_lens=[0, 1, 128], causal=True))
+
+
+@pytest.mark.parametrize("per_head", [False, True])
+def test_block_mask(ea, per_head):
+    B, H, N = 2, 2, 700
+    nb = (N + 127) // 128
+    g = torch.Generator().manual_seed(3)
+    shape = (B, H, nb, nb) if per_head else (nb, nb)
+    bm = (torch.rand(shape, generator=g) < 0.4).to(torch.uint8)
+    if per_head:
+        bm[0, 1, 2, :] = 0          # a query tile with no kept block at all
+    else:
+        bm[2, :] = 0
+    _check_full(ea, _inputs(B, H, N, 64, seed=13, block_mask=bm))
+
+
+def test_block_mask_causal_padding_dropout(ea):
+    B, H, N = 2, 2, 520
+    bm = workloads.make_block_mask(5, 0.5, seed=4)
+    _check_full(ea, _inputs(B, H, N, 128, seed=14, block_mask=bm, causal=True,
+                            key_lens=[520, 333], dropout_p=0.2))
+
+
+def test_large_scores_force_rescales(ea):
+    # large-magnitude scores: the running max jumps by far more than the
+    # lazy-rescale threshold many times along a row
+    inp = _inputs(1, 2, 640, 64, seed=15)
+    inp["q"] = (inp["q"].float() * 3).to(torch.bfloat16)   # score std ~9
+    inp["k"] = (inp["k"].float() * 3).to(torch.bfloat16)
+    _check_full(ea, inp)
+
+
+def test_fp32_single_head_config(ea):
+    w = workloads.get("single-head-fp32")
+    inp = workloads.make_inputs(w)
+    o, lse = _run_fwd(ea, inp)
+    O, L = oracle.attention_forward(np64(inp["q"]), np64(inp["k"]), np64(inp["v"]),
+                                    **oracle_kwargs(inp))
+    assert max_abs(np64(o), O) <= 1e-4
+    assert max_abs(lse.numpy(), L) <= 1e-4
+
+
+@pytest.mark.parametrize("kw", [dict(causal=True), dict(key_lens=[300, 77], dropout_p=0.3)])
+def test_fp32_masks(ea, kw):
+    _check_full(ea, _inputs(2, 2, 300, 64, seed=16, dtype=torch.float32, **kw))
+
+
+def test_strided_bnhd_layout(ea):
+    # [B, N, H, d] storage viewed as [B, H, N, d]
+    B, H, N, d = 2, 3, 200, 64
+    g = torch.Generator().manual_seed(17)
+    base = [torch.randn(B, N, H, d, generator=g).to(torch.bfloat16) for _ in range(3)]
+    q, k, v = (t.transpose(1, 2) for t in base)
+    inp = dict(q=q, k=k, v=v, key_lens=None, block_mask=None, scale=0.125, causal=True,
+               dropout_p=0.0, seed=0, offset=0)
+    qd, kd, vd = (t.cuda() for t in base)
+    o, lse = ea.attention_fwd(qd.transpose(1, 2), kd.transpose(1, 2), vd.transpose(1, 2),
+                              scale=0.125, causal=True)
+    O, L = oracle.attention_forward(np64(q), np64(k), np64(v), **oracle_kwargs(inp))
+    assert o_err(np64(o.cpu()), O) <= O_MAX_ABS
+    assert max_abs(lse.cpu().numpy(), L) <= L_MAX_ABS
+
+
+def test_mask_and_keep_bits_are_exact(ea):
+    """Causal, padding, block and dropout masks, bit-exactly through the API.
+
+    With Q = K = 0 every allowed score is 0, so P_ij = 1 / n_allowed(i) on
+    allowed keys.  Making column c of V the indicator of key g*128 + c turns
+    O[i, c] into Z_ij / ((1 - p) n_allowed(i)) for j = g*128 + c: nonzero
+    exactly where key j is allowed and kept.
+    """
+    B, H, N, d = 2, 2, 384, 128
+    key_lens = torch.tensor([384, 250], dtype=torch.int32)
+    bm = torch.tensor([[1, 0, 1], [1, 1, 0], [0, 1, 1]], dtype=torch.uint8)
+    p, seed, offset = 0.25, 0xDEADBEEF12345, 9
+    z = torch.zeros(B, H, N, d, dtype=torch.bfloat16)
+    got = np.zeros((B, H, N, N), dtype=bool)
+    for g in range(N // d):
+        v = torch.zeros(B, H, N, d, dtype=torch.bfloat16)
+        idx = torch.arange(d)
+        v[:, :, g * d + idx, idx] = 1.0
+        o, _ = ea.attention_fwd(z.cuda(), z.cuda(), v.cuda(), scale=0.1, causal=True,
+                                key_lens=key_lens.cuda(), block_mask=bm.cuda(), dropout_p=p,
+                                seed=seed, offset=offset)
+        got[..., g * d:(g + 1) * d] = (o.cpu().float().numpy() != 0)
+    want = np.zeros_like(got)
+    for b in range(B):
+        for h in range(H):
+            allowed = oracle.allowed_mask(np.arange(N), np.arange(N), True, int(key_lens[b]),
+                                          bm.numpy())
+            keep = oracle.keep_mask(np.arange(N), np.arange(N), b * H + h, seed, offset, p)
+            want[b, h] = allowed & keep
+    assert np.array_equal(got, want)
+
+
+def test_empty_problem_sizes(ea):
+    for shape in [(0, 2, 16, 64), (1, 0, 16, 64), (1, 1, 0, 64)]:
+        q = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+        o, lse = ea.attention_fwd(q, q, q)
+        assert o.shape == q.shape and tuple(lse.shape) == shape[:3]
+
+
+# ------------------------------------------------- full-size workloads ----
+
+def _sampled_rows(N, seed):
+    rng = np.random.default_rng(seed)
+    fixed = {0, 1, 127, 128, 129, N // 2, N - 129, N - 128, N - 1}
+    rows = sorted({r for r in fixed if 0 <= r < N} | set(rng.integers(0, N, 12).tolist()))
+    return np.array(rows)
+
+
+@pytest.mark.parametrize("name", ["bert-large", "gpt2-1k", "gpt2-4k", "long-causal-512",
+                                  "long-causal-4096", "long-causal-16384",
+                                  "block-sparse-64k"])
+def test_full_size_workload_sampled(ea, name):
+    w = workloads.get(name)
+    inp = workloads.make_inputs(w)
+    o, lse = _run_fwd(ea, inp)
+    q, k, v = np64(inp["q"]), np64(inp["k"]), np64(inp["v"])
+    kw = oracle_kwargs(inp)
+    rng = np.random.default_rng(5)
+    heads = {(0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))}
+    for b, h in heads:
+        rows = _sampled_rows(w.N, b * 100 + h)
+        O, L = oracle.forward_rows(q, k, v, b, h, rows, **kw)
+        eo = o_err(np64(o[b, h, rows]), O)
+        el = max_abs(lse[b, h, rows].numpy(), L)
+        assert eo <= O_MAX_ABS and el <= L_MAX_ABS, (name, b, h, eo, el)
+    # every row of the output is finite (no unwritten or NaN rows)
+    assert torch.isfinite(o.float()).all()

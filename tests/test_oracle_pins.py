@@ -358,6 +358,8 @@ def test_sampled_helpers_match_full_evaluation():
     Or, Lr = A.forward_rows(q, k, v, 1, 0, rows, **kw)
     np.testing.assert_allclose(Or, O[1, 0, rows], atol=1e-13)
     np.testing.assert_allclose(Lr, L[1, 0, rows], atol=1e-13)
+    dQs = A.backward_rows(q, k, v, do, 1, 1, rows, **kw)
+    np.testing.assert_allclose(dQs, dQ[1, 1, rows], atol=1e-12)
     keys = np.array([0, 127, 128, 249, 260])
     dKs, dVs = A.backward_keys(q, k, v, do, 0, 1, keys, **kw)
     np.testing.assert_allclose(dKs, dK[0, 1, keys], atol=1e-12)
