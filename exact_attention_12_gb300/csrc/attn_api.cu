@@ -150,10 +150,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [B, H, N, d] tensor with element strides; boxes of `box_cols` x 128 rows.
+// [B, H, N, d] tensor with element strides; boxes of `box_cols` x `box_rows`.
 attn_status make_map(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, int elem_bytes,
                      int B, int H, int N, int d, int64_t sb, int64_t sh, int64_t sn, int box_cols,
-                     CUtensorMapSwizzle swz) {
+                     int box_rows, CUtensorMapSwizzle swz) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
@@ -161,7 +161,7 @@ attn_status make_map(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, 
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(sn * elem_bytes),
                                  static_cast<cuuint64_t>(sh * elem_bytes),
                                  static_cast<cuuint64_t>(sb * elem_bytes)};
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(kTile), 1, 1};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   const CUresult r = enc(map, dt, 4, const_cast<void*>(ptr), dims, strides, box, es,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -172,7 +172,7 @@ attn_status make_map(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, 
 
 attn_status make_bf16_map(CUtensorMap* map, const void* ptr, const attn_params* p) {
   return make_map(map, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->B, p->H, p->N, p->d,
-                  p->stride_b, p->stride_h, p->stride_n, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+                  p->stride_b, p->stride_h, p->stride_n, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 attn::MaskArgs mask_args(const attn_params* p, const WsLayout& L, char* ws, bool by_column) {
@@ -324,6 +324,13 @@ attn_status attn_bwd_main(const attn_params* p, const void* q, const void* k, co
   if ((st = make_bf16_map(&tm.k, k, p)) != ATTN_OK) return st;
   if ((st = make_bf16_map(&tm.v, v, p)) != ATTN_OK) return st;
   if ((st = make_bf16_map(&tm.dout, dout, p)) != ATTN_OK) return st;
+  // fp32 dQ accumulator: contiguous [B, H, N, d]; 32 x 32 boxes, 128-byte swizzle
+  const int64_t d64 = p->d;
+  if ((st = make_map(&tm.dq_acc, a.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->B, p->H, p->N,
+                     p->d, static_cast<int64_t>(p->H) * p->N * d64,
+                     static_cast<int64_t>(p->N) * d64, d64, 32, 32,
+                     CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK)
+    return st;
   cudaError_t e;
   if (p->block_mask != nullptr) {
     e = attn::launch_compact_mask(p->block_mask, p->block_mask_head_stride, num_masks(p), a.m.nb,

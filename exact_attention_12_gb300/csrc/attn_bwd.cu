@@ -20,18 +20,22 @@
 //                      dK  += dS^T Q_i       (A = dS^T in shared memory)
 //                      dQ_i = dS K_j         (A = the same dS^T buffer read
 //                                             as an MN-major operand)
-//                    dK and dV stay in TMEM for the whole loop; dQ_i is
-//                    drained by four warps into the fp32 accumulator with
-//                    vector atomics.
+//                    dK and dV stay in TMEM for the whole loop; each dQ_i is
+//                    staged through shared memory and added into the fp32
+//                    accumulator with TMA bulk reduce-adds.
 //   dq_convert       dQ = c * accumulator -> bf16.
 //
 // Warp roles of bwd_kernel (320 threads):
-//   warps 0-3  "softmax": thread t owns key row t (TMEM lane t): P^T row,
-//              dropout mask, dS^T row; epilogue writes dK, dV.
-//   warps 4-7  dQ drain: thread t owns query row t of the dQ tile.
+//   warps 0-7  compute: warp w owns key rows 32*(w%4) .. +31 (TMEM lanes) and
+//              query columns 64*(w/4) .. +63 of the S^T / dP^T tiles.  The
+//              backward needs no row reduction, so the 128 columns of a row
+//              split freely between two warps.  Per query tile: P^T and the
+//              dropout mask, P~^T into TMEM, dS^T into shared memory, and the
+//              drain of the previous dQ tile; epilogue writes dK, dV.
 //   warp 8     TMA producer (K_j, V_j once; Q_i, dO_i per query tile).
 //   warp 9     MMA issuer, TMEM owner.
-// TMEM columns: S^T [0,128) (P~^T as bf16 over [0,64) once S^T is read),
+// TMEM columns: S^T [0,128) -- P~^T (bf16 pairs) overwrites columns [0,32)
+//   and [64,96), each half by the warps that read that half of S^T --,
 //   dP^T [128,256), dV [256,256+d), dK [256+d,256+2d), dQ [384,448) for
 //   d = 64 and over the dP^T columns for d = 128.
 #include <cuda_bf16.h>
@@ -46,6 +50,7 @@ using namespace sm103;
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kComputeWarps = 8;
 
 template <int D>
 struct BwdCfg {
@@ -54,11 +59,14 @@ struct BwdCfg {
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kStages = (D == 64) ? 2 : 1;          // Q_i / dO_i stages
   static constexpr int kDsBytes = kTile * kTile * 2;          // dS^T tile, bf16
-  static constexpr int kSmem = 1024 + 2 * kTileBytes + 2 * kStages * kTileBytes + kDsBytes;
+  static constexpr int kStageBytes = 32 * 32 * 4;             // per-warp dQ staging
+  static constexpr int kSmem = 1024 + 2 * kTileBytes + 2 * kStages * kTileBytes + kDsBytes +
+                               kComputeWarps * kStageBytes;
   static constexpr uint32_t kSCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 256 + D;
   static constexpr uint32_t kDQCol = (D == 64) ? 384 : 128;
   static constexpr bool kDqAliasesDp = (D == 128);
-  static constexpr int kThreads = 320;
+  static constexpr int kHalf = D / 2;                         // dQ/dK/dV columns per warp
+  static constexpr int kThreads = (kComputeWarps + 2) * 32;
 };
 
 template <int ST>
@@ -67,9 +75,9 @@ struct BwdCtl {
   uint64_t qfull[ST], qempty[ST];
   uint64_t sfull, dpfull, pfull, dsfull, dsfree, dqfull, dqfree, done;
   uint64_t final_bar;
-  float sL[4][kTile];     // per softmax warp: L_i * log2(e) of the query tile
-                          // (+inf: the row contributes nothing)
-  float sD[4][kTile];     // per softmax warp: D_i of the query tile
+  float sL[kComputeWarps][64];   // per compute warp: L * log2(e) of its 64 query rows
+                                 // (+inf: the row contributes nothing)
+  float sD[kComputeWarps][64];   // per compute warp: D of its 64 query rows
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -111,18 +119,48 @@ __device__ __forceinline__ int key_limit(const MaskArgs& m, int b) {
   return limit;
 }
 
-// 16-byte chunk `chunk` (8 bf16) of row `r` in a [128][128] bf16 tile stored
-// as two 64-column boxes with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t ds_offset(int r, int chunk) {
-  const int half = chunk >> 3, c = chunk & 7;
-  return half * (kTile * 128) + r * 128 + ((c ^ (r & 7)) << 4);
+// 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled tile of 128-byte rows.
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return r * 128 + ((c ^ (r & 7)) << 4);
+}
+
+// Drain this warp's share of the dQ tile of query tile q0: TMEM -> registers
+// -> a private 32x32 fp32 shared-memory box -> TMA reduce-add into the
+// accumulator.  Arrives on `dqfree` once the TMEM columns have been read.
+template <int D>
+__device__ __forceinline__ void drain_dq(uint32_t tl_dq, uint8_t* stage, const CUtensorMap* tdq,
+                                         uint64_t* dqfree, int q_row0, int col0, int h, int b,
+                                         int lane) {
+  constexpr int kChunks = (D / 2) / 32;
+  uint32_t v[kChunks][32];
+#pragma unroll
+  for (int cc = 0; cc < kChunks; ++cc) tmem_ld32(tl_dq + cc * 32, v[cc]);
+  tmem_wait_ld();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(dqfree);
+#pragma unroll
+  for (int cc = 0; cc < kChunks; ++cc) {
+    if (lane == 0) tma_store_wait_read_all();   // the previous reduce has read the box
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4*>(stage + swz(lane, c)) =
+          make_uint4(v[cc][4 * c], v[cc][4 * c + 1], v[cc][4 * c + 2], v[cc][4 * c + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_reduce_add_4d(tdq, stage, col0 + cc * 32, q_row0, h, b);
+      tma_store_commit();
+    }
+  }
 }
 
 template <int D, bool DROPOUT>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                    const BwdArgs a) {
+                    const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
   using C = BwdCfg<D>;
   constexpr int ST = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -132,7 +170,8 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sV = sK + C::kTileBytes;
   uint8_t* sQ = sV + C::kTileBytes;                 // ST tiles
   uint8_t* sdO = sQ + ST * C::kTileBytes;           // ST tiles
-  uint8_t* sDS = sdO + ST * C::kTileBytes;          // dS^T [kv][q]
+  uint8_t* sDS = sdO + ST * C::kTileBytes;          // dS^T [kv][q], two 64-column boxes
+  uint8_t* sStage = sDS + C::kDsBytes;              // per compute warp, 4 KB
   __shared__ BwdCtl<ST> ctl;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -155,16 +194,16 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(&ctl.sfull, 1);
     mbar_init(&ctl.dpfull, 1);
-    mbar_init(&ctl.pfull, 4);
-    mbar_init(&ctl.dsfull, 4);
+    mbar_init(&ctl.pfull, kComputeWarps);
+    mbar_init(&ctl.dsfull, kComputeWarps);
     mbar_init(&ctl.dsfree, 1);
     mbar_init(&ctl.dqfull, 1);
-    mbar_init(&ctl.dqfree, 4);
+    mbar_init(&ctl.dqfree, kComputeWarps);
     mbar_init(&ctl.done, 1);
     mbar_init(&ctl.final_bar, 1);
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kComputeWarps + 1) {
     tmem_alloc(&ctl.tmem_base, 512);
     tmem_relinquish();
   }
@@ -174,7 +213,7 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = ctl.tmem_base;
   const WaitCtx wc{&ctl.abort_flag, a.status, a.timeout_ns};
 
-  if (warp == 8) {
+  if (warp == kComputeWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n > 0) {
       tma_prefetch_desc(&tq);
@@ -207,7 +246,7 @@ __global__ void __launch_bounds__(320, 1)
           mbar_wait_drain(&ctl.qfull[ii % ST], (ii / ST) & 1, a.timeout_ns);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kComputeWarps + 1) {
     // ------------------------------------------------------------- MMA issue
     if (lane == 0 && n > 0) {
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);   // K-major x K-major
@@ -244,13 +283,14 @@ __global__ void __launch_bounds__(320, 1)
                  smem_desc(do_base + off, 16, 1024), kIdSS, kk > 0 ? 1u : 0u);
         }
         mma_commit(&ctl.dpfull);
-        // dV += P~^T dO_i
+        // dV += P~^T dO_i; P~^T pairs of query rows 0..63 sit in columns
+        // [0,32), those of rows 64..127 in [64,96)
         ok = mbar_wait(&ctl.pfull, ph, wc, kSiteBwdMma);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + C::kDVCol, tmem + C::kSCol + kk * 8,
+          mma_ts(tmem + C::kDVCol, tmem + C::kSCol + kk * 8 + (kk >= 4 ? 32 : 0),
                  smem_desc(do_base + kk * 2048, C::kBoxBytes, 1024), kIdKN,
                  (i > 0 || kk > 0) ? 1u : 0u);
         // dK += dS^T Q_i
@@ -282,82 +322,90 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(&ctl.final_bar);
       mbar_wait_drain(&ctl.final_bar, 0, a.timeout_ns);
     }
-  } else if (warp < 4) {
-    // -------------------------------------------- P^T, dS^T; dK/dV epilogue
-    const int r = threadIdx.x;             // key row within the tile == TMEM lane
+  } else {
+    // -------------------------------------------------------------- compute
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;     // key row within the tile == TMEM lane
     const int kj = k0 + r;                 // global key index
     const bool key_ok = kj < limit;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int qc0 = half * 64;             // this warp's first query column
     const float c2 = a.scale_log2;
     const float ds = m.drop_scale;
     const float* lse = a.lse + static_cast<int64_t>(bh) * m.N;
     const float* dsum = a.Dsum + static_cast<int64_t>(bh) * m.N;
+    float* sLw = ctl.sL[warp];
+    float* sDw = ctl.sD[warp];
+    uint8_t* stage = sStage + warp * C::kStageBytes;
     bool ok = true;
     for (int i = 0; i < n; ++i) {
       const uint32_t ph = i & 1;
       const int qtile = tiles[i];
       const int q0 = qtile * kTile;
-      {   // each warp stages L (log2 units) and D of the query tile for itself
-        __syncwarp();   // the previous tile's values have been read
-#pragma unroll
-        for (int u = 0; u < kTile / 32; ++u) {
-          const int qq = q0 + u * 32 + lane;
-          float l2 = INFINITY, dv = 0.f;
-          if (qq < m.N) {
-            const float L = lse[qq];
-            l2 = (L == -INFINITY) ? INFINITY : L * kLog2e;
-            dv = dsum[qq];
-          }
-          ctl.sL[warp][u * 32 + lane] = l2;
-          ctl.sD[warp][u * 32 + lane] = dv;
-        }
-        __syncwarp();
+      if (i >= 1) {   // dQ of the previous query tile
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dqfull, (i - 1) & 1, wc, kSiteBwdDq));
+        if (!ok) break;
+        tc_fence_after();
+        drain_dq<D>(tl + C::kDQCol + half * C::kHalf, stage, &tdq, &ctl.dqfree,
+                    tiles[i - 1] * kTile + quarter * 32, half * C::kHalf, h, b, lane);
       }
+      // L (log2 units) and D of this warp's 64 query rows
+      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int qq = q0 + qc0 + u * 32 + lane;
+        float l2 = INFINITY, dv = 0.f;
+        if (qq < m.N) {
+          const float L = lse[qq];
+          l2 = (L == -INFINITY) ? INFINITY : L * kLog2e;
+          dv = dsum[qq];
+        }
+        sLw[u * 32 + lane] = l2;
+        sDw[u * 32 + lane] = dv;
+      }
+      __syncwarp();
       const bool diag = m.causal && qtile == kt;   // query q < key: masked
 
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl.sfull, ph, wc, kSiteBwdSoft));
       if (!ok) break;
       tc_fence_after();
-      // P^T row (bf16 pairs kept for dS), P~^T into TMEM columns [0, 64)
-      uint32_t pp[64];
-      uint32_t keepbits[4];
+      // P^T (bf16 pairs kept for dS) and P~^T into TMEM
+      uint32_t pp[32];
+      uint32_t keepbits[2];
 #pragma unroll
-      for (int c = 0; c < kTile; c += 32) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = qc0 + cc * 32;       // query column within the tile
         uint32_t sr[32];
         tmem_ld32(tl + C::kSCol + c, sr);
         tmem_wait_ld();
         uint32_t keep = 0xffffffffu;
         if constexpr (DROPOUT) {
           // element (query q, key kj): word kj mod 4 of the counter (kj/4, q, bh, offset)
-          keep = 0;
-#pragma unroll 4
-          for (int t = 0; t < 32; ++t) {
-            const uint32_t w4 = dropout_keep4(static_cast<uint32_t>(kj >> 2),
-                                              static_cast<uint32_t>(q0 + c + t),
-                                              static_cast<uint32_t>(bh), m.offset, m.seed_lo,
-                                              m.seed_hi, m.drop_threshold);
-            keep |= ((w4 >> (kj & 3)) & 1u) << t;
-          }
+          keep = dropout_keep32_by_key(static_cast<uint32_t>(kj), static_cast<uint32_t>(q0 + c),
+                                       static_cast<uint32_t>(bh), m.offset, m.seed_lo, m.seed_hi,
+                                       m.drop_threshold, static_cast<uint32_t>(lane));
         }
-        keepbits[c / 32] = keep;
+        keepbits[cc] = keep;
         uint32_t pk[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
           const int qa = c + t, qb = c + t + 1;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -ctl.sL[warp][qa]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[t + 1]), c2, -ctl.sL[warp][qb]));
+          float p0 = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -sLw[cc * 32 + t]));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sr[t + 1]), c2, -sLw[cc * 32 + t + 1]));
           if (!key_ok || (diag && qa < r)) p0 = 0.f;
           if (!key_ok || (diag && qb < r)) p1 = 0.f;
-          pp[(c + t) / 2] = pack_bf16x2(p0, p1);
+          pp[cc * 16 + t / 2] = pack_bf16x2(p0, p1);
           if constexpr (DROPOUT) {
             p0 = ((keep >> t) & 1u) ? p0 * ds : 0.f;
             p1 = ((keep >> (t + 1)) & 1u) ? p1 * ds : 0.f;
             pk[t / 2] = pack_bf16x2(p0, p1);
           } else {
-            pk[t / 2] = pp[(c + t) / 2];
+            pk[t / 2] = pp[cc * 16 + t / 2];
           }
         }
-        tmem_st16(tl + C::kSCol + c / 2, pk);
+        // pairs of query rows c .. c+31 -> column 64*half + 16*cc (within S^T's
+        // own half, already read by this warp)
+        tmem_st16(tl + C::kSCol + half * 64 + cc * 16, pk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -374,53 +422,60 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
       }
 #pragma unroll
-      for (int c = 0; c < kTile; c += 32) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t dr[32];
-        tmem_ld32(tl + C::kDPCol + c, dr);
+        tmem_ld32(tl + C::kDPCol + qc0 + cc * 32, dr);
         tmem_wait_ld();
-        const uint32_t keep = keepbits[c / 32];
+        const uint32_t keep = keepbits[cc];
         uint32_t pk[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
-          const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[(c + t) / 2]));
+          const float2 p =
+              __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[cc * 16 + t / 2]));
           float d0 = __uint_as_float(dr[t]), d1 = __uint_as_float(dr[t + 1]);
           if constexpr (DROPOUT) {
             d0 = ((keep >> t) & 1u) ? d0 * ds : 0.f;
             d1 = ((keep >> (t + 1)) & 1u) ? d1 * ds : 0.f;
           }
-          const float s0 = p.x * (d0 - ctl.sD[warp][c + t]);
-          const float s1 = p.y * (d1 - ctl.sD[warp][c + t + 1]);
-          pk[t / 2] = pack_bf16x2(s0, s1);
+          pk[t / 2] = pack_bf16x2(p.x * (d0 - sDw[cc * 32 + t]), p.y * (d1 - sDw[cc * 32 + t + 1]));
         }
+        uint8_t* box = sDS + half * C::kBoxBytes;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t off = ds_offset(r, (c >> 3) + u);
-          *reinterpret_cast<uint4*>(sDS + off) =
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<uint4*>(box + swz(r, cc * 4 + u)) =
               make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.dsfull);
     }
+    if (ok && n > 0) {   // dQ of the last query tile
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dqfull, (n - 1) & 1, wc, kSiteBwdDq));
+      if (ok) {
+        tc_fence_after();
+        drain_dq<D>(tl + C::kDQCol + half * C::kHalf, stage, &tdq, &ctl.dqfree,
+                    tiles[n - 1] * kTile + quarter * 32, half * C::kHalf, h, b, lane);
+      }
+    }
 
-    // epilogue: dV and c*dK rows of this key tile
+    // epilogue: dV and c*dK, this warp's rows and half of the columns
     if (ok && n > 0) {
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl.done, 0, wc, kSiteBwdSoft));
       if (ok) tc_fence_after();
     }
     if (ok) {
-      const int64_t row_off = b * a.stride_b + h * a.stride_h + static_cast<int64_t>(kj) * a.stride_n;
+      const int64_t row_off =
+          b * a.stride_b + h * a.stride_h + static_cast<int64_t>(kj) * a.stride_n + half * C::kHalf;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(which ? a.dk : a.dv) + row_off;
         const float mul = which ? a.scale : 1.f;
 #pragma unroll
-        for (int c = 0; c < D; c += 32) {
+        for (int c = 0; c < C::kHalf; c += 32) {
           uint32_t o[32];
           if (n > 0) {
-            tmem_ld32(tl + (which ? C::kDKCol : C::kDVCol) + c, o);
+            tmem_ld32(tl + (which ? C::kDKCol : C::kDVCol) + half * C::kHalf + c, o);
             tmem_wait_ld();
           } else {
 #pragma unroll
@@ -440,41 +495,12 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
-  } else {
-    // ------------------------------------------------------- dQ drain (4-7)
-    const int r = threadIdx.x - 128;       // query row within the tile == TMEM lane
-    const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    float* acc_head = a.dq_acc + static_cast<int64_t>(bh) * m.N * D;
-    for (int i = 0; i < n; ++i) {
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dqfull, i & 1, wc, kSiteBwdDq));
-      if (!ok) break;
-      tc_fence_after();
-      const int qq = tiles[i] * kTile + r;
-      float4* dst = reinterpret_cast<float4*>(acc_head + static_cast<int64_t>(qq) * D);
-#pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tl + C::kDQCol + c, v);
-        tmem_wait_ld();
-        if (c + 32 >= D) {   // last chunk read: the MMA may reuse the columns
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl.dqfree);
-        }
-        if (qq < m.N) {
-#pragma unroll
-          for (int t = 0; t < 32; t += 4)
-            atomicAdd(dst + (c + t) / 4,
-                      make_float4(__uint_as_float(v[t]), __uint_as_float(v[t + 1]),
-                                  __uint_as_float(v[t + 2]), __uint_as_float(v[t + 3])));
-        }
-      }
-    }
+    if (lane == 0) tma_store_wait_all();   // this warp's reduce-adds are complete
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kComputeWarps + 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -550,7 +576,8 @@ cudaError_t launch_main(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s) 
     attr_set = true;
   }
   const unsigned grid = static_cast<unsigned>(a.m.nb) * a.m.B * a.m.H;
-  bwd_bf16_kernel<D, DROP><<<grid, C::kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, tm.dout, a);
+  bwd_bf16_kernel<D, DROP><<<grid, C::kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, tm.dout,
+                                                                 tm.dq_acc, a);
   return cudaGetLastError();
 }
 

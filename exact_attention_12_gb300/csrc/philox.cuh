@@ -42,4 +42,30 @@ __device__ __forceinline__ uint32_t dropout_keep4(uint32_t g, uint32_t i, uint32
          (u.z >= threshold ? 4u : 0u) | (u.w >= threshold ? 8u : 0u);
 }
 
+// Keep bits of the 32 query rows q0 .. q0+31 for key kj, where the four
+// lanes of an aligned lane quad hold the four keys 4g .. 4g+3 (kj mod 4 ==
+// lane mod 4).  One Philox call at query q yields the words of all four
+// keys, so each lane evaluates the 8 queries q0 + 4s + (lane mod 4) and the
+// quad exchanges the results: 8 calls per lane instead of 32.  Bit t of the
+// result is 1 iff (q0 + t, kj) is kept.  All 32 lanes must call it.
+__device__ __forceinline__ uint32_t dropout_keep32_by_key(uint32_t kj, uint32_t q0, uint32_t bh,
+                                                          uint32_t offset, uint32_t seed_lo,
+                                                          uint32_t seed_hi, uint32_t threshold,
+                                                          uint32_t lane) {
+  const uint32_t u = lane & 3u;
+  uint32_t mine = 0;   // bit 4s + x: key 4g+x kept at query q0 + 4s + u
+#pragma unroll
+  for (uint32_t s = 0; s < 8; ++s)
+    mine |= dropout_keep4(kj >> 2, q0 + 4 * s + u, bh, offset, seed_lo, seed_hi, threshold)
+            << (4 * s);
+  uint32_t keep = 0;
+#pragma unroll
+  for (uint32_t src = 0; src < 4; ++src) {
+    const uint32_t m = __shfl_sync(0xffffffffu, mine, (lane & ~3u) | src);
+#pragma unroll
+    for (uint32_t s = 0; s < 8; ++s) keep |= ((m >> (4 * s + u)) & 1u) << (4 * s + src);
+  }
+  return keep;
+}
+
 }  // namespace attn
