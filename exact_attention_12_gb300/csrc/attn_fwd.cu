@@ -2,28 +2,39 @@
 //
 // Method: the tiled forward of FlashAttention (paper summary page, "Theo dõi
 // Softmax tăng dần" and its four per-block steps; the "3.3 Self-Attention"
-// page, §12.2 Tiling and §12.3 Online Softmax).  Each CTA owns one 128-row
-// query tile Q_i of one (b, h) and streams the allowed 128-row key/value
-// tiles K_j, V_j past it (query-outer order, §12.5 of the same page), keeping
-// the running row max m and exp-sum l on chip; only O and the per-row
-// logsumexp L = c*m + ln l are written.
+// page, §12.2 Tiling and §12.3 Online Softmax).  Query tiles of 128 rows
+// stream the allowed 128-row key/value tiles past them (query-outer order,
+// §12.5 of the same page), keeping the running row max m and exp-sum l on
+// chip; only O and the per-row logsumexp L = c*m + ln l are written.
 //
-// GB300 mapping (differs from the pages' A100 design: no B_r/B_c from the
-// SRAM size; tiles are sized by TMEM and the 128-lane MMA):
-//   warp 4      TMA producer: Q_i once, then K_j / V_j into a ring of
-//               kStages shared-memory stages (128-byte swizzle).
-//   warp 5      MMA issuer (one thread): S_j = Q_i K_j^T into one of two TMEM
-//               S buffers, then O += P_j V_j with P_j read from TMEM.  S_{j+1}
-//               is issued before O += P_j V_j so the tensor core works on the
-//               next scores while the softmax warps handle the current ones.
-//   warps 0-3   softmax: thread t owns row t (TMEM lane t).  Loads its S row,
-//               applies the masks, updates m, rescales O in TMEM only when
-//               the max grew by more than 2^8 (lazy rescale; the final O/l
-//               is exact either way), computes P = 2^(S*c*log2e - m*c*log2e)
-//               with ex2, applies the dropout keep mask, packs P to bf16 into
-//               TMEM, and in the epilogue writes O / l and L.
-// TMEM columns: S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384)
-//               O [384, 384 + d).
+// GB300 mapping (the pages' A100 block sizes B_r/B_c from the SRAM size do
+// not apply: tiles are sized by the 128-lane MMA and TMEM):
+//   * One CTA owns a pair of query tiles A = 2u and B = 2u+1 of one (b, h)
+//     and walks the union of their key-tile lists once; K_j / V_j are loaded
+//     once for both tiles.  A key tile that only one of the two needs (the
+//     causal diagonal, block-sparse lists) is skipped by the other.
+//   * warp 8     TMA producer: Q_A, Q_B once, then K_j / V_j into a ring of
+//                kStages shared-memory stages (128-byte swizzle).
+//   * warp 9     MMA issuer (one thread) in the order
+//                  ... O_A += P_A V_t, S_A = Q_A K_{t+1}^T, O_B += P_B V_t,
+//                  S_B = Q_B K_{t+1}^T ...
+//                so each tile's softmax runs while the tensor core works on
+//                the other tile: the two tiles ping-pong.
+//   * warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread t
+//                owns row t of its tile (TMEM lane t).  Pass 1 reads the S
+//                row from TMEM for the masked row max; if the max grew by
+//                more than 2^8 the row's O is rescaled in TMEM (lazy rescale;
+//                the final O / l is exact either way); pass 2 re-reads S,
+//                forms P = 2^(S c log2e - m c log2e) with ex2, applies the
+//                dropout keep mask and writes P as bf16 over the first 64
+//                columns of S, where O += P V reads it.
+//   Because every tcgen05.commit covers all earlier MMAs of the issuing
+//   thread, "S_X(t+1) is complete" already implies "O_X += P_X V_t is
+//   complete": the softmax may then overwrite P_X and rescale O_X.
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256, 256+d),
+//               O_B [256+d, 256+2d).
+#include <climits>
+
 #include <cuda_bf16.h>
 
 #include "attn_kernels.cuh"
@@ -43,17 +54,17 @@ struct FwdCfg {
   static constexpr int kBoxBytes = kTile * 128;       // 128 rows x 128 bytes
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kStages = (D == 64) ? 4 : 2;
-  static constexpr int kSmem = 1024 + kTileBytes * (1 + 2 * kStages);
-  static constexpr uint32_t kSCol = 0, kPCol = 256, kOCol = 384;
-  static constexpr int kThreads = 192;
+  static constexpr int kSmem = 1024 + kTileBytes * (2 + 2 * kStages);
+  static constexpr uint32_t kSCol = 0, kOCol = 256;   // S_X at kSCol + 128X, O_X at kOCol + D*X
+  static constexpr int kThreads = 320;
 };
 
 template <int ST>
 struct FwdCtl {
   uint64_t qfull;
   uint64_t kfull[ST], vfull[ST], kvempty[ST];
-  uint64_t sfull[2], sfree[2], pfull[2], pvdone[2];
-  uint64_t final_bar;
+  uint64_t sfull[2], pfull[2];
+  uint64_t done, final_bar;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -72,6 +83,7 @@ __device__ __forceinline__ int key_limit(const MaskArgs& m, int b) {
 }
 
 __device__ __forceinline__ TileList fwd_tiles(const MaskArgs& m, int qt, int bh, int limit) {
+  if (qt >= m.nb) return TileList{nullptr, 0};   // past the last query tile
   int cap = (limit + kTile - 1) / kTile;
   if (m.causal) cap = min(cap, qt + 1);
   TileList t{nullptr, cap};
@@ -89,8 +101,46 @@ __device__ __forceinline__ TileList fwd_tiles(const MaskArgs& m, int qt, int bh,
   return t;
 }
 
+// Walks the union of two sorted key-tile lists in ascending order.
+struct PairWalk {
+  TileList a, b;
+  int ia = 0, ib = 0;
+  __device__ __forceinline__ bool next(int& j, bool& na, bool& nb) {
+    const int ja = ia < a.n ? a[ia] : INT_MAX;
+    const int jb = ib < b.n ? b[ib] : INT_MAX;
+    if (ja == INT_MAX && jb == INT_MAX) return false;
+    j = min(ja, jb);
+    na = ja == j;
+    nb = jb == j;
+    ia += na ? 1 : 0;
+    ib += nb ? 1 : 0;
+    return true;
+  }
+};
+
+template <int D>
+__device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint32_t q_base, uint32_t k_base) {
+  constexpr uint32_t kId = idesc_bf16(128, 128, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * FwdCfg<D>::kBoxBytes + (kk & 3) * 32;
+    mma_ss(d_tmem, smem_desc(q_base + off, 16, 1024), smem_desc(k_base + off, 16, 1024), kId,
+           kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void mma_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_base,
+                                       bool accumulate) {
+  constexpr uint32_t kId = idesc_bf16(128, D, false, true);
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk)
+    mma_ts(o_tmem, p_tmem + kk * 8, smem_desc(v_base + kk * 2048, FwdCfg<D>::kBoxBytes, 1024),
+           kId, (accumulate || kk > 0) ? 1u : 0u);
+}
+
 template <int D, bool DROPOUT>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
   using C = FwdCfg<D>;
@@ -98,21 +148,22 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK = smem + C::kTileBytes;
+  uint8_t* sQ = smem;                          // Q_A, Q_B
+  uint8_t* sK = smem + 2 * C::kTileBytes;
   uint8_t* sV = sK + ST * C::kTileBytes;
   __shared__ FwdCtl<ST> ctl;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const MaskArgs& m = a.m;
   const int BH = m.B * m.H;
-  const int qt = m.nb - 1 - static_cast<int>(blockIdx.x / BH);   // heaviest tiles first
+  const int npairs = (m.nb + 1) / 2;
+  const int pair = npairs - 1 - static_cast<int>(blockIdx.x / BH);   // heaviest pairs first
   const int bh = static_cast<int>(blockIdx.x % BH);
   const int b = bh / m.H, h = bh - b * m.H;
-  const int q0 = qt * kTile;
   const int limit = key_limit(m, b);
-  const TileList tiles = fwd_tiles(m, qt, bh, limit);
-  const int n = tiles.n;
+  const TileList listA = fwd_tiles(m, 2 * pair, bh, limit);
+  const TileList listB = fwd_tiles(m, 2 * pair + 1, bh, limit);
+  const bool any = listA.n > 0 || listB.n > 0;
 
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
@@ -122,16 +173,15 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&ctl.vfull[s], 1);
       mbar_init(&ctl.kvempty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&ctl.sfull[s], 1);
-      mbar_init(&ctl.sfree[s], 4);
-      mbar_init(&ctl.pfull[s], 4);
-      mbar_init(&ctl.pvdone[s], 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&ctl.sfull[x], 1);
+      mbar_init(&ctl.pfull[x], 4);
     }
+    mbar_init(&ctl.done, 1);
     mbar_init(&ctl.final_bar, 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&ctl.tmem_base, 512);
     tmem_relinquish();
   }
@@ -141,21 +191,26 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = ctl.tmem_base;
   const WaitCtx wc{&ctl.abort_flag, a.status, a.timeout_ns};
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n > 0) {
+    if (lane == 0 && any) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      mbar_arrive_expect_tx(&ctl.qfull, C::kTileBytes);
+      mbar_arrive_expect_tx(&ctl.qfull, 2 * C::kTileBytes);
 #pragma unroll
-      for (int x = 0; x < C::kBoxes; ++x)
-        tma_load_4d(sQ + x * C::kBoxBytes, &tq, &ctl.qfull, x * 64, q0, h, b);
-      int j = 0;
-      for (; j < n; ++j) {
-        const int s = j % ST;
-        if (j >= ST && !mbar_wait(&ctl.kvempty[s], ((j / ST) - 1) & 1, wc, kSiteFwdKvEmpty)) break;
-        const int kv0 = tiles[j] * kTile;
+      for (int x = 0; x < C::kBoxes; ++x) {
+        tma_load_4d(sQ + x * C::kBoxBytes, &tq, &ctl.qfull, x * 64, 2 * pair * kTile, h, b);
+        tma_load_4d(sQ + C::kTileBytes + x * C::kBoxBytes, &tq, &ctl.qfull, x * 64,
+                    (2 * pair + 1) * kTile, h, b);
+      }
+      PairWalk walk{listA, listB};
+      int j, t = 0;
+      bool na, nb;
+      while (walk.next(j, na, nb)) {
+        const int s = t % ST;
+        if (t >= ST && !mbar_wait(&ctl.kvempty[s], ((t / ST) - 1) & 1, wc, kSiteFwdKvEmpty)) break;
+        const int kv0 = j * kTile;
         uint8_t* dk = sK + s * C::kTileBytes;
         uint8_t* dv = sV + s * C::kTileBytes;
         mbar_arrive_expect_tx(&ctl.kfull[s], C::kTileBytes);
@@ -166,98 +221,119 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int x = 0; x < C::kBoxes; ++x)
           tma_load_4d(dv + x * C::kBoxBytes, &tv, &ctl.vfull[s], x * 64, kv0, h, b);
+        ++t;
       }
       if (ctl.abort_flag) {   // let issued copies land before the CTA exits
         mbar_wait_drain(&ctl.qfull, 0, a.timeout_ns);
-        for (int jj = max(0, j - ST); jj < j; ++jj) {
-          mbar_wait_drain(&ctl.kfull[jj % ST], (jj / ST) & 1, a.timeout_ns);
-          mbar_wait_drain(&ctl.vfull[jj % ST], (jj / ST) & 1, a.timeout_ns);
+        for (int tt = max(0, t - ST); tt < t; ++tt) {
+          mbar_wait_drain(&ctl.kfull[tt % ST], (tt / ST) & 1, a.timeout_ns);
+          mbar_wait_drain(&ctl.vfull[tt % ST], (tt / ST) & 1, a.timeout_ns);
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------- MMA issue
-    if (lane == 0 && n > 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);
-      const uint32_t q_base = smem_u32(sQ);
+    if (lane == 0 && any) {
+      const uint32_t q_base[2] = {smem_u32(sQ), smem_u32(sQ + C::kTileBytes)};
+      uint32_t cnt[2] = {0, 0};   // tiles each query tile has started
       bool ok = mbar_wait(&ctl.qfull, 0, wc, kSiteFwdQ);
-      for (int j = 0; ok && j <= n; ++j) {
-        if (j < n) {
-          const int s = j % ST, bb = j & 1;
-          ok = mbar_wait(&ctl.kfull[s], (j / ST) & 1, wc, kSiteFwdK);
-          if (ok && j >= 2) ok = mbar_wait(&ctl.sfree[bb], ((j - 2) >> 1) & 1, wc, kSiteFwdSFree);
-          if (!ok) break;
+      PairWalk walk{listA, listB};
+      int j;
+      bool need[2], need_next[2];
+      bool have = walk.next(j, need[0], need[1]);
+      // prologue: scores of the first key tile
+      if (ok && have) {
+        ok = mbar_wait(&ctl.kfull[0], 0, wc, kSiteFwdK);
+        if (ok) {
           tc_fence_after();
-          const uint32_t k_base = smem_u32(sK + s * C::kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-            mma_ss(tmem + C::kSCol + bb * 128, smem_desc(q_base + off, 16, 1024),
-                   smem_desc(k_base + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&ctl.sfull[bb]);
-        }
-        if (j >= 1) {
-          const int jj = j - 1, s = jj % ST, bb = jj & 1;
-          ok = mbar_wait(&ctl.pfull[bb], (jj >> 1) & 1, wc, kSiteFwdPFull) &&
-               mbar_wait(&ctl.vfull[s], (jj / ST) & 1, wc, kSiteFwdV);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t v_base = smem_u32(sV + s * C::kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            mma_ts(tmem + C::kOCol, tmem + C::kPCol + bb * 64 + kk * 8,
-                   smem_desc(v_base + kk * 2048, C::kBoxBytes, 1024), kIdO,
-                   (jj > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&ctl.pvdone[bb]);
-          mma_commit(&ctl.kvempty[s]);
+          for (int x = 0; x < 2; ++x)
+            if (need[x]) {
+              mma_scores<D>(tmem + C::kSCol + 128 * x, q_base[x], smem_u32(sK));
+              mma_commit(&ctl.sfull[x]);
+            }
         }
       }
+      for (int t = 0; ok && have; ++t) {
+        const int s = t % ST;
+        const int s1 = (t + 1) % ST;
+        int jn;
+        const bool have_next = walk.next(jn, need_next[0], need_next[1]);
+        bool k_next_ready = false, v_ready = false;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (need[x]) {   // O_X += P_X V_t
+            ok = mbar_wait(&ctl.pfull[x], cnt[x] & 1, wc, kSiteFwdPFull);
+            if (ok && !v_ready) ok = v_ready = mbar_wait(&ctl.vfull[s], (t / ST) & 1, wc, kSiteFwdV);
+            if (!ok) break;
+            tc_fence_after();
+            mma_pv<D>(tmem + C::kOCol + D * x, tmem + C::kSCol + 128 * x,
+                      smem_u32(sV + s * C::kTileBytes), cnt[x] > 0);
+            ++cnt[x];
+          }
+          if (x == 1) mma_commit(&ctl.kvempty[s]);   // K_t, V_t no longer needed
+          if (have_next && need_next[x]) {   // S_X = Q_X K_{t+1}^T
+            if (!k_next_ready) {
+              ok = k_next_ready = mbar_wait(&ctl.kfull[s1], ((t + 1) / ST) & 1, wc, kSiteFwdK);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            mma_scores<D>(tmem + C::kSCol + 128 * x, q_base[x], smem_u32(sK + s1 * C::kTileBytes));
+            mma_commit(&ctl.sfull[x]);
+          }
+        }
+        j = jn;
+        need[0] = need_next[0];
+        need[1] = need_next[1];
+        have = have_next;
+      }
+      if (ok) mma_commit(&ctl.done);
       mma_commit(&ctl.final_bar);   // every MMA of this CTA done before TMEM is freed
       mbar_wait_drain(&ctl.final_bar, 0, a.timeout_ns);
     }
   } else {
     // ---------------------------------------------------- softmax, epilogue
-    const int row = threadIdx.x;   // == TMEM lane == row within the tile
+    const int x = warp >> 2;                        // query tile: 0 = A, 1 = B
+    const int row = (warp & 3) * 32 + lane;         // TMEM lane == row within the tile
+    const int q0 = (2 * pair + x) * kTile;
     const int qi = q0 + row;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const TileList tiles = x ? listB : listA;
+    const int n = tiles.n;
+    const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t sc = tl + C::kSCol + 128 * x;    // this tile's S (and P) columns
+    const uint32_t oc = tl + C::kOCol + D * x;      // this tile's O columns
     const float c2 = a.scale_log2;
     float m_used = -INFINITY;      // raw-score max the exponentials are taken against
     float l_sum = 0.f;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int bb = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.sfull[bb], (j >> 1) & 1, wc, kSiteFwdSFull));
+    for (int jj = 0; jj < n; ++jj) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.sfull[x], jj & 1, wc, kSiteFwdSFull));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tl + C::kSCol + bb * 128 + c * 32, sr + c * 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.sfree[bb]);
-
-      const int kv0 = tiles[j] * kTile;
+      const int kv0 = tiles[jj] * kTile;
       const int col_lim = min(limit - kv0, kTile);
       const bool diag = m.causal && kv0 == q0;
-      if (col_lim < kTile || diag) {
-        const int lim = diag ? min(col_lim, row + 1) : col_lim;
+      const bool masked = col_lim < kTile || diag;
+      const int lim = diag ? min(col_lim, row + 1) : col_lim;
+      // pass 1: masked row max
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
-      }
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+      for (int c = 0; c < 128; c += 32) {
+        uint32_t sr[32];
+        tmem_ld32(sc + c, sr);
+        tmem_wait_ld();
+        if (masked) {
 #pragma unroll
-      for (int c = 0; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
-        mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
-        mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
-        mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+          for (int t = 0; t < 32; ++t)
+            if (c + t >= lim) sr[t] = __float_as_uint(-INFINITY);
+        }
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          mx0 = fmaxf(mx0, __uint_as_float(sr[t]));
+          mx1 = fmaxf(mx1, __uint_as_float(sr[t + 1]));
+        }
       }
-      const float m_new = fmaxf(m_used, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
+      const float m_new = fmaxf(m_used, fmaxf(mx0, mx1));
       const bool need =
           m_new > m_used && (m_used == -INFINITY || (m_new - m_used) * c2 > kRescaleTau);
       float alpha = 1.f;
@@ -266,32 +342,26 @@ __global__ void __launch_bounds__(192, 1)
         m_used = m_new;
         l_sum *= alpha;
       }
-      if (j >= 1 && __any_sync(0xffffffffu, need)) {
-        // O holds P_0 V_0 + ... + P_{j-1} V_{j-1} once that MMA is done
-        ok = __all_sync(0xffffffffu, mbar_wait(&ctl.pvdone[(j - 1) & 1], ((j - 1) >> 1) & 1, wc,
-                                               kSiteFwdPvDone));
-        if (!ok) break;
-        tc_fence_after();
+      if (jj >= 1 && __any_sync(0xffffffffu, need)) {
+        // O holds the sum through the previous key tile (complete: see above)
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
           uint32_t o[32];
-          tmem_ld32(tl + C::kOCol + c, o);
+          tmem_ld32(oc + c, o);
           tmem_wait_ld();
 #pragma unroll
           for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-          tmem_st32(tl + C::kOCol + c, o);
+          tmem_st32(oc + c, o);
         }
       }
-      if (j >= 2) {   // P buffer bb was last read by O += P_{j-2} V_{j-2}
-        ok = __all_sync(0xffffffffu, mbar_wait(&ctl.pvdone[bb], ((j - 2) >> 1) & 1, wc,
-                                               kSiteFwdPvDone));
-        if (!ok) break;
-        tc_fence_after();
-      }
+      // pass 2: P = 2^(S c2 - m c2), bf16 over the first 64 columns of S
       const float mc = (m_used == -INFINITY) ? 0.f : m_used * c2;
       float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
       for (int c = 0; c < 128; c += 32) {
+        uint32_t sr[32];
+        tmem_ld32(sc + c, sr);
+        tmem_wait_ld();
         uint32_t keep = 0xffffffffu;
         if constexpr (DROPOUT) {
           keep = 0;
@@ -305,8 +375,9 @@ __global__ void __launch_bounds__(192, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[c + t]), c2, -mc));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + t + 1]), c2, -mc));
+          const bool v0 = !masked || c + t < lim, v1 = !masked || c + t + 1 < lim;
+          float p0 = v0 ? ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -mc)) : 0.f;
+          float p1 = v1 ? ex2_approx(fmaf(__uint_as_float(sr[t + 1]), c2, -mc)) : 0.f;
           ls0 += p0;
           ls1 += p1;
           if constexpr (DROPOUT) {
@@ -315,21 +386,20 @@ __global__ void __launch_bounds__(192, 1)
           }
           pk[t / 2] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(tl + C::kPCol + bb * 64 + c / 2, pk);
+        tmem_st16(sc + c / 2, pk);   // S columns [c/2, c/2+16) were read already
       }
       l_sum += ls0 + ls1;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.pfull[bb]);
+      if (lane == 0) mbar_arrive(&ctl.pfull[x]);
     }
 
-    if (ok && n > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.pvdone[(n - 1) & 1], ((n - 1) >> 1) & 1, wc,
-                                             kSiteFwdPvDone));
+    if (ok && any) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.done, 0, wc, kSiteFwdPvDone));
       if (ok) tc_fence_after();
     }
-    if (ok) {
+    if (ok && q0 < m.N) {
       const bool live = l_sum > 0.f;
       const float inv = live ? m.drop_scale / l_sum : 0.f;
       const float L = live ? (m_used * c2 + __log2f(l_sum)) * kLn2 : -INFINITY;
@@ -339,7 +409,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
         if (n > 0) {
-          tmem_ld32(tl + C::kOCol + c, o);
+          tmem_ld32(oc + c, o);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -362,7 +432,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -378,7 +448,7 @@ cudaError_t launch_one(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const unsigned grid = static_cast<unsigned>(a.m.nb) * a.m.B * a.m.H;
+  const unsigned grid = static_cast<unsigned>((a.m.nb + 1) / 2) * a.m.B * a.m.H;
   fwd_bf16_kernel<D, DROP><<<grid, C::kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, a);
   return cudaGetLastError();
 }
