@@ -169,13 +169,14 @@ class Step:
         self.abi.check_status(st, "attn_fwd")
         if ev:
             ev[1].record(stream)
-        st = lib.attn_bwd_preprocess(P, self.o.data_ptr(), self.do.data_ptr(), wsp, wsn, s)
+        st = lib.attn_bwd_preprocess(P, self.o.data_ptr(), self.lse.data_ptr(), self.do.data_ptr(),
+                                     wsp, wsn, s)
         self.abi.check_status(st, "attn_bwd_preprocess")
         if ev:
             ev[2].record(stream)
         st = lib.attn_bwd_main(P, self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
-                               self.lse.data_ptr(), self.do.data_ptr(), self.dk.data_ptr(),
-                               self.dv.data_ptr(), wsp, wsn, s)
+                               self.do.data_ptr(), self.dk.data_ptr(), self.dv.data_ptr(),
+                               wsp, wsn, s)
         self.abi.check_status(st, "attn_bwd_main")
         if ev:
             ev[3].record(stream)

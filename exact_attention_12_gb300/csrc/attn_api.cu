@@ -38,7 +38,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
   size_t list_cnt = 0, list_idx = 0;   // compacted block mask (0 = none)
-  size_t dsum = 0, dq_acc = 0;         // backward only
+  size_t lse2 = 0, dsum = 0, dq_acc = 0;   // backward only
   size_t total = 0;
 };
 
@@ -59,8 +59,11 @@ WsLayout layout(const attn_params* p, bool bwd) {
     off = round_up(off + masks * nb * nb * sizeof(uint16_t), 256);
   }
   if (bwd) {
+    const size_t bhpad = static_cast<size_t>(p->B) * p->H * nb * kTile;
+    L.lse2 = off;
+    off = round_up(off + bhpad * sizeof(float), 256);
     L.dsum = off;
-    off = round_up(off + bhn * sizeof(float), 256);
+    off = round_up(off + bhpad * sizeof(float), 256);
     L.dq_acc = off;
     off = round_up(off + bhn * p->d * sizeof(float), 256);
   }
@@ -207,6 +210,18 @@ attn::MaskArgs mask_args(const attn_params* p, const WsLayout& L, char* ws, bool
 
 bool empty_problem(const attn_params* p) { return p->B == 0 || p->H == 0 || p->N == 0; }
 
+// Heads per scheduling group: as many as keep `bytes_per_head` of re-read
+// operands within a share of the 129 MB L2.  Causal work is not grouped: its
+// tiles differ in length, and a group's long tiles starting late would leave
+// a tail; longest-first over all heads balances better.
+int head_group(const attn_params* p, double bytes_per_head) {
+  const double budget = 48.0 * 1024 * 1024;
+  const int bh = p->B * p->H;
+  if (p->causal) return bh > 0 ? bh : 1;
+  const int g = static_cast<int>(budget / (bytes_per_head > 1.0 ? bytes_per_head : 1.0));
+  return g < 1 ? 1 : (g > bh ? bh : g);
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 
 }  // namespace
@@ -231,6 +246,7 @@ attn_status attn_fwd(const attn_params* p, const void* q, const void* k, const v
 
   attn::FwdArgs a{};
   a.m = mask_args(p, L, w, false);
+  a.m.head_group = head_group(p, 4.0 * p->N * p->d);   // K and V, bf16
   a.d = p->d;
   a.scale = p->scale;
   a.scale_log2 = p->scale * kLog2e;
@@ -276,10 +292,13 @@ attn_status bwd_setup(const attn_params* p, void* ws, size_t ws_bytes, attn::Bwd
   *L = layout(p, true);
   *a = attn::BwdArgs{};
   a->m = mask_args(p, *L, w, true);
+  a->m.head_group = head_group(p, 8.0 * p->N * p->d);   // Q, dO bf16 + dQ accumulator fp32
   a->d = p->d;
   a->scale = p->scale;
   a->scale_log2 = p->scale * kLog2e;
-  a->Dsum = reinterpret_cast<const float*>(w + L->dsum);
+  a->lse2 = reinterpret_cast<float*>(w + L->lse2);
+  a->dsum = reinterpret_cast<float*>(w + L->dsum);
+  a->npad = a->m.nb * kTile;
   a->dq_acc = reinterpret_cast<float*>(w + L->dq_acc);
   a->stride_b = p->stride_b;
   a->stride_h = p->stride_h;
@@ -293,30 +312,30 @@ attn_status bwd_setup(const attn_params* p, void* ws, size_t ws_bytes, attn::Bwd
 
 extern "C" {
 
-attn_status attn_bwd_preprocess(const attn_params* p, const void* o, const void* dout, void* ws,
-                                size_t ws_bytes, void* stream) {
+attn_status attn_bwd_preprocess(const attn_params* p, const void* o, const float* lse,
+                                const void* dout, void* ws, size_t ws_bytes, void* stream) {
   attn::BwdArgs a;
   WsLayout L;
   attn_status st = bwd_setup(p, ws, ws_bytes, &a, &L);
   if (st != ATTN_OK) return st;
   if (empty_problem(p)) return ATTN_OK;
-  if ((st = check_ptrs({o, dout})) != ATTN_OK) return st;
+  if ((st = check_ptrs({o, lse, dout})) != ATTN_OK) return st;
+  a.lse = lse;
   const cudaError_t e = attn::launch_bwd_preprocess(o, dout, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "backward preprocess launch");
 }
 
 attn_status attn_bwd_main(const attn_params* p, const void* q, const void* k, const void* v,
-                          const float* lse, const void* dout, void* dk, void* dv, void* ws,
-                          size_t ws_bytes, void* stream) {
+                          const void* dout, void* dk, void* dv, void* ws, size_t ws_bytes,
+                          void* stream) {
   attn::BwdArgs a;
   WsLayout L;
   attn_status st = bwd_setup(p, ws, ws_bytes, &a, &L);
   if (st != ATTN_OK) return st;
   if (empty_problem(p)) return ATTN_OK;
-  if ((st = check_ptrs({q, k, v, lse, dout, dk, dv})) != ATTN_OK) return st;
+  if ((st = check_ptrs({q, k, v, dout, dk, dv})) != ATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
-  a.lse = lse;
   a.dk = dk;
   a.dv = dv;
   attn::TensorMaps tm{};
@@ -362,8 +381,8 @@ attn_status attn_bwd(const attn_params* p, const void* q, const void* k, const v
   if (st != ATTN_OK) return st;
   if (empty_problem(p)) return ATTN_OK;
   if ((st = check_ptrs({q, k, v, o, lse, dout, dq, dk, dv})) != ATTN_OK) return st;
-  if ((st = attn_bwd_preprocess(p, o, dout, ws, ws_bytes, stream)) != ATTN_OK) return st;
-  if ((st = attn_bwd_main(p, q, k, v, lse, dout, dk, dv, ws, ws_bytes, stream)) != ATTN_OK)
+  if ((st = attn_bwd_preprocess(p, o, lse, dout, ws, ws_bytes, stream)) != ATTN_OK) return st;
+  if ((st = attn_bwd_main(p, q, k, v, dout, dk, dv, ws, ws_bytes, stream)) != ATTN_OK)
     return st;
   return attn_bwd_dq(p, dq, ws, ws_bytes, stream);
 }

@@ -25,7 +25,7 @@
 //                    accumulator with TMA bulk reduce-adds.
 //   dq_convert       dQ = c * accumulator -> bf16.
 //
-// Warp roles of bwd_kernel (320 threads):
+// Warp roles of bwd_kernel (384 threads; registers re-split with setmaxnreg):
 //   warps 0-7  compute: warp w owns key rows 32*(w%4) .. +31 (TMEM lanes) and
 //              query columns 64*(w/4) .. +63 of the S^T / dP^T tiles.  The
 //              backward needs no row reduction, so the 128 columns of a row
@@ -33,7 +33,8 @@
 //              dropout mask, P~^T into TMEM, dS^T into shared memory, and the
 //              drain of the previous dQ tile; epilogue writes dK, dV.
 //   warp 8     TMA producer (K_j, V_j once; Q_i, dO_i per query tile).
-//   warp 9     MMA issuer, TMEM owner.
+//   warp 9     MMA issuer, TMEM owner.  (warps 10-11 idle: they complete the
+//              third warpgroup, whose registers go to the compute warps.)
 // TMEM columns: S^T [0,128) -- P~^T (bf16 pairs) overwrites columns [0,32)
 //   and [64,96), each half by the warps that read that half of S^T --,
 //   dP^T [128,256), dV [256,256+d), dK [256+d,256+2d), dQ [384,448) for
@@ -60,13 +61,18 @@ struct BwdCfg {
   static constexpr int kStages = (D == 64) ? 2 : 1;          // Q_i / dO_i stages
   static constexpr int kDsBytes = kTile * kTile * 2;          // dS^T tile, bf16
   static constexpr int kStageBytes = 32 * 32 * 4;             // per-warp dQ staging
+  static constexpr int kLDBytes = 2 * kTile * 4;              // L*log2e and D of a query tile
   static constexpr int kSmem = 1024 + 2 * kTileBytes + 2 * kStages * kTileBytes + kDsBytes +
-                               kComputeWarps * kStageBytes;
+                               kComputeWarps * kStageBytes + kStages * kLDBytes;
   static constexpr uint32_t kSCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 256 + D;
   static constexpr uint32_t kDQCol = (D == 64) ? 384 : 128;
   static constexpr bool kDqAliasesDp = (D == 128);
   static constexpr int kHalf = D / 2;                         // dQ/dK/dV columns per warp
-  static constexpr int kThreads = (kComputeWarps + 2) * 32;
+  // warpgroups 0, 1: compute; warpgroup 2: producer (warp 8), MMA issuer
+  // (warp 9), two idle warps.  Registers are re-split after the start:
+  // 256 * kRegsCompute + 128 * kRegsOther <= 384 * kRegsLaunch.
+  static constexpr int kThreads = 384;
+  static constexpr uint32_t kRegsLaunch = 168, kRegsCompute = 208, kRegsOther = 80;
 };
 
 template <int ST>
@@ -75,9 +81,6 @@ struct BwdCtl {
   uint64_t qfull[ST], qempty[ST];
   uint64_t sfull, dpfull, pfull, dsfull, dsfree, dqfull, dqfree, done;
   uint64_t final_bar;
-  float sL[kComputeWarps][64];   // per compute warp: L * log2(e) of its 64 query rows
-                                 // (+inf: the row contributes nothing)
-  float sD[kComputeWarps][64];   // per compute warp: D of its 64 query rows
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -157,7 +160,7 @@ __device__ __forceinline__ void drain_dq(uint32_t tl_dq, uint8_t* stage, const C
 }
 
 template <int D, bool DROPOUT>
-__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+__global__ void __launch_bounds__(384, 1)
     bwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                     const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
@@ -172,13 +175,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   uint8_t* sdO = sQ + ST * C::kTileBytes;           // ST tiles
   uint8_t* sDS = sdO + ST * C::kTileBytes;          // dS^T [kv][q], two 64-column boxes
   uint8_t* sStage = sDS + C::kDsBytes;              // per compute warp, 4 KB
+  float* sLD = reinterpret_cast<float*>(sStage + kComputeWarps * C::kStageBytes);   // ST x 256
   __shared__ BwdCtl<ST> ctl;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const MaskArgs& m = a.m;
   const int BH = m.B * m.H;
-  const int kt = static_cast<int>(blockIdx.x / BH);   // heaviest (earliest) key tiles first
-  const int bh = static_cast<int>(blockIdx.x % BH);
+  // head groups of G consecutive (b, h); within a group, key tiles in
+  // ascending order (heaviest first for causal)
+  int kt, bh;
+  {
+    const int G = m.head_group, per = G * m.nb, nfull = BH / G;
+    const int w = static_cast<int>(blockIdx.x);
+    const int g = w < nfull * per ? w / per : nfull;
+    const int gs = g < nfull ? G : BH - nfull * G;
+    const int rem = w - g * per;
+    kt = rem / gs;
+    bh = g * G + rem % gs;
+  }
   const int b = bh / m.H, h = bh - b * m.H;
   const int k0 = kt * kTile;
   const int limit = key_limit(m, b);
@@ -212,7 +226,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   const WaitCtx wc{&ctl.abort_flag, a.status, a.timeout_ns};
+  const int wg = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 128, 0);
 
+  if (wg == 2) {
+    regs_decrease<C::kRegsOther>();
   if (warp == kComputeWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n > 0) {
@@ -231,7 +248,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const int s = i % ST;
         if (i >= ST && !mbar_wait(&ctl.qempty[s], ((i / ST) - 1) & 1, wc, kSiteBwdEmpty)) break;
         const int q0 = tiles[i] * kTile;
-        mbar_arrive_expect_tx(&ctl.qfull[s], 2 * C::kTileBytes);
+        mbar_arrive_expect_tx(&ctl.qfull[s], 2 * C::kTileBytes + C::kLDBytes);
 #pragma unroll
         for (int x = 0; x < C::kBoxes; ++x) {
           tma_load_4d(sQ + s * C::kTileBytes + x * C::kBoxBytes, &tq, &ctl.qfull[s], x * 64, q0,
@@ -239,6 +256,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           tma_load_4d(sdO + s * C::kTileBytes + x * C::kBoxBytes, &tdo, &ctl.qfull[s], x * 64,
                       q0, h, b);
         }
+        const int64_t row = static_cast<int64_t>(bh) * a.npad + q0;
+        bulk_load(sLD + s * 2 * kTile, a.lse2 + row, kTile * 4, &ctl.qfull[s]);
+        bulk_load(sLD + s * 2 * kTile + kTile, a.dsum + row, kTile * 4, &ctl.qfull[s]);
       }
       if (ctl.abort_flag) {   // let issued copies land before the CTA exits
         mbar_wait_drain(&ctl.kvfull, 0, a.timeout_ns);
@@ -322,7 +342,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mma_commit(&ctl.final_bar);
       mbar_wait_drain(&ctl.final_bar, 0, a.timeout_ns);
     }
+  }
   } else {
+    regs_increase<C::kRegsCompute>();
     // -------------------------------------------------------------- compute
     const int quarter = warp & 3, half = warp >> 2;
     const int r = quarter * 32 + lane;     // key row within the tile == TMEM lane
@@ -332,10 +354,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int qc0 = half * 64;             // this warp's first query column
     const float c2 = a.scale_log2;
     const float ds = m.drop_scale;
-    const float* lse = a.lse + static_cast<int64_t>(bh) * m.N;
-    const float* dsum = a.Dsum + static_cast<int64_t>(bh) * m.N;
-    float* sLw = ctl.sL[warp];
-    float* sDw = ctl.sD[warp];
     uint8_t* stage = sStage + warp * C::kStageBytes;
     bool ok = true;
     for (int i = 0; i < n; ++i) {
@@ -349,21 +367,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         drain_dq<D>(tl + C::kDQCol + half * C::kHalf, stage, &tdq, &ctl.dqfree,
                     tiles[i - 1] * kTile + quarter * 32, half * C::kHalf, h, b, lane);
       }
-      // L (log2 units) and D of this warp's 64 query rows
-      __syncwarp();
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int qq = q0 + qc0 + u * 32 + lane;
-        float l2 = INFINITY, dv = 0.f;
-        if (qq < m.N) {
-          const float L = lse[qq];
-          l2 = (L == -INFINITY) ? INFINITY : L * kLog2e;
-          dv = dsum[qq];
-        }
-        sLw[u * 32 + lane] = l2;
-        sDw[u * 32 + lane] = dv;
-      }
-      __syncwarp();
+      // L (log2 units) and D of this warp's 64 query rows, staged by the producer
+      const float* sLw = sLD + (i % ST) * 2 * kTile + qc0;
+      const float* sDw = sLw + kTile;
       const bool diag = m.causal && qtile == kt;   // query q < key: masked
 
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl.sfull, ph, wc, kSiteBwdSoft));
@@ -372,12 +378,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // P^T (bf16 pairs kept for dS) and P~^T into TMEM
       uint32_t pp[32];
       uint32_t keepbits[2];
+      uint32_t srr[64];
+      tmem_ld32(tl + C::kSCol + qc0, srr);
+      tmem_ld32(tl + C::kSCol + qc0 + 32, srr + 32);
+      tmem_wait_ld();
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c = qc0 + cc * 32;       // query column within the tile
-        uint32_t sr[32];
-        tmem_ld32(tl + C::kSCol + c, sr);
-        tmem_wait_ld();
+        const uint32_t* sr = srr + cc * 32;
         uint32_t keep = 0xffffffffu;
         if constexpr (DROPOUT) {
           // element (query q, key kj): word kj mod 4 of the counter (kj/4, q, bh, offset)
@@ -421,11 +429,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         if (!ok) break;
         tc_fence_after();
       }
+      uint32_t drr[64];
+      tmem_ld32(tl + C::kDPCol + qc0, drr);
+      tmem_ld32(tl + C::kDPCol + qc0 + 32, drr + 32);
+      tmem_wait_ld();
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        uint32_t dr[32];
-        tmem_ld32(tl + C::kDPCol + qc0 + cc * 32, dr);
-        tmem_wait_ld();
+        const uint32_t* dr = drr + cc * 32;
         const uint32_t keep = keepbits[cc];
         uint32_t pk[16];
 #pragma unroll
@@ -506,20 +516,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   }
 }
 
-// D = rowsum(dO * O) (one row per group of d/8 lanes) and dQacc = 0.
+// Per query row of the padded [B*H][npad] layout (one row per group of d/8
+// lanes): D = rowsum(dO * O) and L * log2(e) (+inf for padding rows and rows
+// with no allowed key, so they contribute nothing); and dQacc = 0.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                             const __nv_bfloat16* __restrict__ dout,
                                                             const BwdArgs a) {
   constexpr int kLanes = D / 8;                 // lanes per row
-  const int64_t rows = static_cast<int64_t>(a.m.B) * a.m.H * a.m.N;
+  const int64_t rows = static_cast<int64_t>(a.m.B) * a.m.H * a.npad;
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t row = gtid / kLanes;
   const int part = static_cast<int>(gtid % kLanes);
+  const int64_t n = row % a.npad;
+  const int64_t bh = row / a.npad;
+  const bool real = row < rows && n < a.m.N;
   float s = 0.f;
-  if (row < rows) {
-    const int64_t n = row % a.m.N;
-    const int64_t bh = row / a.m.N;
+  if (real) {
     const int64_t b = bh / a.m.H, h = bh % a.m.H;
     const int64_t off = b * a.stride_b + h * a.stride_h + n * a.stride_n + part * 8;
     const uint4 ov = *reinterpret_cast<const uint4*>(o + off);
@@ -535,9 +548,17 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
   }
 #pragma unroll
   for (int w = kLanes / 2; w > 0; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
-  if (row < rows && part == 0) const_cast<float*>(a.Dsum)[row] = s;
+  if (row < rows && part == 0) {
+    float l2 = INFINITY;
+    if (real) {
+      const float L = a.lse[bh * a.m.N + n];
+      if (L != -INFINITY) l2 = L * kLog2e;
+    }
+    a.dsum[row] = s;
+    a.lse2[row] = l2;
+  }
   // zero the dQ accumulator
-  const int64_t n4 = rows * D / 4;
+  const int64_t n4 = static_cast<int64_t>(a.m.B) * a.m.H * a.m.N * D / 4;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   float4* acc = reinterpret_cast<float4*>(a.dq_acc);
   for (int64_t e = gtid; e < n4; e += stride) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -573,6 +594,10 @@ cudaError_t launch_main(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s) 
     cudaError_t e = cudaFuncSetAttribute(bwd_bf16_kernel<D, DROP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
+    // the register re-split inside the kernel assumes the launch allocation
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, bwd_bf16_kernel<D, DROP>)) != cudaSuccess) return e;
+    if (static_cast<uint32_t>(fa.numRegs) < C::kRegsLaunch) return cudaErrorInvalidConfiguration;
     attr_set = true;
   }
   const unsigned grid = static_cast<unsigned>(a.m.nb) * a.m.B * a.m.H;
@@ -590,7 +615,7 @@ unsigned blocks_for(int64_t threads) {
 
 cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const BwdArgs& a,
                                   cudaStream_t s) {
-  const int64_t rows = static_cast<int64_t>(a.m.B) * a.m.H * a.m.N;
+  const int64_t rows = static_cast<int64_t>(a.m.B) * a.m.H * a.npad;
   const unsigned grid = blocks_for(rows * (a.d / 8));
   if (a.d == 64)
     bwd_preprocess_kernel<64><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),

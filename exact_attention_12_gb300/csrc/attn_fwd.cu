@@ -21,13 +21,14 @@
 //                so each tile's softmax runs while the tensor core works on
 //                the other tile: the two tiles ping-pong.
 //   * warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread t
-//                owns row t of its tile (TMEM lane t).  Pass 1 reads the S
-//                row from TMEM for the masked row max; if the max grew by
-//                more than 2^8 the row's O is rescaled in TMEM (lazy rescale;
-//                the final O / l is exact either way); pass 2 re-reads S,
-//                forms P = 2^(S c log2e - m c log2e) with ex2, applies the
-//                dropout keep mask and writes P as bf16 over the first 64
-//                columns of S, where O += P V reads it.
+//                owns row t of its tile (TMEM lane t).  It loads its whole
+//                S row from TMEM into registers (four loads in flight), takes
+//                the masked row max; if the max grew by more than 2^8 the
+//                row's O is rescaled in TMEM (lazy rescale; the final O / l is
+//                exact either way); then forms P = 2^(S c log2e - m c log2e)
+//                (packed f32x2 FMA, ex2), applies the dropout keep mask and
+//                writes P as bf16 over the first 64 columns of S, where
+//                O += P V reads it.
 //   Because every tcgen05.commit covers all earlier MMAs of the issuing
 //   thread, "S_X(t+1) is complete" already implies "O_X += P_X V_t is
 //   complete": the softmax may then overwrite P_X and rescale O_X.
@@ -56,7 +57,12 @@ struct FwdCfg {
   static constexpr int kStages = (D == 64) ? 4 : 2;
   static constexpr int kSmem = 1024 + kTileBytes * (2 + 2 * kStages);
   static constexpr uint32_t kSCol = 0, kOCol = 256;   // S_X at kSCol + 128X, O_X at kOCol + D*X
-  static constexpr int kThreads = 320;
+  // warpgroups 0, 1: softmax of tiles A, B; warpgroup 2: producer (warp 8),
+  // MMA issuer (warp 9), two idle warps.  Registers are re-split after the
+  // start: kRegsSoftmax for the softmax warpgroups, kRegsOther for the rest;
+  // 256 * 208 + 128 * 80 <= 384 * kRegsLaunch.
+  static constexpr int kThreads = 384;
+  static constexpr uint32_t kRegsLaunch = 168, kRegsSoftmax = 208, kRegsOther = 80;
 };
 
 template <int ST>
@@ -140,7 +146,7 @@ __device__ __forceinline__ void mma_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_
 }
 
 template <int D, bool DROPOUT>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
   using C = FwdCfg<D>;
@@ -157,8 +163,17 @@ __global__ void __launch_bounds__(320, 1)
   const MaskArgs& m = a.m;
   const int BH = m.B * m.H;
   const int npairs = (m.nb + 1) / 2;
-  const int pair = npairs - 1 - static_cast<int>(blockIdx.x / BH);   // heaviest pairs first
-  const int bh = static_cast<int>(blockIdx.x % BH);
+  // head groups of G consecutive (b, h); within a group, heaviest pairs first
+  int pair, bh;
+  {
+    const int G = m.head_group, per = G * npairs, nfull = BH / G;
+    const int w = static_cast<int>(blockIdx.x);
+    const int g = w < nfull * per ? w / per : nfull;
+    const int gs = g < nfull ? G : BH - nfull * G;
+    const int rem = w - g * per;
+    pair = npairs - 1 - rem / gs;
+    bh = g * G + rem % gs;
+  }
   const int b = bh / m.H, h = bh - b * m.H;
   const int limit = key_limit(m, b);
   const TileList listA = fwd_tiles(m, 2 * pair, bh, limit);
@@ -190,7 +205,9 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   const WaitCtx wc{&ctl.abort_flag, a.status, a.timeout_ns};
-
+  const int wg = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 128, 0);
+  if (wg == 2) {
+    regs_decrease<C::kRegsOther>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && any) {
@@ -291,7 +308,9 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(&ctl.final_bar);   // every MMA of this CTA done before TMEM is freed
       mbar_wait_drain(&ctl.final_bar, 0, a.timeout_ns);
     }
+  }
   } else {
+    regs_increase<C::kRegsSoftmax>();
     // ---------------------------------------------------- softmax, epilogue
     const int x = warp >> 2;                        // query tile: 0 = A, 1 = B
     const int row = (warp & 3) * 32 + lane;         // TMEM lane == row within the tile
@@ -313,27 +332,26 @@ __global__ void __launch_bounds__(320, 1)
       const int kv0 = tiles[jj] * kTile;
       const int col_lim = min(limit - kv0, kTile);
       const bool diag = m.causal && kv0 == q0;
-      const bool masked = col_lim < kTile || diag;
-      const int lim = diag ? min(col_lim, row + 1) : col_lim;
-      // pass 1: masked row max
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+      // the whole S row: four loads in flight, one wait
+      uint32_t sr[128];
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) {
-        uint32_t sr[32];
-        tmem_ld32(sc + c, sr);
-        tmem_wait_ld();
-        if (masked) {
+      for (int c = 0; c < 128; c += 32) tmem_ld32(sc + c, sr + c);
+      tmem_wait_ld();
+      if (col_lim < kTile || diag) {
+        const int lim = diag ? min(col_lim, row + 1) : col_lim;
 #pragma unroll
-          for (int t = 0; t < 32; ++t)
-            if (c + t >= lim) sr[t] = __float_as_uint(-INFINITY);
-        }
-#pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          mx0 = fmaxf(mx0, __uint_as_float(sr[t]));
-          mx1 = fmaxf(mx1, __uint_as_float(sr[t + 1]));
-        }
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      const float m_new = fmaxf(m_used, fmaxf(mx0, mx1));
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; c += 8) {
+        mx0 = max3f(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+        mx1 = max3f(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+        mx2 = max3f(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+        mx3 = max3f(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+      }
+      const float m_new = max3f(m_used, max3f(mx0, mx1, mx2), mx3);
       const bool need =
           m_new > m_used && (m_used == -INFINITY || (m_new - m_used) * c2 > kRescaleTau);
       float alpha = 1.f;
@@ -354,18 +372,17 @@ __global__ void __launch_bounds__(320, 1)
           tmem_st32(oc + c, o);
         }
       }
-      // pass 2: P = 2^(S c2 - m c2), bf16 over the first 64 columns of S
+      // P = 2^(S c2 - m c2) (masked entries are -inf: 2^-inf = 0), bf16 over
+      // the first 64 columns of S
       const float mc = (m_used == -INFINITY) ? 0.f : m_used * c2;
-      float ls0 = 0.f, ls1 = 0.f;
+      const uint64_t c2x2 = f2_pack(c2, c2), nmc2 = f2_pack(-mc, -mc);
+      uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
       for (int c = 0; c < 128; c += 32) {
-        uint32_t sr[32];
-        tmem_ld32(sc + c, sr);
-        tmem_wait_ld();
         uint32_t keep = 0xffffffffu;
         if constexpr (DROPOUT) {
           keep = 0;
-#pragma unroll
+#pragma unroll 1
           for (int g = 0; g < 8; ++g)
             keep |= dropout_keep4(static_cast<uint32_t>((kv0 + c) / 4 + g), static_cast<uint32_t>(qi),
                                   static_cast<uint32_t>(bh), m.offset, m.seed_lo, m.seed_hi,
@@ -374,20 +391,31 @@ __global__ void __launch_bounds__(320, 1)
         }
         uint32_t pk[16];
 #pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          const bool v0 = !masked || c + t < lim, v1 = !masked || c + t + 1 < lim;
-          float p0 = v0 ? ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -mc)) : 0.f;
-          float p1 = v1 ? ex2_approx(fmaf(__uint_as_float(sr[t + 1]), c2, -mc)) : 0.f;
-          ls0 += p0;
-          ls1 += p1;
+        for (int t = 0; t < 32; t += 4) {
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c + t]), __uint_as_float(sr[c + t + 1])),
+                           c2x2, nmc2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c + t + 2]), __uint_as_float(sr[c + t + 3])),
+                           c2x2, nmc2), x2, x3);
+          float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+          acc0 = f2_add(acc0, f2_pack(p0, p1));
+          acc1 = f2_add(acc1, f2_pack(p2, p3));
           if constexpr (DROPOUT) {
             p0 = ((keep >> t) & 1u) ? p0 : 0.f;
             p1 = ((keep >> (t + 1)) & 1u) ? p1 : 0.f;
+            p2 = ((keep >> (t + 2)) & 1u) ? p2 : 0.f;
+            p3 = ((keep >> (t + 3)) & 1u) ? p3 : 0.f;
           }
           pk[t / 2] = pack_bf16x2(p0, p1);
+          pk[t / 2 + 1] = pack_bf16x2(p2, p3);
         }
-        tmem_st16(sc + c / 2, pk);   // S columns [c/2, c/2+16) were read already
+        tmem_st16(sc + c / 2, pk);   // S columns [c/2, c/2+16) are already in registers
       }
+      float ls0, ls1, ls2, ls3;
+      f2_unpack(acc0, ls0, ls1);
+      f2_unpack(acc1, ls2, ls3);
+      ls0 += ls2;
+      ls1 += ls3;
       l_sum += ls0 + ls1;
       tmem_wait_st();
       tc_fence_before();
@@ -446,6 +474,10 @@ cudaError_t launch_one(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, DROP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
+    // the register re-split inside the kernel assumes the launch allocation
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, fwd_bf16_kernel<D, DROP>)) != cudaSuccess) return e;
+    if (static_cast<uint32_t>(fa.numRegs) < C::kRegsLaunch) return cudaErrorInvalidConfiguration;
     attr_set = true;
   }
   const unsigned grid = static_cast<unsigned>((a.m.nb + 1) / 2) * a.m.B * a.m.H;

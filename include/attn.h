@@ -114,21 +114,21 @@ attn_status attn_bwd(const attn_params* p, const void* q, const void* k,
 
 /* The three stages attn_bwd runs, callable one by one on the same workspace
  * (for callers that schedule or time them separately):
- *   attn_bwd_preprocess  D = rowsum(dO * O) into the workspace; zeroes the
- *                        workspace's fp32 dQ accumulator.
+ *   attn_bwd_preprocess  D = rowsum(dO * O) and L * log2(e) into the
+ *                        workspace (rows padded to a multiple of 128);
+ *                        zeroes the workspace's fp32 dQ accumulator.
  *   attn_bwd_main        the fused recomputing backward: dK, dV written,
- *                        dQ accumulated into the workspace.  Needs the
- *                        preprocess of the same call sequence.
+ *                        dQ accumulated into the workspace.  Reads what the
+ *                        preprocess of the same call sequence wrote.
  *   attn_bwd_dq          dQ = scale * accumulator, converted to bf16.
  * Arguments mean the same as for attn_bwd; the workspace must be the same
  * and at least attn_workspace_size(p, 1) bytes. */
 attn_status attn_bwd_preprocess(const attn_params* p, const void* o,
-                                const void* dout, void* ws, size_t ws_bytes,
-                                void* stream);
+                                const float* lse, const void* dout, void* ws,
+                                size_t ws_bytes, void* stream);
 attn_status attn_bwd_main(const attn_params* p, const void* q, const void* k,
-                          const void* v, const float* lse, const void* dout,
-                          void* dk, void* dv, void* ws, size_t ws_bytes,
-                          void* stream);
+                          const void* v, const void* dout, void* dk, void* dv,
+                          void* ws, size_t ws_bytes, void* stream);
 attn_status attn_bwd_dq(const attn_params* p, void* dq, void* ws,
                         size_t ws_bytes, void* stream);
 
