@@ -226,6 +226,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 }  // namespace
 
+int attn::record_error(int status, const char* msg) {
+  return static_cast<int>(fail(static_cast<attn_status>(status), "%s", msg));
+}
+
 extern "C" {
 
 size_t attn_workspace_size(const attn_params* p, int for_backward) {

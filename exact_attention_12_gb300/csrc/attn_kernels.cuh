@@ -87,4 +87,8 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const BwdArgs
 cudaError_t launch_bwd_bf16(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_dq_convert(void* dq, const BwdArgs& a, cudaStream_t s);
 
+// Records `msg` as the calling thread's last error (what attn_last_error()
+// returns) and passes `status` through.
+int record_error(int status, const char* msg);
+
 }  // namespace attn

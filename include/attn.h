@@ -132,6 +132,31 @@ attn_status attn_bwd_main(const attn_params* p, const void* q, const void* k,
 attn_status attn_bwd_dq(const attn_params* p, void* dq, void* ws,
                         size_t ws_bytes, void* stream);
 
+/* Backward without a caller workspace.  The pages have no counterpart: this
+ * is an interface for callers that cannot allocate device memory (a plug-in
+ * inside a host application that owns all device allocations, a runtime with
+ * a fixed device-memory budget, a latency-critical loop where cudaMalloc
+ * could synchronise the device).  Arguments and results are those of
+ * attn_bwd; the scratch attn_bwd would take from `ws` comes from a 64 MiB
+ * array built into the library, which every GPU that loads the library holds
+ * until the process exits.
+ *   - Problems needing more than 64 MiB of scratch (attn_workspace_size(p, 1))
+ *     are rejected with ATTN_ERR_WORKSPACE before anything is enqueued.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current and caches it; make that
+ *     first call before any stream capture.
+ *   - All calls share the one array and it keeps the previous call's
+ *     contents: calls that overlap on the GPU (other streams, other host
+ *     threads) race with each other.  The call clears the status words and
+ *     rewrites everything else it reads.
+ *   - A device-side time-out is recorded in the built-in array's status words,
+ *     which callers cannot pass to attn_check; it is cleared by the next call. */
+attn_status attn_bwd_noalloc(const attn_params* p, const void* q,
+                             const void* k, const void* v, const void* o,
+                             const float* lse, const void* dout, void* dq,
+                             void* dk, void* dv, void* stream);
+
 /* Synchronises `stream`, returns the workspace's device status (ATTN_OK or
  * ATTN_ERR_TIMEOUT) and clears it. */
 attn_status attn_check(void* ws, void* stream);
