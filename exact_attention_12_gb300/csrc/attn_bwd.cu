@@ -58,12 +58,12 @@ struct BwdCfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kBoxBytes = kTile * 128;
   static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kStages = (D == 64) ? 2 : 1;          // Q_i / dO_i stages
+  static constexpr int kQStages = 2;                         // Q_i (+ its L, D) stages
+  static constexpr int kDoStages = (D == 64) ? 2 : 1;        // dO_i stages
   static constexpr int kDsBytes = kTile * kTile * 2;          // dS^T tile, bf16
-  static constexpr int kStageBytes = 32 * 32 * 4;             // per-warp dQ staging
   static constexpr int kLDBytes = 2 * kTile * 4;              // L*log2e and D of a query tile
-  static constexpr int kSmem = 1024 + 2 * kTileBytes + 2 * kStages * kTileBytes + kDsBytes +
-                               kComputeWarps * kStageBytes + kStages * kLDBytes;
+  static constexpr int kSmem = 1024 + 2 * kTileBytes + kQStages * kTileBytes +
+                               kDoStages * kTileBytes + kDsBytes + kQStages * kLDBytes;
   static constexpr uint32_t kSCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 256 + D;
   static constexpr uint32_t kDQCol = (D == 64) ? 384 : 128;
   static constexpr bool kDqAliasesDp = (D == 128);
@@ -75,11 +75,10 @@ struct BwdCfg {
   static constexpr uint32_t kRegsLaunch = 168, kRegsCompute = 208, kRegsOther = 80;
 };
 
-template <int ST>
 struct BwdCtl {
   uint64_t kvfull;
-  uint64_t qfull[ST], qempty[ST];
-  uint64_t sfull, dpfull, pfull, dsfull, dsfree, dqfull, dqfree, done;
+  uint64_t qfull[2], qempty[2], dofull[2], doempty[2];
+  uint64_t sfull, dpfull, pfull, dsfull, dqfull, dqfree, done;
   uint64_t final_bar;
   uint32_t tmem_base;
   int abort_flag;
@@ -127,9 +126,10 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return r * 128 + ((c ^ (r & 7)) << 4);
 }
 
-// Drain this warp's share of the dQ tile of query tile q0: TMEM -> registers
-// -> a private 32x32 fp32 shared-memory box -> TMA reduce-add into the
-// accumulator.  Arrives on `dqfree` once the TMEM columns have been read.
+// Drain this warp's share of a dQ tile: TMEM -> registers -> the warp's 4 KB
+// region of shared memory (32 rows x 32 fp32, 128-byte swizzle) -> TMA
+// reduce-add into the accumulator, 32 columns at a time.  Arrives on
+// `dqfree` once the TMEM columns have been read.
 template <int D>
 __device__ __forceinline__ void drain_dq(uint32_t tl_dq, uint8_t* stage, const CUtensorMap* tdq,
                                          uint64_t* dqfree, int q_row0, int col0, int h, int b,
@@ -144,7 +144,7 @@ __device__ __forceinline__ void drain_dq(uint32_t tl_dq, uint8_t* stage, const C
   if (lane == 0) mbar_arrive(dqfree);
 #pragma unroll
   for (int cc = 0; cc < kChunks; ++cc) {
-    if (lane == 0) tma_store_wait_read_all();   // the previous reduce has read the box
+    if (lane == 0) tma_store_wait_read_all();   // the previous reduce has read the region
     __syncwarp();
 #pragma unroll
     for (int c = 0; c < 8; ++c)
@@ -159,24 +159,36 @@ __device__ __forceinline__ void drain_dq(uint32_t tl_dq, uint8_t* stage, const C
   }
 }
 
+template <int D>
+__device__ __forceinline__ void mma_kt_qt(uint32_t d_tmem, uint32_t a_base, uint32_t b_base) {
+  // D[128 x 128] = A[128 x D] B[128 x D]^T, both K-major (K = D)
+  constexpr uint32_t kId = idesc_bf16(128, 128, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * BwdCfg<D>::kBoxBytes + (kk & 3) * 32;
+    mma_ss(d_tmem, smem_desc(a_base + off, 16, 1024), smem_desc(b_base + off, 16, 1024), kId,
+           kk > 0 ? 1u : 0u);
+  }
+}
+
 template <int D, bool DROPOUT>
 __global__ void __launch_bounds__(384, 1)
     bwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                     const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
   using C = BwdCfg<D>;
-  constexpr int ST = C::kStages;
+  constexpr int QS = C::kQStages, DS = C::kDoStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sK = smem;
   uint8_t* sV = sK + C::kTileBytes;
-  uint8_t* sQ = sV + C::kTileBytes;                 // ST tiles
-  uint8_t* sdO = sQ + ST * C::kTileBytes;           // ST tiles
-  uint8_t* sDS = sdO + ST * C::kTileBytes;          // dS^T [kv][q], two 64-column boxes
-  uint8_t* sStage = sDS + C::kDsBytes;              // per compute warp, 4 KB
-  float* sLD = reinterpret_cast<float*>(sStage + kComputeWarps * C::kStageBytes);   // ST x 256
-  __shared__ BwdCtl<ST> ctl;
+  uint8_t* sQ = sV + C::kTileBytes;                 // QS tiles
+  uint8_t* sdO = sQ + QS * C::kTileBytes;           // DS tiles
+  uint8_t* sDS = sdO + DS * C::kTileBytes;          // dS^T [kv][q], two 64-column boxes;
+                                                    // also the dQ staging area
+  float* sLD = reinterpret_cast<float*>(sDS + C::kDsBytes);   // QS x (L2[128], D[128])
+  __shared__ BwdCtl ctl;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const MaskArgs& m = a.m;
@@ -202,15 +214,16 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
     mbar_init(&ctl.kvfull, 1);
-    for (int s = 0; s < ST; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&ctl.qfull[s], 1);
       mbar_init(&ctl.qempty[s], 1);
+      mbar_init(&ctl.dofull[s], 1);
+      mbar_init(&ctl.doempty[s], 1);
     }
     mbar_init(&ctl.sfull, 1);
     mbar_init(&ctl.dpfull, 1);
     mbar_init(&ctl.pfull, kComputeWarps);
     mbar_init(&ctl.dsfull, kComputeWarps);
-    mbar_init(&ctl.dsfree, 1);
     mbar_init(&ctl.dqfull, 1);
     mbar_init(&ctl.dqfree, kComputeWarps);
     mbar_init(&ctl.done, 1);
@@ -230,119 +243,132 @@ __global__ void __launch_bounds__(384, 1)
 
   if (wg == 2) {
     regs_decrease<C::kRegsOther>();
-  if (warp == kComputeWarps) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && n > 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-      tma_prefetch_desc(&tdo);
-      mbar_arrive_expect_tx(&ctl.kvfull, 2 * C::kTileBytes);
-#pragma unroll
-      for (int x = 0; x < C::kBoxes; ++x) {
-        tma_load_4d(sK + x * C::kBoxBytes, &tk, &ctl.kvfull, x * 64, k0, h, b);
-        tma_load_4d(sV + x * C::kBoxBytes, &tv, &ctl.kvfull, x * 64, k0, h, b);
-      }
-      int i = 0;
-      for (; i < n; ++i) {
-        const int s = i % ST;
-        if (i >= ST && !mbar_wait(&ctl.qempty[s], ((i / ST) - 1) & 1, wc, kSiteBwdEmpty)) break;
-        const int q0 = tiles[i] * kTile;
-        mbar_arrive_expect_tx(&ctl.qfull[s], 2 * C::kTileBytes + C::kLDBytes);
+    if (warp == kComputeWarps) {
+      // ---------------------------------------------------------- producer
+      if (lane == 0 && n > 0) {
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+        tma_prefetch_desc(&tdo);
+        mbar_arrive_expect_tx(&ctl.kvfull, 2 * C::kTileBytes);
 #pragma unroll
         for (int x = 0; x < C::kBoxes; ++x) {
-          tma_load_4d(sQ + s * C::kTileBytes + x * C::kBoxBytes, &tq, &ctl.qfull[s], x * 64, q0,
-                      h, b);
-          tma_load_4d(sdO + s * C::kTileBytes + x * C::kBoxBytes, &tdo, &ctl.qfull[s], x * 64,
-                      q0, h, b);
+          tma_load_4d(sK + x * C::kBoxBytes, &tk, &ctl.kvfull, x * 64, k0, h, b);
+          tma_load_4d(sV + x * C::kBoxBytes, &tv, &ctl.kvfull, x * 64, k0, h, b);
         }
-        const int64_t row = static_cast<int64_t>(bh) * a.npad + q0;
-        bulk_load(sLD + s * 2 * kTile, a.lse2 + row, kTile * 4, &ctl.qfull[s]);
-        bulk_load(sLD + s * 2 * kTile + kTile, a.dsum + row, kTile * 4, &ctl.qfull[s]);
+        int iq = 0, id = 0;   // Q / dO tiles issued
+        bool ok = true;
+        for (int i = 0; ok && i < n; ++i) {
+          const int q0 = tiles[i] * kTile;
+          const int sq = i % QS;
+          if (i >= QS && !(ok = mbar_wait(&ctl.qempty[sq], ((i / QS) - 1) & 1, wc, kSiteBwdEmpty)))
+            break;
+          mbar_arrive_expect_tx(&ctl.qfull[sq], C::kTileBytes + C::kLDBytes);
+#pragma unroll
+          for (int x = 0; x < C::kBoxes; ++x)
+            tma_load_4d(sQ + sq * C::kTileBytes + x * C::kBoxBytes, &tq, &ctl.qfull[sq], x * 64,
+                        q0, h, b);
+          const int64_t row = static_cast<int64_t>(bh) * a.npad + q0;
+          bulk_load(sLD + sq * 2 * kTile, a.lse2 + row, kTile * 4, &ctl.qfull[sq]);
+          bulk_load(sLD + sq * 2 * kTile + kTile, a.dsum + row, kTile * 4, &ctl.qfull[sq]);
+          ++iq;
+          const int sd = i % DS;
+          if (i >= DS && !(ok = mbar_wait(&ctl.doempty[sd], ((i / DS) - 1) & 1, wc, kSiteBwdEmpty)))
+            break;
+          mbar_arrive_expect_tx(&ctl.dofull[sd], C::kTileBytes);
+#pragma unroll
+          for (int x = 0; x < C::kBoxes; ++x)
+            tma_load_4d(sdO + sd * C::kTileBytes + x * C::kBoxBytes, &tdo, &ctl.dofull[sd],
+                        x * 64, q0, h, b);
+          ++id;
+        }
+        if (ctl.abort_flag) {   // let issued copies land before the CTA exits
+          mbar_wait_drain(&ctl.kvfull, 0, a.timeout_ns);
+          for (int ii = max(0, iq - QS); ii < iq; ++ii)
+            mbar_wait_drain(&ctl.qfull[ii % QS], (ii / QS) & 1, a.timeout_ns);
+          for (int ii = max(0, id - DS); ii < id; ++ii)
+            mbar_wait_drain(&ctl.dofull[ii % DS], (ii / DS) & 1, a.timeout_ns);
+        }
       }
-      if (ctl.abort_flag) {   // let issued copies land before the CTA exits
-        mbar_wait_drain(&ctl.kvfull, 0, a.timeout_ns);
-        for (int ii = max(0, i - ST); ii < i; ++ii)
-          mbar_wait_drain(&ctl.qfull[ii % ST], (ii / ST) & 1, a.timeout_ns);
+    } else if (warp == kComputeWarps + 1) {
+      // ----------------------------------------------------------- MMA issue
+      // Order: S^T_0, dP^T_0, then per query tile i:
+      //   dV_i, S^T_{i+1}, dK_i, dQ_i, dP^T_{i+1}
+      // so S^T_{i+1} runs while the compute warps form dS_i, and dK_i / dQ_i
+      // run while they form P_{i+1}.
+      if (lane == 0 && n > 0) {
+        constexpr uint32_t kIdKN = idesc_bf16(128, D, false, true);   // K-major A, MN-major B
+        constexpr uint32_t kIdNN = idesc_bf16(128, D, true, true);    // MN-major A and B
+        const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), ds_base = smem_u32(sDS);
+        bool ok = mbar_wait(&ctl.kvfull, 0, wc, kSiteBwdKV) &&
+                  mbar_wait(&ctl.qfull[0], 0, wc, kSiteBwdQ) &&
+                  mbar_wait(&ctl.dofull[0], 0, wc, kSiteBwdQ);
+        if (ok) {
+          tc_fence_after();
+          mma_kt_qt<D>(tmem + C::kSCol, k_base, smem_u32(sQ));        // S^T_0
+          mma_commit(&ctl.sfull);
+          mma_kt_qt<D>(tmem + C::kDPCol, v_base, smem_u32(sdO));      // dP^T_0
+          mma_commit(&ctl.dpfull);
+        }
+        for (int i = 0; ok && i < n; ++i) {
+          const uint32_t ph = i & 1;
+          const uint32_t q_base = smem_u32(sQ + (i % QS) * C::kTileBytes);
+          const uint32_t do_base = smem_u32(sdO + (i % DS) * C::kTileBytes);
+          // dV += P~^T dO_i; P~^T pairs of query rows 0..63 sit in columns
+          // [0,32), those of rows 64..127 in [64,96)
+          if (!(ok = mbar_wait(&ctl.pfull, ph, wc, kSiteBwdMma))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(tmem + C::kDVCol, tmem + C::kSCol + kk * 8 + (kk >= 4 ? 32 : 0),
+                   smem_desc(do_base + kk * 2048, C::kBoxBytes, 1024), kIdKN,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&ctl.doempty[i % DS]);
+          // S^T_{i+1}: the S^T columns were read by the compute warps before
+          // pfull and P~^T_i is consumed by dV_i, issued just before
+          if (i + 1 < n) {
+            if (!(ok = mbar_wait(&ctl.qfull[(i + 1) % QS], ((i + 1) / QS) & 1, wc, kSiteBwdQ)))
+              break;
+            tc_fence_after();
+            mma_kt_qt<D>(tmem + C::kSCol, k_base, smem_u32(sQ + ((i + 1) % QS) * C::kTileBytes));
+            mma_commit(&ctl.sfull);
+          }
+          // dK += dS^T Q_i
+          if (!(ok = mbar_wait(&ctl.dsfull, ph, wc, kSiteBwdMma))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+            mma_ss(tmem + C::kDKCol, smem_desc(ds_base + off, 16, 1024),
+                   smem_desc(q_base + kk * 2048, C::kBoxBytes, 1024), kIdKN,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          // dQ_i = dS K_j (its columns: drained copy of dQ_{i-1} read out)
+          if (!C::kDqAliasesDp && i >= 1) {
+            if (!(ok = mbar_wait(&ctl.dqfree, (i - 1) & 1, wc, kSiteBwdMma))) break;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ss(tmem + C::kDQCol, smem_desc(ds_base + kk * 2048, C::kBoxBytes, 1024),
+                   smem_desc(k_base + kk * 2048, C::kBoxBytes, 1024), kIdNN, kk > 0 ? 1u : 0u);
+          mma_commit(&ctl.dqfull);
+          mma_commit(&ctl.qempty[i % QS]);
+          // dP^T_{i+1} (for d = 128 its columns hold dQ_i until drained)
+          if (i + 1 < n) {
+            if (C::kDqAliasesDp && !(ok = mbar_wait(&ctl.dqfree, i & 1, wc, kSiteBwdMma))) break;
+            if (!(ok = mbar_wait(&ctl.dofull[(i + 1) % DS], ((i + 1) / DS) & 1, wc, kSiteBwdQ)))
+              break;
+            tc_fence_after();
+            mma_kt_qt<D>(tmem + C::kDPCol, v_base, smem_u32(sdO + ((i + 1) % DS) * C::kTileBytes));
+            mma_commit(&ctl.dpfull);
+          }
+        }
+        if (ok) mma_commit(&ctl.done);
+        mma_commit(&ctl.final_bar);
+        mbar_wait_drain(&ctl.final_bar, 0, a.timeout_ns);
       }
     }
-  } else if (warp == kComputeWarps + 1) {
-    // ------------------------------------------------------------- MMA issue
-    if (lane == 0 && n > 0) {
-      constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);   // K-major x K-major
-      constexpr uint32_t kIdKN = idesc_bf16(128, D, false, true);      // K-major A, MN-major B
-      constexpr uint32_t kIdNN = idesc_bf16(128, D, true, true);       // MN-major A and B
-      const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), ds_base = smem_u32(sDS);
-      bool ok = mbar_wait(&ctl.kvfull, 0, wc, kSiteBwdKV);
-      for (int i = 0; ok && i < n; ++i) {
-        const int s = i % ST;
-        const uint32_t ph = i & 1;
-        const uint32_t q_base = smem_u32(sQ + s * C::kTileBytes);
-        const uint32_t do_base = smem_u32(sdO + s * C::kTileBytes);
-        ok = mbar_wait(&ctl.qfull[s], (i / ST) & 1, wc, kSiteBwdQ);
-        if (!ok) break;
-        tc_fence_after();
-        // S^T = K_j Q_i^T
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kSCol, smem_desc(k_base + off, 16, 1024),
-                 smem_desc(q_base + off, 16, 1024), kIdSS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&ctl.sfull);
-        if (C::kDqAliasesDp && i >= 1) {   // dQ_{i-1} shares the dP^T columns
-          ok = mbar_wait(&ctl.dqfree, (i - 1) & 1, wc, kSiteBwdMma);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        // dP^T = V_j dO_i^T
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kDPCol, smem_desc(v_base + off, 16, 1024),
-                 smem_desc(do_base + off, 16, 1024), kIdSS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&ctl.dpfull);
-        // dV += P~^T dO_i; P~^T pairs of query rows 0..63 sit in columns
-        // [0,32), those of rows 64..127 in [64,96)
-        ok = mbar_wait(&ctl.pfull, ph, wc, kSiteBwdMma);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + C::kDVCol, tmem + C::kSCol + kk * 8 + (kk >= 4 ? 32 : 0),
-                 smem_desc(do_base + kk * 2048, C::kBoxBytes, 1024), kIdKN,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q_i
-        ok = mbar_wait(&ctl.dsfull, ph, wc, kSiteBwdMma);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kDKCol, smem_desc(ds_base + off, 16, 1024),
-                 smem_desc(q_base + kk * 2048, C::kBoxBytes, 1024), kIdKN,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (!C::kDqAliasesDp && i >= 1) {
-          ok = mbar_wait(&ctl.dqfree, (i - 1) & 1, wc, kSiteBwdMma);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        // dQ_i = dS K_j
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ss(tmem + C::kDQCol, smem_desc(ds_base + kk * 2048, C::kBoxBytes, 1024),
-                 smem_desc(k_base + kk * 2048, C::kBoxBytes, 1024), kIdNN, kk > 0 ? 1u : 0u);
-        mma_commit(&ctl.dqfull);
-        mma_commit(&ctl.dsfree);
-        mma_commit(&ctl.qempty[s]);
-      }
-      if (ok) mma_commit(&ctl.done);
-      mma_commit(&ctl.final_bar);
-      mbar_wait_drain(&ctl.final_bar, 0, a.timeout_ns);
-    }
-  }
   } else {
     regs_increase<C::kRegsCompute>();
     // -------------------------------------------------------------- compute
@@ -354,21 +380,16 @@ __global__ void __launch_bounds__(384, 1)
     const int qc0 = half * 64;             // this warp's first query column
     const float c2 = a.scale_log2;
     const float ds = m.drop_scale;
-    uint8_t* stage = sStage + warp * C::kStageBytes;
+    // this warp's 4 KB of the dS^T buffer: its rows of box `half`; also its
+    // dQ staging region
+    uint8_t* region = sDS + half * C::kBoxBytes + quarter * 4096;
     bool ok = true;
     for (int i = 0; i < n; ++i) {
       const uint32_t ph = i & 1;
       const int qtile = tiles[i];
       const int q0 = qtile * kTile;
-      if (i >= 1) {   // dQ of the previous query tile
-        ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dqfull, (i - 1) & 1, wc, kSiteBwdDq));
-        if (!ok) break;
-        tc_fence_after();
-        drain_dq<D>(tl + C::kDQCol + half * C::kHalf, stage, &tdq, &ctl.dqfree,
-                    tiles[i - 1] * kTile + quarter * 32, half * C::kHalf, h, b, lane);
-      }
       // L (log2 units) and D of this warp's 64 query rows, staged by the producer
-      const float* sLw = sLD + (i % ST) * 2 * kTile + qc0;
+      const float* sLw = sLD + (i % QS) * 2 * kTile + qc0;
       const float* sDw = sLw + kTile;
       const bool diag = m.causal && qtile == kt;   // query q < key: masked
 
@@ -420,19 +441,24 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.pfull);
 
+      if (i >= 1) {   // dQ of the previous query tile: its dS^T is consumed
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dqfull, (i - 1) & 1, wc, kSiteBwdDq));
+        if (!ok) break;
+        tc_fence_after();
+        drain_dq<D>(tl + C::kDQCol + half * C::kHalf, region, &tdq, &ctl.dqfree,
+                    tiles[i - 1] * kTile + quarter * 32, half * C::kHalf, h, b, lane);
+      }
+
       // dS^T = P * (dP~ * Z/(1-p) - D)
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dpfull, ph, wc, kSiteBwdSoft));
       if (!ok) break;
       tc_fence_after();
-      if (i >= 1) {   // dS^T buffer was last read by dQ_{i-1}
-        ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dsfree, (i - 1) & 1, wc, kSiteBwdSoft));
-        if (!ok) break;
-        tc_fence_after();
-      }
       uint32_t drr[64];
       tmem_ld32(tl + C::kDPCol + qc0, drr);
       tmem_ld32(tl + C::kDPCol + qc0 + 32, drr + 32);
       tmem_wait_ld();
+      if (lane == 0) tma_store_wait_read_all();   // the staged dQ has been read
+      __syncwarp();
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const uint32_t* dr = drr + cc * 32;
@@ -449,10 +475,9 @@ __global__ void __launch_bounds__(384, 1)
           }
           pk[t / 2] = pack_bf16x2(p.x * (d0 - sDw[cc * 32 + t]), p.y * (d1 - sDw[cc * 32 + t + 1]));
         }
-        uint8_t* box = sDS + half * C::kBoxBytes;
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          *reinterpret_cast<uint4*>(box + swz(r, cc * 4 + u)) =
+          *reinterpret_cast<uint4*>(region + swz(lane, cc * 4 + u)) =
               make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       }
       fence_proxy_async_smem();
@@ -464,7 +489,7 @@ __global__ void __launch_bounds__(384, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dqfull, (n - 1) & 1, wc, kSiteBwdDq));
       if (ok) {
         tc_fence_after();
-        drain_dq<D>(tl + C::kDQCol + half * C::kHalf, stage, &tdq, &ctl.dqfree,
+        drain_dq<D>(tl + C::kDQCol + half * C::kHalf, region, &tdq, &ctl.dqfree,
                     tiles[n - 1] * kTile + quarter * 32, half * C::kHalf, h, b, lane);
       }
     }

@@ -157,6 +157,13 @@ attn_status attn_bwd_noalloc(const attn_params* p, const void* q,
                              const float* lse, const void* dout, void* dq,
                              void* dk, void* dv, void* stream);
 
+/* Diagnostic: runs the kernels' time-out path on purpose.  Enqueues one warp
+ * that waits on a barrier nothing arrives at, giving up after `limit_ns`
+ * (clamped to [1 ms, 2 s]); it records ATTN_ERR_TIMEOUT in the workspace's
+ * status words exactly as a stalled attention kernel would, so a following
+ * attn_check returns ATTN_ERR_TIMEOUT.  `ws` needs 256 bytes. */
+attn_status attn_selftest_timeout(void* ws, uint64_t limit_ns, void* stream);
+
 /* Synchronises `stream`, returns the workspace's device status (ATTN_OK or
  * ATTN_ERR_TIMEOUT) and clears it. */
 attn_status attn_check(void* ws, void* stream);
