@@ -205,6 +205,7 @@ attn::MaskArgs mask_args(const attn_params* p, const WsLayout& L, char* ws, bool
   m.seed_lo = static_cast<uint32_t>(p->philox_seed & 0xFFFFFFFFull);
   m.seed_hi = static_cast<uint32_t>(p->philox_seed >> 32);
   m.offset = static_cast<uint32_t>(p->philox_offset);
+  m.rk = attn::philox_round_keys(m.seed_lo, m.seed_hi);
   return m;
 }
 

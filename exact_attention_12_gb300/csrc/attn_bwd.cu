@@ -376,6 +376,7 @@ __global__ void __launch_bounds__(384, 1)
     const int r = quarter * 32 + lane;     // key row within the tile == TMEM lane
     const int kj = k0 + r;                 // global key index
     const bool key_ok = kj < limit;
+    const bool tile_keys_ok = k0 + kTile <= limit;   // no key of the tile is masked
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const int qc0 = half * 64;             // this warp's first query column
     const float c2 = a.scale_log2;
@@ -388,52 +389,66 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t ph = i & 1;
       const int qtile = tiles[i];
       const int q0 = qtile * kTile;
-      // L (log2 units) and D of this warp's 64 query rows, staged by the producer
-      const float* sLw = sLD + (i % QS) * 2 * kTile + qc0;
-      const float* sDw = sLw + kTile;
+      // -L (log2 units) and -D of this warp's 64 query rows, staged by the producer
+      const float* nLw = sLD + (i % QS) * 2 * kTile + qc0;
+      const float* nDw = nLw + kTile;
       const bool diag = m.causal && qtile == kt;   // query q < key: masked
+      const bool edge = diag || !tile_keys_ok;
 
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl.sfull, ph, wc, kSiteBwdSoft));
       if (!ok) break;
       tc_fence_after();
-      // P^T (bf16 pairs kept for dS) and P~^T into TMEM
-      uint32_t pp[32];
+      // P^T = 2^(S^T c log2e - L log2e), kept in fp32 for dS; P~^T into TMEM
+      float p[64];
       uint32_t keepbits[2];
-      uint32_t srr[64];
-      tmem_ld32(tl + C::kSCol + qc0, srr);
-      tmem_ld32(tl + C::kSCol + qc0 + 32, srr + 32);
-      tmem_wait_ld();
+      {
+        uint32_t srr[64];
+        tmem_ld32(tl + C::kSCol + qc0, srr);
+        tmem_ld32(tl + C::kSCol + qc0 + 32, srr + 32);
+        tmem_wait_ld();
+        const uint64_t c2x2 = f2_pack(c2, c2);
+#pragma unroll
+        for (int t = 0; t < 64; t += 4) {
+          const float4 nl = *reinterpret_cast<const float4*>(nLw + t);
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(srr[t]), __uint_as_float(srr[t + 1])), c2x2,
+                           f2_pack(nl.x, nl.y)), x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(srr[t + 2]), __uint_as_float(srr[t + 3])), c2x2,
+                           f2_pack(nl.z, nl.w)), x2, x3);
+          p[t] = ex2_approx(x0);
+          p[t + 1] = ex2_approx(x1);
+          p[t + 2] = ex2_approx(x2);
+          p[t + 3] = ex2_approx(x3);
+        }
+      }
+      if (edge) {   // keys past the padding length; causal diagonal tile
+#pragma unroll
+        for (int t = 0; t < 64; ++t)
+          if (!key_ok || (diag && qc0 + t < r)) p[t] = 0.f;
+      }
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        const int c = qc0 + cc * 32;       // query column within the tile
-        const uint32_t* sr = srr + cc * 32;
         uint32_t keep = 0xffffffffu;
         if constexpr (DROPOUT) {
           // element (query q, key kj): word kj mod 4 of the counter (kj/4, q, bh, offset)
-          keep = dropout_keep32_by_key(static_cast<uint32_t>(kj), static_cast<uint32_t>(q0 + c),
-                                       static_cast<uint32_t>(bh), m.offset, m.seed_lo, m.seed_hi,
+          keep = dropout_keep32_by_key(static_cast<uint32_t>(kj),
+                                       static_cast<uint32_t>(q0 + qc0 + cc * 32),
+                                       static_cast<uint32_t>(bh), m.offset, m.rk,
                                        m.drop_threshold, static_cast<uint32_t>(lane));
         }
         keepbits[cc] = keep;
         uint32_t pk[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
-          const int qa = c + t, qb = c + t + 1;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -sLw[cc * 32 + t]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[t + 1]), c2, -sLw[cc * 32 + t + 1]));
-          if (!key_ok || (diag && qa < r)) p0 = 0.f;
-          if (!key_ok || (diag && qb < r)) p1 = 0.f;
-          pp[cc * 16 + t / 2] = pack_bf16x2(p0, p1);
+          float p0 = p[cc * 32 + t], p1 = p[cc * 32 + t + 1];
           if constexpr (DROPOUT) {
             p0 = ((keep >> t) & 1u) ? p0 * ds : 0.f;
             p1 = ((keep >> (t + 1)) & 1u) ? p1 * ds : 0.f;
-            pk[t / 2] = pack_bf16x2(p0, p1);
-          } else {
-            pk[t / 2] = pp[cc * 16 + t / 2];
           }
+          pk[t / 2] = pack_bf16x2(p0, p1);
         }
-        // pairs of query rows c .. c+31 -> column 64*half + 16*cc (within S^T's
-        // own half, already read by this warp)
+        // pairs of query rows qc0+32cc .. +31 -> column 64*half + 16*cc (within
+        // S^T's own half, already read by this warp)
         tmem_st16(tl + C::kSCol + half * 64 + cc * 16, pk);
       }
       tmem_wait_st();
@@ -461,19 +476,28 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        const uint32_t* dr = drr + cc * 32;
         const uint32_t keep = keepbits[cc];
         uint32_t pk[16];
 #pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          const float2 p =
-              __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[cc * 16 + t / 2]));
-          float d0 = __uint_as_float(dr[t]), d1 = __uint_as_float(dr[t + 1]);
+        for (int t = 0; t < 32; t += 4) {
+          const int e = cc * 32 + t;
+          const float4 nd = *reinterpret_cast<const float4*>(nDw + e);
+          float d0 = __uint_as_float(drr[e]), d1 = __uint_as_float(drr[e + 1]);
+          float d2 = __uint_as_float(drr[e + 2]), d3 = __uint_as_float(drr[e + 3]);
           if constexpr (DROPOUT) {
             d0 = ((keep >> t) & 1u) ? d0 * ds : 0.f;
             d1 = ((keep >> (t + 1)) & 1u) ? d1 * ds : 0.f;
+            d2 = ((keep >> (t + 2)) & 1u) ? d2 * ds : 0.f;
+            d3 = ((keep >> (t + 3)) & 1u) ? d3 * ds : 0.f;
           }
-          pk[t / 2] = pack_bf16x2(p.x * (d0 - sDw[cc * 32 + t]), p.y * (d1 - sDw[cc * 32 + t + 1]));
+          float s0, s1, s2, s3;
+          f2_unpack(f2_mul(f2_pack(p[e], p[e + 1]), f2_add(f2_pack(d0, d1), f2_pack(nd.x, nd.y))),
+                    s0, s1);
+          f2_unpack(f2_mul(f2_pack(p[e + 2], p[e + 3]),
+                           f2_add(f2_pack(d2, d3), f2_pack(nd.z, nd.w))),
+                    s2, s3);
+          pk[t / 2] = pack_bf16x2(s0, s1);
+          pk[t / 2 + 1] = pack_bf16x2(s2, s3);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u)
@@ -542,8 +566,9 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // Per query row of the padded [B*H][npad] layout (one row per group of d/8
-// lanes): D = rowsum(dO * O) and L * log2(e) (+inf for padding rows and rows
-// with no allowed key, so they contribute nothing); and dQacc = 0.
+// lanes): -D = -rowsum(dO * O) and -L * log2(e) (-inf for padding rows and
+// rows with no allowed key, so they contribute nothing); and dQacc = 0.  The
+// negated forms let the backward use one fused multiply-add per element.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                             const __nv_bfloat16* __restrict__ dout,
@@ -574,13 +599,13 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
 #pragma unroll
   for (int w = kLanes / 2; w > 0; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
   if (row < rows && part == 0) {
-    float l2 = INFINITY;
+    float nl2 = -INFINITY;
     if (real) {
       const float L = a.lse[bh * a.m.N + n];
-      if (L != -INFINITY) l2 = L * kLog2e;
+      if (L != -INFINITY) nl2 = -L * kLog2e;
     }
-    a.dsum[row] = s;
-    a.lse2[row] = l2;
+    a.dsum[row] = -s;
+    a.lse2[row] = nl2;
   }
   // zero the dQ accumulator
   const int64_t n4 = static_cast<int64_t>(a.m.B) * a.m.H * a.m.N * D / 4;

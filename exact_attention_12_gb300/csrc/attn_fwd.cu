@@ -382,11 +382,10 @@ __global__ void __launch_bounds__(384, 1)
         uint32_t keep = 0xffffffffu;
         if constexpr (DROPOUT) {
           keep = 0;
-#pragma unroll 1
+#pragma unroll 4
           for (int g = 0; g < 8; ++g)
             keep |= dropout_keep4(static_cast<uint32_t>((kv0 + c) / 4 + g), static_cast<uint32_t>(qi),
-                                  static_cast<uint32_t>(bh), m.offset, m.seed_lo, m.seed_hi,
-                                  m.drop_threshold)
+                                  static_cast<uint32_t>(bh), m.offset, m.rk, m.drop_threshold)
                     << (4 * g);
         }
         uint32_t pk[16];

@@ -100,8 +100,7 @@ __global__ void __launch_bounds__(kRows) fwd_fp32_kernel(const float* __restrict
       if constexpr (DROPOUT) {
         if ((j & 3) == 0)
           keep = dropout_keep4(static_cast<uint32_t>((kv0 + j) / 4), static_cast<uint32_t>(qi),
-                               static_cast<uint32_t>(bh), m.offset, m.seed_lo, m.seed_hi,
-                               m.drop_threshold);
+                               static_cast<uint32_t>(bh), m.offset, m.rk, m.drop_threshold);
       }
       const float p = exp2f((srow[j] - m_new) * kLog2e);
       lrow += p;

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "philox.cuh"
+
 namespace attn {
 
 constexpr int kTile = 128;            // query/key tile rows == block-mask granularity
@@ -36,6 +38,7 @@ struct MaskArgs {
   uint32_t drop_threshold;        // 0 = no dropout
   float drop_scale;               // 1 / (1 - p)
   uint32_t seed_lo, seed_hi, offset;
+  PhiloxRoundKeys rk;             // the ten round keys of (seed_lo, seed_hi)
   // CTAs are scheduled in groups of `head_group` consecutive (b, h) so that a
   // group's re-read operands stay in L2
   int head_group;
@@ -59,9 +62,9 @@ struct BwdArgs {
   float scale;
   float scale_log2;
   const float* lse;               // [B,H,N] from the forward (read by the preprocess)
-  float* lse2;                    // workspace [B*H][npad]: L * log2(e); +inf where the
+  float* lse2;                    // workspace [B*H][npad]: -L * log2(e); -inf where the
                                   // row contributes nothing (padding rows, empty rows)
-  float* dsum;                    // workspace [B*H][npad]: rowsum(dO * O); 0 on padding
+  float* dsum;                    // workspace [B*H][npad]: -rowsum(dO * O); 0 on padding
   int npad;                       // nb * 128
   float* dq_acc;                  // [B,H,N,d] fp32, zeroed by the preprocess
   void* dk;
