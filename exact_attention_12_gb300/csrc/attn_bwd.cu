@@ -61,9 +61,12 @@ struct BwdCfg {
   static constexpr int kQStages = 2;                         // Q_i (+ its L, D) stages
   static constexpr int kDoStages = (D == 64) ? 2 : 1;        // dO_i stages
   static constexpr int kDsBytes = kTile * kTile * 2;          // dS^T tile, bf16
-  static constexpr int kLDBytes = 2 * kTile * 4;              // L*log2e and D of a query tile
-  static constexpr int kSmem = 1024 + 2 * kTileBytes + kQStages * kTileBytes +
-                               kDoStages * kTileBytes + kDsBytes + kQStages * kLDBytes;
+  static constexpr int kStageBytes = kComputeWarps * 4096;    // dQ staging, 4 KB per warp
+  static constexpr int kLDBytes = 2 * kTile * 4;              // -L*log2e and -D of a query tile
+  // every buffer is a multiple of 1024 bytes; the dynamic base must be
+  // 1024-aligned (checked at run time), so no alignment slack is requested
+  static constexpr int kSmem = 2 * kTileBytes + kQStages * kTileBytes + kDoStages * kTileBytes +
+                               kDsBytes + kStageBytes;
   static constexpr uint32_t kSCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 256 + D;
   static constexpr uint32_t kDQCol = (D == 64) ? 384 : 128;
   static constexpr bool kDqAliasesDp = (D == 128);
@@ -75,14 +78,20 @@ struct BwdCfg {
   static constexpr uint32_t kRegsLaunch = 168, kRegsCompute = 208, kRegsOther = 80;
 };
 
-struct BwdCtl {
+// Barriers, TMEM address and the staged row statistics: the kernel's static
+// shared memory, padded to 3 KB so that the dynamic buffers after it start on
+// a 1024-byte boundary.
+struct __align__(1024) BwdCtl {
+  float ld[2][2 * kTile];   // per Q stage: -L*log2e [0,128), -D [128,256)
   uint64_t kvfull;
   uint64_t qfull[2], qempty[2], dofull[2], doempty[2];
   uint64_t sfull, dpfull, pfull, dsfull, dqfull, dqfree, done;
   uint64_t final_bar;
   uint32_t tmem_base;
   int abort_flag;
+  uint8_t pad[3072 - 2 * 2 * kTile * 4 - 19 * 8 - 8];
 };
+static_assert(sizeof(BwdCtl) == 3072, "static shared block must stay 3 KB");
 
 struct QList {
   const uint16_t* idx;   // block-mask column list, or null (dense)
@@ -126,14 +135,17 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return r * 128 + ((c ^ (r & 7)) << 4);
 }
 
-// Drain this warp's share of a dQ tile: TMEM -> registers -> the warp's 4 KB
-// region of shared memory (32 rows x 32 fp32, 128-byte swizzle) -> TMA
-// reduce-add into the accumulator, 32 columns at a time.  Arrives on
-// `dqfree` once the TMEM columns have been read.
+// Drain this warp's share of a dQ tile: TMEM -> registers -> shared memory
+// (32 rows x 32 fp32 boxes, 128-byte swizzle) -> TMA reduce-add into the
+// accumulator.  Arrives on `dqfree` once the TMEM columns have been read.
+// The reduce-adds run on while the warp goes on: the first box goes to the
+// warp's slice of the dS^T buffer (free: dS^T of this tile is consumed) when
+// there are two, the last to the warp's dedicated staging box; a box is only
+// rewritten after its reduce has read it (cp.async.bulk.wait_group.read).
 template <int D>
-__device__ __forceinline__ void drain_dq(uint32_t tl_dq, uint8_t* stage, const CUtensorMap* tdq,
-                                         uint64_t* dqfree, int q_row0, int col0, int h, int b,
-                                         int lane) {
+__device__ __forceinline__ void drain_dq(uint32_t tl_dq, uint8_t* stage, uint8_t* ds_slice,
+                                         const CUtensorMap* tdq, uint64_t* dqfree, int q_row0,
+                                         int col0, int h, int b, int lane) {
   constexpr int kChunks = (D / 2) / 32;
   uint32_t v[kChunks][32];
 #pragma unroll
@@ -144,16 +156,25 @@ __device__ __forceinline__ void drain_dq(uint32_t tl_dq, uint8_t* stage, const C
   if (lane == 0) mbar_arrive(dqfree);
 #pragma unroll
   for (int cc = 0; cc < kChunks; ++cc) {
-    if (lane == 0) tma_store_wait_read_all();   // the previous reduce has read the region
+    const bool last = cc == kChunks - 1;
+    uint8_t* box = last ? stage : ds_slice;
+    // the staging box's previous reduce (one query tile ago) has read it;
+    // for the dS^T slice nothing is pending
+    if (last && lane == 0) {
+      if (kChunks == 2)
+        tma_store_wait_read_1();
+      else
+        tma_store_wait_read_all();
+    }
     __syncwarp();
 #pragma unroll
     for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<uint4*>(stage + swz(lane, c)) =
+      *reinterpret_cast<uint4*>(box + swz(lane, c)) =
           make_uint4(v[cc][4 * c], v[cc][4 * c + 1], v[cc][4 * c + 2], v[cc][4 * c + 3]);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_reduce_add_4d(tdq, stage, col0 + cc * 32, q_row0, h, b);
+      tma_reduce_add_4d(tdq, box, col0 + cc * 32, q_row0, h, b);
       tma_store_commit();
     }
   }
@@ -178,17 +199,20 @@ __global__ void __launch_bounds__(384, 1)
                     const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
   using C = BwdCfg<D>;
   constexpr int QS = C::kQStages, DS = C::kDoStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sK = smem;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ BwdCtl ctl;
+  if ((smem_u32(smem_raw) & 1023u) != 0) {   // buffers need 1024-byte alignment
+    if (threadIdx.x == 0 && atomicCAS(a.status, 0, kStatusSmemAlign) == 0)
+      atomicExch(a.status + 1, kSiteBwdSmem);
+    return;
+  }
+  uint8_t* sK = smem_raw;
   uint8_t* sV = sK + C::kTileBytes;
   uint8_t* sQ = sV + C::kTileBytes;                 // QS tiles
   uint8_t* sdO = sQ + QS * C::kTileBytes;           // DS tiles
-  uint8_t* sDS = sdO + DS * C::kTileBytes;          // dS^T [kv][q], two 64-column boxes;
-                                                    // also the dQ staging area
-  float* sLD = reinterpret_cast<float*>(sDS + C::kDsBytes);   // QS x (L2[128], D[128])
-  __shared__ BwdCtl ctl;
+  uint8_t* sDS = sdO + DS * C::kTileBytes;          // dS^T [kv][q], two 64-column boxes
+  uint8_t* sStage = sDS + C::kDsBytes;              // dQ staging, 4 KB per compute warp
+  float* sLD = &ctl.ld[0][0];                       // QS x (-L2[128], -D[128])
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const MaskArgs& m = a.m;
@@ -381,9 +405,10 @@ __global__ void __launch_bounds__(384, 1)
     const int qc0 = half * 64;             // this warp's first query column
     const float c2 = a.scale_log2;
     const float ds = m.drop_scale;
-    // this warp's 4 KB of the dS^T buffer: its rows of box `half`; also its
-    // dQ staging region
+    // this warp's 4 KB of the dS^T buffer (its rows of box `half`) and its
+    // dedicated dQ staging box
     uint8_t* region = sDS + half * C::kBoxBytes + quarter * 4096;
+    uint8_t* stage = sStage + warp * 4096;
     bool ok = true;
     for (int i = 0; i < n; ++i) {
       const uint32_t ph = i & 1;
@@ -460,7 +485,7 @@ __global__ void __launch_bounds__(384, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dqfull, (i - 1) & 1, wc, kSiteBwdDq));
         if (!ok) break;
         tc_fence_after();
-        drain_dq<D>(tl + C::kDQCol + half * C::kHalf, region, &tdq, &ctl.dqfree,
+        drain_dq<D>(tl + C::kDQCol + half * C::kHalf, stage, region, &tdq, &ctl.dqfree,
                     tiles[i - 1] * kTile + quarter * 32, half * C::kHalf, h, b, lane);
       }
 
@@ -472,8 +497,10 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld32(tl + C::kDPCol + qc0, drr);
       tmem_ld32(tl + C::kDPCol + qc0 + 32, drr + 32);
       tmem_wait_ld();
-      if (lane == 0) tma_store_wait_read_all();   // the staged dQ has been read
-      __syncwarp();
+      if (C::kHalf > 32) {   // the dS^T slice held a dQ box: its reduce has read it
+        if (lane == 0) tma_store_wait_read_1();
+        __syncwarp();
+      }
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const uint32_t keep = keepbits[cc];
@@ -513,7 +540,7 @@ __global__ void __launch_bounds__(384, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dqfull, (n - 1) & 1, wc, kSiteBwdDq));
       if (ok) {
         tc_fence_after();
-        drain_dq<D>(tl + C::kDQCol + half * C::kHalf, region, &tdq, &ctl.dqfree,
+        drain_dq<D>(tl + C::kDQCol + half * C::kHalf, stage, region, &tdq, &ctl.dqfree,
                     tiles[n - 1] * kTile + quarter * 32, half * C::kHalf, h, b, lane);
       }
     }

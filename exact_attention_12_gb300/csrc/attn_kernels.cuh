@@ -17,8 +17,12 @@ enum WaitSite : int {
   kSiteFwdQ = 1, kSiteFwdK, kSiteFwdV, kSiteFwdKvEmpty, kSiteFwdSFull, kSiteFwdSFree,
   kSiteFwdPFull, kSiteFwdPvDone,
   kSiteBwdLoad = 20, kSiteBwdKV, kSiteBwdQ, kSiteBwdMma, kSiteBwdSoft, kSiteBwdDq,
-  kSiteBwdEmpty, kSiteBwdFree
+  kSiteBwdEmpty, kSiteBwdFree, kSiteBwdSmem
 };
+
+// Device status code for a kernel that found its shared memory misaligned
+// and returned without doing anything (equals ATTN_ERR_CUDA in attn.h).
+constexpr int kStatusSmemAlign = 3;
 
 // Per-call mask/dropout settings common to every kernel.
 struct MaskArgs {
