@@ -194,14 +194,16 @@ attn::MaskArgs mask_args(const attn_params* p, const WsLayout& L, char* ws, bool
     m.list_idx = reinterpret_cast<const uint16_t*>(ws + L.list_idx);
   }
   (void)by_column;
+  // 16-bit uniforms: drop iff u < T, T = min(2^16 - 1, floor(p * 2^16)); the
+  // drop rate is exactly T / 2^16 and kept values are scaled by its inverse
   const double p32 = static_cast<double>(p->dropout_p);
   uint32_t T = 0;
   if (p32 > 0.0) {
-    const double t = std::floor(p32 * 4294967296.0);
-    T = t >= 4294967295.0 ? 0xFFFFFFFFu : static_cast<uint32_t>(t);
+    const double t = std::floor(p32 * 65536.0);
+    T = t >= 65535.0 ? 65535u : static_cast<uint32_t>(t);
   }
   m.drop_threshold = T;
-  m.drop_scale = p32 > 0.0 ? static_cast<float>(1.0 / (1.0 - p32)) : 1.0f;
+  m.drop_scale = T ? static_cast<float>(65536.0 / (65536.0 - T)) : 1.0f;
   m.seed_lo = static_cast<uint32_t>(p->philox_seed & 0xFFFFFFFFull);
   m.seed_hi = static_cast<uint32_t>(p->philox_seed >> 32);
   m.offset = static_cast<uint32_t>(p->philox_offset);

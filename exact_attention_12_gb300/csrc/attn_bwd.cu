@@ -455,7 +455,8 @@ __global__ void __launch_bounds__(384, 1)
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t keep = 0xffffffffu;
         if constexpr (DROPOUT) {
-          // element (query q, key kj): word kj mod 4 of the counter (kj/4, q, bh, offset)
+          // element (query q, key kj): 16-bit half kj mod 2 of word (kj mod 8)/2
+          // of the counter (kj/8, q, bh, offset)
           keep = dropout_keep32_by_key(static_cast<uint32_t>(kj),
                                        static_cast<uint32_t>(q0 + qc0 + cc * 32),
                                        static_cast<uint32_t>(bh), m.offset, m.rk,

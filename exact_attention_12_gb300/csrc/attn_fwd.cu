@@ -382,11 +382,11 @@ __global__ void __launch_bounds__(384, 1)
         uint32_t keep = 0xffffffffu;
         if constexpr (DROPOUT) {
           keep = 0;
-#pragma unroll 4
-          for (int g = 0; g < 8; ++g)
-            keep |= dropout_keep4(static_cast<uint32_t>((kv0 + c) / 4 + g), static_cast<uint32_t>(qi),
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            keep |= dropout_keep8(static_cast<uint32_t>((kv0 + c) / 8 + g), static_cast<uint32_t>(qi),
                                   static_cast<uint32_t>(bh), m.offset, m.rk, m.drop_threshold)
-                    << (4 * g);
+                    << (8 * g);
         }
         uint32_t pk[16];
 #pragma unroll

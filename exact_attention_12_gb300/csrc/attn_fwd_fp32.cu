@@ -95,16 +95,16 @@ __global__ void __launch_bounds__(kRows) fwd_fp32_kernel(const float* __restrict
 #pragma unroll
     for (int c = 0; c < D; ++c) o[c] *= alpha;
     mrow = m_new;
-    uint32_t keep = 0xFu;
+    uint32_t keep = 0xFFu;
     for (int j = 0; j < kKeys; ++j) {
       if constexpr (DROPOUT) {
-        if ((j & 3) == 0)
-          keep = dropout_keep4(static_cast<uint32_t>((kv0 + j) / 4), static_cast<uint32_t>(qi),
+        if ((j & 7) == 0)
+          keep = dropout_keep8(static_cast<uint32_t>((kv0 + j) / 8), static_cast<uint32_t>(qi),
                                static_cast<uint32_t>(bh), m.offset, m.rk, m.drop_threshold);
       }
       const float p = exp2f((srow[j] - m_new) * kLog2e);
       lrow += p;
-      const float pd = ((keep >> (j & 3)) & 1u) ? p : 0.f;
+      const float pd = ((keep >> (j & 7)) & 1u) ? p : 0.f;
 #pragma unroll
       for (int c = 0; c < D; ++c) o[c] = fmaf(pd, sV[j * D + c], o[c]);
     }

@@ -44,37 +44,45 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxRoundKeys& r
   return c;
 }
 
-// Keep bits of four consecutive keys j = 4g .. 4g+3 of query row i:
-// bit t of the result is 1 iff key 4g+t is kept (word t >= threshold).
-__device__ __forceinline__ uint32_t dropout_keep4(uint32_t g, uint32_t i, uint32_t bh,
+// Keep bits of eight consecutive keys j = 8g .. 8g+7 of query row i.  Word w
+// of the Philox output holds the 16-bit uniforms of keys 8g+2w (low half)
+// and 8g+2w+1 (high half); key j is kept iff its uniform >= threshold.  Bit t
+// of the result is 1 iff key 8g+t is kept.
+__device__ __forceinline__ uint32_t dropout_keep8(uint32_t g, uint32_t i, uint32_t bh,
                                                   uint32_t offset, const PhiloxRoundKeys& rk,
                                                   uint32_t threshold) {
   const uint4 u = philox4x32_10(make_uint4(g, i, bh, offset), rk);
-  return (u.x >= threshold ? 1u : 0u) | (u.y >= threshold ? 2u : 0u) |
-         (u.z >= threshold ? 4u : 0u) | (u.w >= threshold ? 8u : 0u);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  uint32_t bits = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    bits |= ((w[k] & 0xFFFFu) >= threshold ? 1u : 0u) << (2 * k);
+    bits |= ((w[k] >> 16) >= threshold ? 1u : 0u) << (2 * k + 1);
+  }
+  return bits;
 }
 
-// Keep bits of the 32 query rows q0 .. q0+31 for key kj, where the four
-// lanes of an aligned lane quad hold the four keys 4g .. 4g+3 (kj mod 4 ==
-// lane mod 4).  One Philox call at query q yields the words of all four
-// keys, so each lane evaluates the 8 queries q0 + 4s + (lane mod 4) and the
-// quad exchanges the results: 8 calls per lane instead of 32.  Bit t of the
+// Keep bits of the 32 query rows q0 .. q0+31 for key kj, where the eight
+// lanes of an aligned lane octet hold the keys 8g .. 8g+7 (kj mod 8 ==
+// lane mod 8).  One Philox call at query q yields the uniforms of all eight
+// keys, so each lane evaluates the 4 queries q0 + 8s + (lane mod 8) and the
+// octet exchanges the results: 4 calls per lane instead of 32.  Bit t of the
 // result is 1 iff (q0 + t, kj) is kept.  All 32 lanes must call it.
 __device__ __forceinline__ uint32_t dropout_keep32_by_key(uint32_t kj, uint32_t q0, uint32_t bh,
                                                           uint32_t offset,
                                                           const PhiloxRoundKeys& rk,
                                                           uint32_t threshold, uint32_t lane) {
-  const uint32_t u = lane & 3u;
-  uint32_t mine = 0;   // bit 4s + x: key 4g+x kept at query q0 + 4s + u
+  const uint32_t u = lane & 7u;
+  uint32_t mine = 0;   // bit 8s + x: key 8g+x kept at query q0 + 8s + u
 #pragma unroll
-  for (uint32_t s = 0; s < 8; ++s)
-    mine |= dropout_keep4(kj >> 2, q0 + 4 * s + u, bh, offset, rk, threshold) << (4 * s);
+  for (uint32_t s = 0; s < 4; ++s)
+    mine |= dropout_keep8(kj >> 3, q0 + 8 * s + u, bh, offset, rk, threshold) << (8 * s);
   uint32_t keep = 0;
 #pragma unroll
-  for (uint32_t src = 0; src < 4; ++src) {
-    const uint32_t m = __shfl_sync(0xffffffffu, mine, (lane & ~3u) | src);
+  for (uint32_t src = 0; src < 8; ++src) {
+    const uint32_t m = __shfl_sync(0xffffffffu, mine, (lane & ~7u) | src);
 #pragma unroll
-    for (uint32_t s = 0; s < 8; ++s) keep |= ((m >> (4 * s + u)) & 1u) << (4 * s + src);
+    for (uint32_t s = 0; s < 4; ++s) keep |= ((m >> (8 * s + u)) & 1u) << (8 * s + src);
   }
   return keep;
 }

@@ -12,7 +12,7 @@
  *
  *   S = scale * Q K^T, with S_ij = -inf where key j is not allowed for query i
  *   L_i = logsumexp_j S_ij               (natural log, fp32)
- *   P = exp(S - L),  P~ = P * Z / (1 - p)  (Z: Philox dropout keep mask)
+ *   P = exp(S - L),  P~ = P * Z / (1 - p')  (Z: Philox dropout keep mask)
  *   O = P~ V
  *
  * Allowed(i, j) = (!causal || j <= i) && j < key_lens[b] &&
@@ -21,15 +21,18 @@
  *
  * Backward (chain rule of the above; the pages state only that S and P are
  * recomputed from Q, K, V and the stored statistics):
- *   D = rowsum(dO * O),  dV = P~^T dO,  dP = (dO V^T) * Z / (1 - p),
+ *   D = rowsum(dO * O),  dV = P~^T dO,  dP = (dO V^T) * Z / (1 - p'),
  *   dS = P * (dP - D),   dQ = scale * dS K,  dK = scale * dS^T Q.
  *
- * Dropout keep mask: for element (b, h, i, j) the 32-bit word j mod 4 of
- * Philox4x32-10 (Salmon et al., SC'11) at counter
- * (floor(j / 4), i, b * H + h, philox_offset) under key
- * (low 32 bits of philox_seed, high 32 bits) is u; the element is dropped
- * iff u < T, T = min(2^32 - 1, floor(dropout_p * 2^32)) computed in fp64
- * from the float dropout_p.  The backward call regenerates the same mask.
+ * Dropout keep mask: Philox4x32-10 (Salmon et al., SC'11) at counter
+ * (floor(j / 8), i, b * H + h, philox_offset) under key (low 32 bits of
+ * philox_seed, high 32 bits) gives four 32-bit words; word (j mod 8) / 2
+ * holds the 16-bit uniform u of element (b, h, i, j) in its low half when j
+ * is even, its high half when j is odd.  The element is dropped iff u < T,
+ * T = min(2^16 - 1, floor(dropout_p * 2^16)) computed in fp64 from the float
+ * dropout_p: the drop rate is exactly p' = T / 2^16 (within 2^-16 of
+ * dropout_p) and kept probabilities are scaled by 1 / (1 - p'), so P~ =
+ * P * Z / (1 - p').  The backward call regenerates the same mask.
  *
  * Layout: Q, K, V, O, dO, dQ, dK, dV are logical [B, H, N, d] arrays with
  * unit stride along d and the element strides stride_b, stride_h, stride_n

@@ -37,5 +37,6 @@ from .attention import (  # noqa: F401
     backward_keys,
     backward_rows,
     dropout_threshold,
+    keep_scale,
     keep_mask,
 )

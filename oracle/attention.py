@@ -17,9 +17,10 @@ inputs the GPU sees:
      L is the stored softmax statistic of the paper summary's
      "recomputation in the backward pass" idea, kept as one logsumexp)
   4. P = exp(S - L)                          (softmax, §3.4)
-  5. P~ = P * Z / (1 - p)                    (dropout on the probabilities,
+  5. P~ = P * Z / (1 - p')                   (dropout on the probabilities,
      fused between softmax and the second matmul per the kernel-fusion idea;
-     Z is the Philox keep mask defined in `keep_mask`)
+     Z is the Philox keep mask defined in `keep_mask`, p' = T / 2^16 its exact
+     drop rate, see `dropout_threshold`)
   6. O = P~ V                                (§3.5)
 
 A row with no allowed key has L = -inf, P = 0, O = 0 and contributes nothing
@@ -28,7 +29,7 @@ to any gradient.
 Backward (the chain rule applied to the definition above; the pages state only
 that S and P are recomputed):
 
-  dV = P~^T dO,  dP~ = dO V^T,  dP = dP~ * Z / (1 - p),
+  dV = P~^T dO,  dP~ = dO V^T,  dP = dP~ * Z / (1 - p'),
   D = rowsum(dO * O)  (= rowsum(P * dP)),  dS = P * (dP - D),
   dQ = c * dS K,  dK = c * dS^T Q.
 
@@ -49,25 +50,34 @@ _ROW_CHUNK = 256     # query rows per chunk
 
 
 def dropout_threshold(p):
-    """Integer drop threshold T = min(2^32 - 1, floor(p * 2^32)).
+    """Integer drop threshold T = min(2^16 - 1, floor(p * 2^16)).
 
     p is taken at float32 precision (the width the C interface carries) and
     the product is formed in fp64, where it is exact.  An element is dropped
-    iff its 32-bit uniform word u satisfies u < T.
+    iff its 16-bit uniform u satisfies u < T, so the drop probability is
+    exactly T / 2^16 (within 2^-16 of p).
     """
     p32 = float(np.float32(p))
     if p32 <= 0.0:
         return 0
-    return min(2 ** 32 - 1, int(math.floor(p32 * 2.0 ** 32)))
+    return min(2 ** 16 - 1, int(math.floor(p32 * 2.0 ** 16)))
+
+
+def keep_scale(p):
+    """Scale of the kept probabilities: 1 / (1 - T / 2^16), the inverse keep rate."""
+    T = dropout_threshold(p)
+    return 2.0 ** 16 / (2.0 ** 16 - T) if T else 1.0
 
 
 def keep_mask(rows, cols, bh, seed, offset, p):
     """Dropout keep mask Z[i, j] in {0, 1} for one (b, h).
 
     rows, cols: 1-D integer arrays of query/key indices; bh = b * H + h.
-    Counter = (floor(j / 4), i, bh, offset), key = (low 32 bits of seed,
-    high 32 bits of seed); word j mod 4 of the Philox4x32-10 output is the
-    uniform u of element (i, j); keep iff u >= T (see dropout_threshold).
+    Counter = (floor(j / 8), i, bh, offset), key = (low 32 bits of seed,
+    high 32 bits of seed).  Of the four 32-bit Philox4x32-10 output words,
+    word (j mod 8) div 2 holds keys j with j mod 2 = 0 in its low 16 bits and
+    j mod 2 = 1 in its high 16 bits; that 16-bit value is the uniform u of
+    element (i, j); keep iff u >= T (see dropout_threshold).
     """
     rows = np.asarray(rows, dtype=np.int64)
     cols = np.asarray(cols, dtype=np.int64)
@@ -76,11 +86,12 @@ def keep_mask(rows, cols, bh, seed, offset, p):
         return np.ones((rows.size, cols.size), dtype=bool)
     seed = int(seed)
     k0, k1 = seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF
-    groups, inv = np.unique(cols // 4, return_inverse=True)
+    groups, inv = np.unique(cols // 8, return_inverse=True)
     words = philox4x32_10(groups[None, :], rows[:, None], bh, int(offset), k0, k1)
     stacked = np.stack(words, axis=-1)                 # [R, G, 4]
-    u = stacked[:, inv, cols % 4]                      # [R, C]
-    return u.astype(np.uint64) >= np.uint64(T)
+    w = stacked[:, inv, (cols % 8) // 2]               # [R, C]
+    u16 = (w.astype(np.uint64) >> (16 * (cols % 2)).astype(np.uint64)) & np.uint64(0xFFFF)
+    return u16 >= np.uint64(T)
 
 
 def allowed_mask(rows, cols, causal=False, key_len=None, block_mask=None):
@@ -133,9 +144,9 @@ class _Head:
             ml = m[live]
             L[live] = ml + np.log(np.exp(Sl - ml[:, None]).sum(axis=1))
             P[live] = np.exp(Sl - L[live][:, None])
-        if self.p > 0.0:
+        if dropout_threshold(self.p) > 0:
             Z = keep_mask(rows, cols, self.bh, self.seed, self.offset, self.p)
-            Zs = Z.astype(np.float64) / (1.0 - self.p)
+            Zs = Z.astype(np.float64) * keep_scale(self.p)
         else:
             Zs = np.ones_like(P)
         return cols, P, Zs, L

@@ -194,9 +194,10 @@ def _brute_force(q, k, v, c, causal, key_len, p, seed, offset, bh):
                 continue
             pij = math.exp(s[j] - L[i])
             if T:
-                w = philox4x32_10_scalar((j // 4, i, bh, offset),
-                                         (seed & 0xFFFFFFFF, seed >> 32))[j % 4]
-                pij = 0.0 if w < T else pij / (1.0 - float(np.float32(p)))
+                w = philox4x32_10_scalar((j // 8, i, bh, offset),
+                                         (seed & 0xFFFFFFFF, seed >> 32))[(j % 8) // 2]
+                u16 = (w >> (16 * (j % 2))) & 0xFFFF
+                pij = 0.0 if u16 < T else pij / (1.0 - T / 65536.0)
             for t in range(len(v[0])):
                 O[i][t] += pij * v[j][t]
     return np.array(O), np.array(L)
@@ -370,26 +371,30 @@ def test_sampled_helpers_match_full_evaluation():
 
 def test_dropout_threshold_values():
     assert A.dropout_threshold(0.0) == 0
-    assert A.dropout_threshold(0.5) == 2 ** 31
-    assert A.dropout_threshold(0.25) == 2 ** 30
-    p32 = float(np.float32(0.1))
-    assert A.dropout_threshold(0.1) == math.floor(p32 * 2 ** 32)
+    assert A.dropout_threshold(0.5) == 2 ** 15
+    assert A.dropout_threshold(0.25) == 2 ** 14
+    assert A.dropout_threshold(0.1) == 6553                 # floor(0.1 * 65536)
+    assert A.dropout_threshold(0.99999) == 65535
+    assert A.dropout_threshold(1e-6) == 0 and A.keep_scale(1e-6) == 1.0
+    assert A.keep_scale(0.5) == 2.0
+    assert A.keep_scale(0.1) == 65536 / (65536 - 6553)
 
 
 def test_keep_mask_uses_counter_word_layout():
     rows = np.array([0, 3, 511])
-    cols = np.array([0, 1, 2, 3, 4, 9, 510])
+    cols = np.array([0, 1, 2, 3, 4, 7, 8, 9, 510])
     seed, offset, bh = (5 << 32) | 17, 11, 6
     Z = A.keep_mask(rows, cols, bh, seed, offset, 0.5)
     for a, i in enumerate(rows):
         for b, j in enumerate(cols):
-            w = philox4x32_10_scalar((j // 4, i, bh, offset), (17, 5))[j % 4]
-            assert Z[a, b] == (w >= 2 ** 31)
+            w = philox4x32_10_scalar((j // 8, i, bh, offset), (17, 5))[(j % 8) // 2]
+            u16 = (w >> (16 * (j % 2))) & 0xFFFF
+            assert Z[a, b] == (u16 >= 2 ** 15)
 
 
 def test_keep_fraction_within_binomial_band():
-    p = 0.1
-    Z = A.keep_mask(np.arange(512), np.arange(512), 3, 0, 0, p)
+    p = A.dropout_threshold(0.1) / 65536.0          # the exact drop rate
+    Z = A.keep_mask(np.arange(512), np.arange(512), 3, 0, 0, 0.1)
     n = Z.size
     keep = Z.mean()
     sigma = math.sqrt(p * (1 - p) / n)
@@ -409,7 +414,7 @@ def test_inverted_dropout_is_unbiased():
     mean = acc / n_seeds
     hd = A._Head(q, k, v, 0.5, False, None, None, 0.0, 0, 0, 0)
     _, P, _, _ = hd.chunk(np.arange(N))
-    pp = float(np.float32(p))
+    pp = A.dropout_threshold(p) / 65536.0              # the exact drop rate
     var = (P ** 2) @ (v ** 2) * pp / (1 - pp)           # per-seed variance
     sigma = np.sqrt(var / n_seeds)
     assert np.all(np.abs(mean - O0) < 6 * sigma + 1e-12)
