@@ -35,9 +35,10 @@ METRIC = "attention fwd+bwd TFLOPS (bf16, causal/non-causal) & % of GB300 dense 
 SPEC_BF16_TFLOPS = 2250.0
 L2_BYTES = 129 * 2 ** 20
 SECONDARY = ("long-causal-16384",)
-# DRAM bytes per launch of the backward main kernel, from the ncu capture in
-# profiles/ (None until a capture of the current kernel exists)
-BWD_MAIN_TRAFFIC = {}
+# DRAM bytes (read + write) per launch of the backward main kernel, from the
+# ncu capture summarised in profiles/bwd_bf16_kernel_bert-large.md; absent
+# (reported as null) for other workloads or once the kernel has changed
+BWD_MAIN_TRAFFIC = {"bert-large": 116.2e6}
 
 
 # ----------------------------------------------------------------- FLOPs --
@@ -242,35 +243,64 @@ def measure_device(ea, w, dev, steps, warmup, dist=None, sample_clocks=True):
 
 
 def measure_e2e(ea, w, dev, steps, warmup):
-    """Same metric through the Python API with host (pinned) inputs and outputs."""
+    """Same metric through the Python API with host (pinned) inputs and outputs.
+
+    Every step copies its inputs host -> device, runs the forward and the
+    backward, and copies dQ, dK, dV device -> host.  Steps are pipelined over
+    three streams (uploads, compute, downloads) with two buffer sets, so the
+    copies of one step overlap the compute of its neighbours; the time is
+    taken from the first upload to the last download.
+    """
     inp = workloads.make_inputs(w)
-    host = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
+    names = ("q", "k", "v", "do")
+    host = {n: inp[n].pin_memory() for n in names}
     kl = None if inp["key_lens"] is None else inp["key_lens"].to(dev)
     bm = None if inp["block_mask"] is None else inp["block_mask"].to(dev)
     kw = dict(scale=inp["scale"], causal=inp["causal"], key_lens=kl, dropout_p=inp["dropout_p"],
               seed=inp["seed"], offset=inp["offset"], block_mask=bm)
-    outs = [torch.empty(inp["q"].shape, dtype=inp["q"].dtype).pin_memory() for _ in range(3)]
+    shape, dtype = inp["q"].shape, inp["q"].dtype
+    dev_in = [{n: torch.empty(shape, dtype=dtype, device=dev) for n in names} for _ in range(2)]
+    dev_out = [[torch.empty(shape, dtype=dtype, device=dev) for _ in range(3)] for _ in range(2)]
+    host_out = [[torch.empty(shape, dtype=dtype).pin_memory() for _ in range(3)] for _ in range(2)]
+    up, comp, down = (torch.cuda.Stream(dev) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in range(2)]        # inputs of buffer set uploaded
+    ev_used = [torch.cuda.Event() for _ in range(2)]      # compute done with buffer set
+    ev_out = [torch.cuda.Event() for _ in range(2)]       # downloads of buffer set done
+    def step(k):
+        b = k % 2
+        with torch.cuda.stream(up):
+            up.wait_event(ev_used[b])
+            for n in names:
+                dev_in[b][n].copy_(host[n], non_blocking=True)
+            ev_in[b].record(up)
+        with torch.cuda.stream(comp):
+            comp.wait_event(ev_in[b])
+            comp.wait_event(ev_out[b])
+            d = dev_in[b]
+            o, lse = ea.attention_fwd(d["q"], d["k"], d["v"], **kw)
+            ea.attention_bwd(d["do"], d["q"], d["k"], d["v"], o, lse, dq=dev_out[b][0],
+                             dk=dev_out[b][1], dv=dev_out[b][2], **kw)
+            ev_used[b].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_used[b])
+            for dst, src in zip(host_out[b], dev_out[b]):
+                dst.copy_(src, non_blocking=True)
+            ev_out[b].record(down)
 
-    def step():
-        q, k, v, do = (host[n].to(dev, non_blocking=True) for n in ("q", "k", "v", "do"))
-        o, lse = ea.attention_fwd(q, k, v, **kw)
-        dq, dk, dv = ea.attention_bwd(do, q, k, v, o, lse, **kw)
-        for dst, src in zip(outs, (dq, dk, dv)):
-            dst.copy_(src, non_blocking=True)
-
-    for _ in range(warmup):
-        step()
+    for k in range(warmup):
+        step(k)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
-    for _ in range(steps):
-        step()
+    for k in range(steps):
+        step(k)
     torch.cuda.synchronize(dev)
     dt = (time.perf_counter() - t0) / steps
     flops = 3.5 * fwd_flops(w, inp["key_lens"], inp["block_mask"])
-    h2d = sum(host[n].numel() * host[n].element_size() for n in host)
-    d2h = sum(t.numel() * t.element_size() for t in outs)
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
     return {"value": flops / dt / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3,
+            "pipelining": "uploads, compute and downloads on three streams, two buffer sets"}
 
 
 # ---------------------------------------------------------- oracle (CPU) --
@@ -430,7 +460,8 @@ def main():
                         "of_spec_2250": 100 * value / world / SPEC_BF16_TFLOPS},
         "roofline": {"kernel": "bwd_bf16_kernel", "bound": "tensor", "achieved": main_tflops,
                      "peak": sustained, "unit": "TFLOP/s", "frac": main_tflops / sustained,
-                     "peak_source": f"bf16_tflops_sustained ({src})", "traffic": traffic},
+                     "peak_source": f"bf16_tflops_sustained ({src})", "traffic": traffic,
+                     "traffic_unit": "bytes per launch (DRAM read + write, ncu)"},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }

@@ -126,3 +126,50 @@ def test_full_size_workload_sampled(ea, name):
         assert max(errs) <= GRAD_REL_L2, (name, b, h, errs)
     for t in (dq, dk, dv):
         assert torch.isfinite(t.float()).all()
+
+
+def test_strided_bnhd_layout(ea):
+    # [B, N, H, d] storage viewed as [B, H, N, d], backward included
+    B, H, N, d = 2, 3, 300, 64
+    g = torch.Generator().manual_seed(31)
+    base = [torch.randn(B, N, H, d, generator=g).to(torch.bfloat16) for _ in range(4)]
+    q, k, v, do = (t.transpose(1, 2) for t in base)
+    kw = dict(scale=0.125, causal=True, key_lens=None, block_mask=None, dropout_p=0.1, seed=3,
+              offset=1)
+    qd, kd, vd, dod = (t.cuda().transpose(1, 2) for t in base)
+    o, lse = ea.attention_fwd(qd, kd, vd, **kw)
+    dq, dk, dv = ea.attention_bwd(dod, qd, kd, vd, o, lse, **kw)
+    _, _, dQ, dK, dV = oracle.attention_backward(np64(q), np64(k), np64(v), np64(do),
+                                                 **dict(kw, key_lens=None, block_mask=None))
+    for got, want in ((dq, dQ), (dk, dK), (dv, dV)):
+        assert rel_l2(np64(got.cpu()), want) <= GRAD_REL_L2
+
+
+def _random_configs(n=14, seed=2026):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        B = int(rng.integers(1, 3))
+        H = int(rng.integers(1, 4))
+        N = int(rng.integers(1, 700))
+        d = int(rng.choice([64, 128]))
+        causal = bool(rng.integers(0, 2))
+        pad = bool(rng.integers(0, 2))
+        drop = float(rng.choice([0.0, 0.0, 0.15, 0.5]))
+        blocks = bool(rng.integers(0, 3) == 0)
+        out.append((B, H, N, d, causal, pad, drop, blocks, int(rng.integers(1 << 30))))
+    return out
+
+
+@pytest.mark.parametrize("cfg", _random_configs())
+def test_random_configurations(ea, cfg):
+    B, H, N, d, causal, pad, drop, blocks, seed = cfg
+    rng = np.random.default_rng(seed)
+    key_lens = [int(x) for x in rng.integers(0, N + 1, B)] if pad else None
+    bm = None
+    if blocks:
+        nb = (N + 127) // 128
+        bm = torch.from_numpy((rng.random((B, H, nb, nb)) < 0.6).astype(np.uint8))
+    inp = _inputs(B, H, N, d, seed=seed % 1000, causal=causal, key_lens=key_lens, block_mask=bm,
+                  dropout_p=drop)
+    _check(ea, inp)

@@ -126,15 +126,16 @@ def test_strided_bnhd_layout(ea):
     assert max_abs(lse.cpu().numpy(), L) <= L_MAX_ABS
 
 
-def test_mask_and_keep_bits_are_exact(ea):
+@pytest.mark.parametrize("d", [64, 128])
+def test_mask_and_keep_bits_are_exact(ea, d):
     """Causal, padding, block and dropout masks, bit-exactly through the API.
 
     With Q = K = 0 every allowed score is 0, so P_ij = 1 / n_allowed(i) on
-    allowed keys.  Making column c of V the indicator of key g*128 + c turns
-    O[i, c] into Z_ij / ((1 - p) n_allowed(i)) for j = g*128 + c: nonzero
+    allowed keys.  Making column c of V the indicator of key g*d + c turns
+    O[i, c] into Z_ij / ((1 - p') n_allowed(i)) for j = g*d + c: nonzero
     exactly where key j is allowed and kept.
     """
-    B, H, N, d = 2, 2, 384, 128
+    B, H, N = 2, 2, 384
     key_lens = torch.tensor([384, 250], dtype=torch.int32)
     bm = torch.tensor([[1, 0, 1], [1, 1, 0], [0, 1, 1]], dtype=torch.uint8)
     p, seed, offset = 0.25, 0xDEADBEEF12345, 9
