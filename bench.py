@@ -38,7 +38,7 @@ SECONDARY = ("long-causal-16384",)
 # DRAM bytes (read + write) per launch of the backward main kernel, from the
 # ncu capture summarised in profiles/bwd_bf16_kernel_bert-large.md; absent
 # (reported as null) for other workloads or once the kernel has changed
-BWD_MAIN_TRAFFIC = {"bert-large": 116.2e6}
+BWD_MAIN_TRAFFIC = {"bert-large": 114.4e6}
 
 
 # ----------------------------------------------------------------- FLOPs --
@@ -383,6 +383,25 @@ def describe(w):
     return ", ".join(parts)
 
 
+# ------------------------------------------------------------- profiling --
+
+def profile_steps(w, n):
+    """`n` forward + backward steps of one resident input set, four kernel
+    launches each (six with a block mask), then a status check."""
+    import exact_attention_12_gb300 as ea
+    from exact_attention_12_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    step = Step(ea, workloads.make_inputs(w), dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(n):
+        step.run(stream)
+    torch.cuda.synchronize(dev)
+    ea.check(step.ws, dev)
+    print(f"profile-steps: {n} steps of {w.name} done")
+
+
 # -------------------------------------------------------------------- main --
 
 def main():
@@ -394,8 +413,15 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing")
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="run this many untimed steps of one input set and exit (a short, "
+                         "fixed launch sequence for ncu captures; no oracle, no JSON line)")
     args = ap.parse_args()
     w = workloads.get(args.workload)
+
+    if args.profile_steps > 0:
+        profile_steps(w, args.profile_steps)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -31,7 +31,8 @@ attn_status cuda_fail(cudaError_t e, const char* what) {
   return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-constexpr size_t kHeaderBytes = 256;   // status words
+constexpr size_t kHeaderBytes = 256;   // status words [0, 8), scheduler words [128, 136)
+constexpr size_t kSchedOffset = 128;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -263,6 +264,7 @@ attn_status attn_fwd(const attn_params* p, const void* q, const void* k, const v
   a.stride_h = p->stride_h;
   a.stride_n = p->stride_n;
   a.status = reinterpret_cast<int*>(w);
+  a.sched = reinterpret_cast<int*>(w + kSchedOffset);
   a.timeout_ns = kTimeoutNs;
 
   cudaError_t e;

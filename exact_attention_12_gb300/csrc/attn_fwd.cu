@@ -49,31 +49,83 @@ namespace {
 
 constexpr float kLn2 = 0.693147180559945309f;
 
-template <int D>
+template <int D, bool DROPOUT = false>
 struct FwdCfg {
   static constexpr int kBoxes = D / 64;               // 64-column TMA boxes per tile
   static constexpr int kBoxBytes = kTile * 128;       // 128 rows x 128 bytes
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kStages = (D == 64) ? 4 : 2;
-  static constexpr int kSmem = 1024 + kTileBytes * (2 + 2 * kStages);
+  // dropout keep masks: per query tile a ring of kMaskStages 128 x 128-bit tiles
+  static constexpr int kMaskStages = 2;
+  static constexpr int kMaskTileBytes = kTile * 16;
+  static constexpr int kMaskBytes = DROPOUT ? 2 * kMaskStages * kMaskTileBytes : 0;
+  static constexpr int kSmem = 1024 + kTileBytes * (2 + 2 * kStages) + kMaskBytes;
   static constexpr uint32_t kSCol = 0, kOCol = 256;   // S_X at kSCol + 128X, O_X at kOCol + D*X
+  // At d = 64 the bf16 P_X has columns of its own (kPCol + 64X), so the
+  // scores of the next key tile can be computed while the softmax still
+  // works on P; at d = 128 the TMEM is full and P_X overwrites S_X.
+  static constexpr bool kSepP = (D == 64);
+  static constexpr uint32_t kPCol = 384;
   // warpgroups 0, 1: softmax of tiles A, B; warpgroup 2: producer (warp 8),
-  // MMA issuer (warp 9), two idle warps.  Registers are re-split after the
-  // start: kRegsSoftmax for the softmax warpgroups, kRegsOther for the rest;
-  // 256 * 208 + 128 * 80 <= 384 * kRegsLaunch.
-  static constexpr int kThreads = 384;
-  static constexpr uint32_t kRegsLaunch = 168, kRegsSoftmax = 208, kRegsOther = 80;
+  // MMA issuer (warp 9), two idle warps; with dropout, warpgroup 3 computes
+  // the keep masks (warp 12 + r: rows 32r .. 32r+31 of both tiles).
+  // Registers are re-split after the start: kRegsSoftmax for the softmax
+  // warpgroups, kRegsOther for warpgroup 2, kRegsMask for warpgroup 3:
+  // 256 * 208 + 128 * 80 <= 384 * 168 and 256 * 200 + 128 * (56 + 56) <= 512 * 128.
+  static constexpr int kThreads = DROPOUT ? 512 : 384;
+  static constexpr uint32_t kRegsLaunch = DROPOUT ? 128 : 168;
+  static constexpr uint32_t kRegsSoftmax = DROPOUT ? 200 : 208;
+  static constexpr uint32_t kRegsOther = DROPOUT ? 56 : 80;
+  static constexpr uint32_t kRegsMask = 56;
+  static_assert(256 * kRegsSoftmax + 128 * kRegsOther + (DROPOUT ? 128 * kRegsMask : 0) <=
+                    kThreads * kRegsLaunch, "register re-split exceeds the launch allocation");
 };
 
-template <int ST>
+// A claimed unit as the producer publishes it to the other roles.
+struct UnitInfo {
+  const uint16_t* idx[2];   // block-mask rows of query tiles A, B (null: dense)
+  int n[2];                 // key tiles A and B visit
+  int pair, bh, b, h, limit;
+  int w;                    // unit index; -1: no more units
+};
+
+// Units a CTA has claimed and not yet handed to every role.
+constexpr int kUnitRing = 4;
+constexpr int kClaimAhead = 2;
+
+template <int ST, int MS>
 struct FwdCtl {
-  uint64_t qfull;
+  uint64_t qfull, qempty, claim;
   uint64_t kfull[ST], vfull[ST], kvempty[ST];
-  uint64_t sfull[2], pfull[2];
+  uint64_t sfull[2], pfull[2], oempty[2];
+  uint64_t sfree[2], pvdone[2];   // separate-P pipeline only
   uint64_t done, final_bar;
+  uint64_t unitfull[kUnitRing], unitempty[kUnitRing];
+  // keep-mask ring, per query tile, stage and 32-row group (mask warp r
+  // feeds softmax warps r and 4 + r)
+  uint64_t maskfull[2][MS][4], maskempty[2][MS][4];
+  UnitInfo unit[kUnitRing];
   uint32_t tmem_base;
   int abort_flag;
 };
+
+// One unit of work: a pair of query tiles of one (b, h) and their key-tile
+// lists.  Units are numbered in head groups of G consecutive (b, h), within
+// a group heaviest pair first; CTAs take units round-robin.
+struct FwdUnit {
+  int pair, bh, b, h, limit;
+};
+
+
+// CTA i starts with unit i; after that CTAs claim units dynamically from a
+// global ticket counter (the scheduler word pair in the workspace header:
+// [0] units claimed beyond the first gridDim.x, [1] CTAs finished).  The producer claims the next unit when the MMA warp signals
+// that the current unit has at most kClaimAhead key tiles left to score (a
+// global atomic takes microseconds, so the claim is made early enough to be
+// answered before the current unit ends, and late enough that a CTA holds no
+// more than one unit it has not started), and publishes it to the MMA and
+// softmax warps through a ring of kUnitRing slots.  The last CTA to make its
+// final claim resets both words to zero for the next launch.
 
 // The key tiles query tile `qt` of head `bh` visits, in ascending order.
 struct TileList {
@@ -146,43 +198,45 @@ __device__ __forceinline__ void mma_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_
 }
 
 template <int D, bool DROPOUT>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, DROPOUT>;
   constexpr int ST = C::kStages;
+  constexpr int MS = C::kMaskStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;                          // Q_A, Q_B
   uint8_t* sK = smem + 2 * C::kTileBytes;
   uint8_t* sV = sK + ST * C::kTileBytes;
-  __shared__ FwdCtl<ST> ctl;
+  uint4* sMask = reinterpret_cast<uint4*>(sV + ST * C::kTileBytes);   // [2][MS][128 rows]
+  __shared__ FwdCtl<ST, MS> ctl;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const MaskArgs& m = a.m;
   const int BH = m.B * m.H;
   const int npairs = (m.nb + 1) / 2;
-  // head groups of G consecutive (b, h); within a group, heaviest pairs first
-  int pair, bh;
-  {
+  const int total = npairs * BH;
+  auto unit_of = [&](int w) {
     const int G = m.head_group, per = G * npairs, nfull = BH / G;
-    const int w = static_cast<int>(blockIdx.x);
     const int g = w < nfull * per ? w / per : nfull;
     const int gs = g < nfull ? G : BH - nfull * G;
     const int rem = w - g * per;
-    pair = npairs - 1 - rem / gs;
-    bh = g * G + rem % gs;
-  }
-  const int b = bh / m.H, h = bh - b * m.H;
-  const int limit = key_limit(m, b);
-  const TileList listA = fwd_tiles(m, 2 * pair, bh, limit);
-  const TileList listB = fwd_tiles(m, 2 * pair + 1, bh, limit);
-  const bool any = listA.n > 0 || listB.n > 0;
+    FwdUnit u;
+    u.pair = npairs - 1 - rem / gs;
+    u.bh = g * G + rem % gs;
+    u.b = u.bh / m.H;
+    u.h = u.bh - u.b * m.H;
+    u.limit = key_limit(m, u.b);
+    return u;
+  };
 
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
     mbar_init(&ctl.qfull, 1);
+    mbar_init(&ctl.qempty, 1);
+    mbar_init(&ctl.claim, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&ctl.kfull[s], 1);
       mbar_init(&ctl.vfull[s], 1);
@@ -191,9 +245,23 @@ __global__ void __launch_bounds__(384, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(&ctl.sfull[x], 1);
       mbar_init(&ctl.pfull[x], 4);
+      mbar_init(&ctl.oempty[x], 4);
+      mbar_init(&ctl.sfree[x], 4);
+      mbar_init(&ctl.pvdone[x], 1);
     }
     mbar_init(&ctl.done, 1);
     mbar_init(&ctl.final_bar, 1);
+    for (int r = 0; r < kUnitRing; ++r) {
+      mbar_init(&ctl.unitfull[r], 1);
+      // the MMA thread, the eight softmax warps and the four mask warps
+      mbar_init(&ctl.unitempty[r], DROPOUT ? 13 : 9);
+    }
+    for (int x = 0; x < 2; ++x)
+      for (int st = 0; st < MS; ++st)
+        for (int g = 0; g < 4; ++g) {
+          mbar_init(&ctl.maskfull[x][st][g], 1);
+          mbar_init(&ctl.maskempty[x][st][g], 1);
+        }
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -206,42 +274,84 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = ctl.tmem_base;
   const WaitCtx wc{&ctl.abort_flag, a.status, a.timeout_ns};
   const int wg = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 128, 0);
+
   if (wg == 2) {
     regs_decrease<C::kRegsOther>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && any) {
+    if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      mbar_arrive_expect_tx(&ctl.qfull, 2 * C::kTileBytes);
+      int t = 0;      // key/value tiles loaded by this CTA (all units)
+      int kw = 0;     // units with work
+      bool ok = true;
+      for (int pub = 0;; ++pub) {
+        // the previous unit is close to its end: claim the next one
+        if (kw >= 1 && !(ok = mbar_wait(&ctl.claim, (kw - 1) & 1, wc, kSiteFwdUnit))) break;
+        // CTA i starts with unit i; later units come from the counter
+        const int w = pub == 0 ? static_cast<int>(blockIdx.x)
+                               : static_cast<int>(gridDim.x) + atomicAdd(a.sched, 1);
+        UnitInfo ui{};
+        ui.w = -1;
+        if (w < total) {
+          const FwdUnit u = unit_of(w);
+          const TileList la = fwd_tiles(m, 2 * u.pair, u.bh, u.limit);
+          const TileList lb = fwd_tiles(m, 2 * u.pair + 1, u.bh, u.limit);
+          ui = UnitInfo{{la.idx, lb.idx}, {la.n, lb.n}, u.pair, u.bh, u.b, u.h, u.limit, w};
+        }
+        const int r = pub % kUnitRing;
+        if (pub >= kUnitRing &&
+            !(ok = mbar_wait(&ctl.unitempty[r], ((pub / kUnitRing) - 1) & 1, wc, kSiteFwdUnit)))
+          break;
+        ctl.unit[r] = ui;
+        mbar_arrive(&ctl.unitfull[r]);   // release: the consumers' wait acquires unit[r]
+        if (ui.w < 0) break;
+        const FwdUnit u{ui.pair, ui.bh, ui.b, ui.h, ui.limit};
+        const TileList listA{ui.idx[0], ui.n[0]}, listB{ui.idx[1], ui.n[1]};
+        if (listA.n == 0 && listB.n == 0) continue;
+        // the previous unit's score MMAs are done with Q
+        if (kw >= 1 && !(ok = mbar_wait(&ctl.qempty, (kw - 1) & 1, wc, kSiteFwdQ))) break;
+        mbar_arrive_expect_tx(&ctl.qfull, 2 * C::kTileBytes);
 #pragma unroll
-      for (int x = 0; x < C::kBoxes; ++x) {
-        tma_load_4d(sQ + x * C::kBoxBytes, &tq, &ctl.qfull, x * 64, 2 * pair * kTile, h, b);
-        tma_load_4d(sQ + C::kTileBytes + x * C::kBoxBytes, &tq, &ctl.qfull, x * 64,
-                    (2 * pair + 1) * kTile, h, b);
+        for (int x = 0; x < C::kBoxes; ++x) {
+          tma_load_4d(sQ + x * C::kBoxBytes, &tq, &ctl.qfull, x * 64, 2 * u.pair * kTile, u.h,
+                      u.b);
+          tma_load_4d(sQ + C::kTileBytes + x * C::kBoxBytes, &tq, &ctl.qfull, x * 64,
+                      (2 * u.pair + 1) * kTile, u.h, u.b);
+        }
+        ++kw;
+        PairWalk walk{listA, listB};
+        int j;
+        bool na, nb;
+        while (walk.next(j, na, nb)) {
+          const int s = t % ST;
+          if (t >= ST && !(ok = mbar_wait(&ctl.kvempty[s], ((t / ST) - 1) & 1, wc, kSiteFwdKvEmpty)))
+            break;
+          const int kv0 = j * kTile;
+          uint8_t* dk = sK + s * C::kTileBytes;
+          uint8_t* dv = sV + s * C::kTileBytes;
+          mbar_arrive_expect_tx(&ctl.kfull[s], C::kTileBytes);
+#pragma unroll
+          for (int x = 0; x < C::kBoxes; ++x)
+            tma_load_4d(dk + x * C::kBoxBytes, &tk, &ctl.kfull[s], x * 64, kv0, u.h, u.b);
+          mbar_arrive_expect_tx(&ctl.vfull[s], C::kTileBytes);
+#pragma unroll
+          for (int x = 0; x < C::kBoxes; ++x)
+            tma_load_4d(dv + x * C::kBoxBytes, &tv, &ctl.vfull[s], x * 64, kv0, u.h, u.b);
+          ++t;
+        }
       }
-      PairWalk walk{listA, listB};
-      int j, t = 0;
-      bool na, nb;
-      while (walk.next(j, na, nb)) {
-        const int s = t % ST;
-        if (t >= ST && !mbar_wait(&ctl.kvempty[s], ((t / ST) - 1) & 1, wc, kSiteFwdKvEmpty)) break;
-        const int kv0 = j * kTile;
-        uint8_t* dk = sK + s * C::kTileBytes;
-        uint8_t* dv = sV + s * C::kTileBytes;
-        mbar_arrive_expect_tx(&ctl.kfull[s], C::kTileBytes);
-#pragma unroll
-        for (int x = 0; x < C::kBoxes; ++x)
-          tma_load_4d(dk + x * C::kBoxBytes, &tk, &ctl.kfull[s], x * 64, kv0, h, b);
-        mbar_arrive_expect_tx(&ctl.vfull[s], C::kTileBytes);
-#pragma unroll
-        for (int x = 0; x < C::kBoxes; ++x)
-          tma_load_4d(dv + x * C::kBoxBytes, &tv, &ctl.vfull[s], x * 64, kv0, h, b);
-        ++t;
+      // this CTA makes no further claims; the last CTA to get here resets the
+      // scheduler words for the next launch (every other CTA's claims are
+      // ordered before its count by the fence)
+      __threadfence();
+      if (atomicAdd(a.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+        atomicExch(a.sched, 0);
+        atomicExch(a.sched + 1, 0);
       }
       if (ctl.abort_flag) {   // let issued copies land before the CTA exits
-        mbar_wait_drain(&ctl.qfull, 0, a.timeout_ns);
+        if (kw >= 1) mbar_wait_drain(&ctl.qfull, (kw - 1) & 1, a.timeout_ns);
         for (int tt = max(0, t - ST); tt < t; ++tt) {
           mbar_wait_drain(&ctl.kfull[tt % ST], (tt / ST) & 1, a.timeout_ns);
           mbar_wait_drain(&ctl.vfull[tt % ST], (tt / ST) & 1, a.timeout_ns);
@@ -250,210 +360,373 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------- MMA issue
-    if (lane == 0 && any) {
+    if (lane == 0) {
       const uint32_t q_base[2] = {smem_u32(sQ), smem_u32(sQ + C::kTileBytes)};
-      uint32_t cnt[2] = {0, 0};   // tiles each query tile has started
-      bool ok = mbar_wait(&ctl.qfull, 0, wc, kSiteFwdQ);
-      PairWalk walk{listA, listB};
-      int j;
-      bool need[2], need_next[2];
-      bool have = walk.next(j, need[0], need[1]);
-      // prologue: scores of the first key tile
-      if (ok && have) {
-        ok = mbar_wait(&ctl.kfull[0], 0, wc, kSiteFwdK);
-        if (ok) {
-          tc_fence_after();
+      uint32_t cnt[2] = {0, 0};   // P tiles consumed per query-tile slot (all units)
+      uint32_t cs_issued[2] = {0, 0};   // S tiles issued per slot (separate-P pipeline)
+      int t = 0;                  // key/value tiles consumed (all units)
+      int kw = 0;                 // units with work
+      bool ok = true;
+      for (int pub = 0; ok; ++pub) {
+        const int r = pub % kUnitRing;
+        if (!(ok = mbar_wait(&ctl.unitfull[r], (pub / kUnitRing) & 1, wc, kSiteFwdUnit))) break;
+        const UnitInfo ui = ctl.unit[r];
+        mbar_arrive(&ctl.unitempty[r]);
+        if (ui.w < 0) break;
+        const TileList listA{ui.idx[0], ui.n[0]}, listB{ui.idx[1], ui.n[1]};
+        if (listA.n == 0 && listB.n == 0) continue;
+        if (!(ok = mbar_wait(&ctl.qfull, kw & 1, wc, kSiteFwdQ))) break;
+        PairWalk walk{listA, listB};
+        int j;
+        bool need[2], need_next[2];
+        bool have = walk.next(j, need[0], need[1]);
+        // scores of the first key tile
+        if (!(ok = mbar_wait(&ctl.kfull[t % ST], (t / ST) & 1, wc, kSiteFwdK))) break;
+        tc_fence_after();
 #pragma unroll
-          for (int x = 0; x < 2; ++x)
-            if (need[x]) {
-              mma_scores<D>(tmem + C::kSCol + 128 * x, q_base[x], smem_u32(sK));
-              mma_commit(&ctl.sfull[x]);
-            }
-        }
-      }
-      for (int t = 0; ok && have; ++t) {
-        const int s = t % ST;
-        const int s1 = (t + 1) % ST;
-        int jn;
-        const bool have_next = walk.next(jn, need_next[0], need_next[1]);
-        bool k_next_ready = false, v_ready = false;
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          if (need[x]) {   // O_X += P_X V_t
-            ok = mbar_wait(&ctl.pfull[x], cnt[x] & 1, wc, kSiteFwdPFull);
-            if (ok && !v_ready) ok = v_ready = mbar_wait(&ctl.vfull[s], (t / ST) & 1, wc, kSiteFwdV);
-            if (!ok) break;
-            tc_fence_after();
-            mma_pv<D>(tmem + C::kOCol + D * x, tmem + C::kSCol + 128 * x,
-                      smem_u32(sV + s * C::kTileBytes), cnt[x] > 0);
-            ++cnt[x];
-          }
-          if (x == 1) mma_commit(&ctl.kvempty[s]);   // K_t, V_t no longer needed
-          if (have_next && need_next[x]) {   // S_X = Q_X K_{t+1}^T
-            if (!k_next_ready) {
-              ok = k_next_ready = mbar_wait(&ctl.kfull[s1], ((t + 1) / ST) & 1, wc, kSiteFwdK);
-              if (!ok) break;
+        for (int x = 0; x < 2; ++x)
+          if (need[x]) {
+            if constexpr (C::kSepP) {   // the softmax has read the previous S_X
+              if (cs_issued[x] >= 1 &&
+                  !(ok = mbar_wait(&ctl.sfree[x], (cs_issued[x] - 1) & 1, wc, kSiteFwdSFree)))
+                break;
               tc_fence_after();
+              ++cs_issued[x];
             }
-            mma_scores<D>(tmem + C::kSCol + 128 * x, q_base[x], smem_u32(sK + s1 * C::kTileBytes));
+            mma_scores<D>(tmem + C::kSCol + 128 * x, q_base[x], smem_u32(sK + (t % ST) * C::kTileBytes));
             mma_commit(&ctl.sfull[x]);
           }
+        if (!ok) break;
+        // O of both tiles was read by the previous unit's epilogues
+        if (kw >= 1) {
+          if (!(ok = mbar_wait(&ctl.oempty[0], (kw - 1) & 1, wc, kSiteFwdPvDone) &&
+                     mbar_wait(&ctl.oempty[1], (kw - 1) & 1, wc, kSiteFwdPvDone)))
+            break;
+          tc_fence_after();
         }
-        j = jn;
-        need[0] = need_next[0];
-        need[1] = need_next[1];
-        have = have_next;
+        bool first[2] = {true, true};
+        bool claimed = false;
+        for (; ok && have; ++t) {
+          const int s = t % ST;
+          const int s1 = (t + 1) % ST;
+          int jn;
+          const bool have_next = walk.next(jn, need_next[0], need_next[1]);
+          if (!have_next) mma_commit(&ctl.qempty);   // every score MMA of the unit is issued
+          if (!claimed && walk.a.n - walk.ia <= kClaimAhead && walk.b.n - walk.ib <= kClaimAhead) {
+            mbar_arrive(&ctl.claim);   // once per unit; at the latest in its last iteration
+            claimed = true;
+          }
+          if constexpr (C::kSepP) {
+            // S_X = Q_X K_{t+1}^T as soon as the softmax has read S_X(t) ...
+            bool k_next_ready = false;
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+              if (!(have_next && need_next[x])) continue;
+              if (cs_issued[x] >= 1 &&
+                  !(ok = mbar_wait(&ctl.sfree[x], (cs_issued[x] - 1) & 1, wc, kSiteFwdSFree)))
+                break;
+              if (!k_next_ready &&
+                  !(ok = k_next_ready = mbar_wait(&ctl.kfull[s1], ((t + 1) / ST) & 1, wc, kSiteFwdK)))
+                break;
+              tc_fence_after();
+              mma_scores<D>(tmem + C::kSCol + 128 * x, q_base[x], smem_u32(sK + s1 * C::kTileBytes));
+              mma_commit(&ctl.sfull[x]);
+              ++cs_issued[x];
+            }
+            if (!ok) break;
+            // ... then O_X += P_X V_t once P_X(t) is written
+            bool v_ready = false;
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+              if (!need[x]) continue;
+              ok = mbar_wait(&ctl.pfull[x], cnt[x] & 1, wc, kSiteFwdPFull);
+              if (ok && !v_ready) ok = v_ready = mbar_wait(&ctl.vfull[s], (t / ST) & 1, wc, kSiteFwdV);
+              if (!ok) break;
+              tc_fence_after();
+              mma_pv<D>(tmem + C::kOCol + D * x, tmem + C::kPCol + 64 * x,
+                        smem_u32(sV + s * C::kTileBytes), !first[x]);
+              mma_commit(&ctl.pvdone[x]);
+              first[x] = false;
+              ++cnt[x];
+            }
+            if (!ok) break;
+            mma_commit(&ctl.kvempty[s]);   // K_t, V_t no longer needed
+          } else {
+            bool k_next_ready = false, v_ready = false;
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+              if (need[x]) {   // O_X += P_X V_t
+                ok = mbar_wait(&ctl.pfull[x], cnt[x] & 1, wc, kSiteFwdPFull);
+                if (ok && !v_ready) ok = v_ready = mbar_wait(&ctl.vfull[s], (t / ST) & 1, wc, kSiteFwdV);
+                if (!ok) break;
+                tc_fence_after();
+                mma_pv<D>(tmem + C::kOCol + D * x, tmem + C::kSCol + 128 * x,
+                          smem_u32(sV + s * C::kTileBytes), !first[x]);
+                first[x] = false;
+                ++cnt[x];
+              }
+              if (x == 1) mma_commit(&ctl.kvempty[s]);   // K_t, V_t no longer needed
+              if (have_next && need_next[x]) {   // S_X = Q_X K_{t+1}^T
+                if (!k_next_ready) {
+                  ok = k_next_ready = mbar_wait(&ctl.kfull[s1], ((t + 1) / ST) & 1, wc, kSiteFwdK);
+                  if (!ok) break;
+                  tc_fence_after();
+                }
+                mma_scores<D>(tmem + C::kSCol + 128 * x, q_base[x], smem_u32(sK + s1 * C::kTileBytes));
+                mma_commit(&ctl.sfull[x]);
+              }
+            }
+          }
+          j = jn;
+          need[0] = need_next[0];
+          need[1] = need_next[1];
+          have = have_next;
+        }
+        if (ok) mma_commit(&ctl.done);
+        ++kw;
       }
-      if (ok) mma_commit(&ctl.done);
       mma_commit(&ctl.final_bar);   // every MMA of this CTA done before TMEM is freed
       mbar_wait_drain(&ctl.final_bar, 0, a.timeout_ns);
     }
   }
+  } else if (wg == 3) {
+    if constexpr (DROPOUT) {
+      regs_decrease<C::kRegsMask>();
+      // ------------------------------------------------------ dropout masks
+      // Rows 32r .. 32r+31 of both query tiles, one row per lane; the tiles
+      // in the order the softmax warps consume them.
+      const int grp = warp - 12;
+      const int row = grp * 32 + lane;
+      uint32_t mc[2] = {0, 0};   // mask tiles produced per query-tile slot (all units)
+      bool ok = true;
+      for (int pub = 0; ok; ++pub) {
+        const int r = pub % kUnitRing;
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&ctl.unitfull[r], (pub / kUnitRing) & 1, wc, kSiteFwdUnit));
+        if (!ok) break;
+        const UnitInfo ui = ctl.unit[r];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.unitempty[r]);
+        if (ui.w < 0) break;
+        const int pair = ui.pair, bh = ui.bh;
+        PairWalk walk{TileList{ui.idx[0], ui.n[0]}, TileList{ui.idx[1], ui.n[1]}};
+        int j;
+        bool need[2];
+        while (ok && walk.next(j, need[0], need[1])) {
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (!need[x]) continue;
+            const int st = mc[x] % MS;
+            if (mc[x] >= MS) {
+              ok = __all_sync(0xffffffffu, mbar_wait(&ctl.maskempty[x][st][grp],
+                                                     ((mc[x] / MS) - 1) & 1, wc, kSiteFwdMask));
+              if (!ok) break;
+            }
+            const uint32_t qi = static_cast<uint32_t>((2 * pair + x) * kTile + row);
+            // one 32-key word per iteration; the loop stays rolled to keep the
+            // kernel's code within the instruction cache
+            uint32_t* dst = reinterpret_cast<uint32_t*>(&sMask[(x * MS + st) * kTile + row]);
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q)
+              dst[q] = dropout_keep32(static_cast<uint32_t>(j * (kTile / 8) + 4 * q), qi,
+                                      static_cast<uint32_t>(bh), m.offset, m.rk,
+                                      m.drop_threshold);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.maskfull[x][st][grp]);
+            ++mc[x];
+          }
+        }
+      }
+    }
   } else {
     regs_increase<C::kRegsSoftmax>();
     // ---------------------------------------------------- softmax, epilogue
     const int x = warp >> 2;                        // query tile: 0 = A, 1 = B
     const int row = (warp & 3) * 32 + lane;         // TMEM lane == row within the tile
-    const int q0 = (2 * pair + x) * kTile;
-    const int qi = q0 + row;
-    const TileList tiles = x ? listB : listA;
-    const int n = tiles.n;
     const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t sc = tl + C::kSCol + 128 * x;    // this tile's S (and P) columns
     const uint32_t oc = tl + C::kOCol + D * x;      // this tile's O columns
+    const uint32_t pc = tl + C::kPCol + 64 * x;     // this tile's P columns (separate-P)
     const float c2 = a.scale_log2;
-    float m_used = -INFINITY;      // raw-score max the exponentials are taken against
-    float l_sum = 0.f;
+    uint32_t cs = 0;   // score tiles of this slot processed (all units)
+    int kw = 0;        // units with work
     bool ok = true;
-    for (int jj = 0; jj < n; ++jj) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.sfull[x], jj & 1, wc, kSiteFwdSFull));
+    for (int pub = 0; ok; ++pub) {
+      const int r = pub % kUnitRing;
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&ctl.unitfull[r], (pub / kUnitRing) & 1, wc, kSiteFwdUnit));
       if (!ok) break;
-      tc_fence_after();
-      const int kv0 = tiles[jj] * kTile;
-      const int col_lim = min(limit - kv0, kTile);
-      const bool diag = m.causal && kv0 == q0;
-      // the whole S row: four loads in flight, one wait
-      uint32_t sr[128];
-#pragma unroll
-      for (int c = 0; c < 128; c += 32) tmem_ld32(sc + c, sr + c);
-      tmem_wait_ld();
-      if (col_lim < kTile || diag) {
-        const int lim = diag ? min(col_lim, row + 1) : col_lim;
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+      const UnitInfo ui = ctl.unit[r];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.unitempty[r]);
+      if (ui.w < 0) break;
+      const TileList tiles{x ? ui.idx[1] : ui.idx[0], x ? ui.n[1] : ui.n[0]};
+      const bool any = ui.n[0] > 0 || ui.n[1] > 0;
+      const int bh = ui.bh, b = ui.b, h = ui.h, limit = ui.limit;
+      const int q0 = (2 * ui.pair + x) * kTile;
+      const int qi = q0 + row;
+      const int n = tiles.n;
+      float m_used = -INFINITY;      // raw-score max the exponentials are taken against
+      float l_sum = 0.f;
+      for (int jj = 0; jj < n; ++jj, ++cs) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl.sfull[x], cs & 1, wc, kSiteFwdSFull));
+        if (!ok) break;
+        tc_fence_after();
+        const int kv0 = tiles[jj] * kTile;
+        const int col_lim = min(limit - kv0, kTile);
+        const bool diag = m.causal && kv0 == q0;
+        // the whole S row: four loads in flight, one wait
+        uint32_t sr[128];
+  #pragma unroll
+        for (int c = 0; c < 128; c += 32) tmem_ld32(sc + c, sr + c);
+        tmem_wait_ld();
+        if constexpr (C::kSepP) {   // S_X may be overwritten by the next key tile's scores
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.sfree[x]);
+        }
+        if (col_lim < kTile || diag) {
+          const int lim = diag ? min(col_lim, row + 1) : col_lim;
+  #pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+  #pragma unroll
+        for (int c = 0; c < 128; c += 8) {
+          mx0 = max3f(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+          mx1 = max3f(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+          mx2 = max3f(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+          mx3 = max3f(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+        }
+        const float m_new = max3f(m_used, max3f(mx0, mx1, mx2), mx3);
+        const bool need =
+            m_new > m_used && (m_used == -INFINITY || (m_new - m_used) * c2 > kRescaleTau);
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2_approx((m_used - m_new) * c2);
+          m_used = m_new;
+          l_sum *= alpha;
+        }
+        if constexpr (C::kSepP) {   // O_X += P_X V of the previous key tile is complete
+          if (jj >= 1) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&ctl.pvdone[x], (cs - 1) & 1, wc, kSiteFwdPvDone));
+            if (!ok) break;
+            tc_fence_after();
+          }
+        }
+        if (jj >= 1 && __any_sync(0xffffffffu, need)) {
+          // O holds the sum through the previous key tile (complete: see above)
+  #pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(oc + c, o);
+            tmem_wait_ld();
+  #pragma unroll
+            for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+            tmem_st32(oc + c, o);
+          }
+        }
+        // P = 2^(S c2 - m c2) (masked entries are -inf: 2^-inf = 0), bf16 over
+        // the first 64 columns of S
+        const float mc = (m_used == -INFINITY) ? 0.f : m_used * c2;
+        const uint64_t c2x2 = f2_pack(c2, c2), nmc2 = f2_pack(-mc, -mc);
+        uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+        uint32_t keepw[4] = {~0u, ~0u, ~0u, ~0u};
+        if constexpr (DROPOUT) {   // this row's 128 keep bits, from the mask warps
+          const int st = cs % MS, grp = warp & 3;
+          ok = __all_sync(0xffffffffu, mbar_wait(&ctl.maskfull[x][st][grp], (cs / MS) & 1, wc,
+                                                 kSiteFwdMask));
+          if (!ok) break;
+          const uint4 kb = sMask[(x * MS + st) * kTile + row];
+          keepw[0] = kb.x;
+          keepw[1] = kb.y;
+          keepw[2] = kb.z;
+          keepw[3] = kb.w;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.maskempty[x][st][grp]);
+        }
+  #pragma unroll
+        for (int c = 0; c < 128; c += 32) {
+          const uint32_t keep = keepw[c / 32];
+          uint32_t pk[16];
+  #pragma unroll
+          for (int t = 0; t < 32; t += 4) {
+            float x0, x1, x2, x3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c + t]), __uint_as_float(sr[c + t + 1])),
+                             c2x2, nmc2), x0, x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c + t + 2]), __uint_as_float(sr[c + t + 3])),
+                             c2x2, nmc2), x2, x3);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+            acc0 = f2_add(acc0, f2_pack(p0, p1));
+            acc1 = f2_add(acc1, f2_pack(p2, p3));
+            if constexpr (DROPOUT) {
+              p0 = ((keep >> t) & 1u) ? p0 : 0.f;
+              p1 = ((keep >> (t + 1)) & 1u) ? p1 : 0.f;
+              p2 = ((keep >> (t + 2)) & 1u) ? p2 : 0.f;
+              p3 = ((keep >> (t + 3)) & 1u) ? p3 : 0.f;
+            }
+            pk[t / 2] = pack_bf16x2(p0, p1);
+            pk[t / 2 + 1] = pack_bf16x2(p2, p3);
+          }
+          if constexpr (C::kSepP)
+            tmem_st16(pc + c / 2, pk);
+          else
+            tmem_st16(sc + c / 2, pk);   // S columns [c/2, c/2+16) are already in registers
+        }
+        float ls0, ls1, ls2, ls3;
+        f2_unpack(acc0, ls0, ls1);
+        f2_unpack(acc1, ls2, ls3);
+        ls0 += ls2;
+        ls1 += ls3;
+        l_sum += ls0 + ls1;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.pfull[x]);
       }
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 128; c += 8) {
-        mx0 = max3f(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-        mx1 = max3f(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-        mx2 = max3f(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-        mx3 = max3f(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+      if (!ok) break;
+      if (any) {   // every warp takes every phase of `done`, so none falls two behind
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl.done, kw & 1, wc, kSiteFwdPvDone));
+        if (!ok) break;
+        tc_fence_after();
       }
-      const float m_new = max3f(m_used, max3f(mx0, mx1, mx2), mx3);
-      const bool need =
-          m_new > m_used && (m_used == -INFINITY || (m_new - m_used) * c2 > kRescaleTau);
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2_approx((m_used - m_new) * c2);
-        m_used = m_new;
-        l_sum *= alpha;
-      }
-      if (jj >= 1 && __any_sync(0xffffffffu, need)) {
-        // O holds the sum through the previous key tile (complete: see above)
+      if (q0 < m.N) {
+        const bool live = l_sum > 0.f;
+        const float inv = live ? m.drop_scale / l_sum : 0.f;
+        const float L = live ? (m_used * c2 + __log2f(l_sum)) * kLn2 : -INFINITY;
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) + b * a.stride_b + h * a.stride_h +
+                              static_cast<int64_t>(qi) * a.stride_n;
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
           uint32_t o[32];
-          tmem_ld32(oc + c, o);
-          tmem_wait_ld();
+          if (n > 0) {
+            tmem_ld32(oc + c, o);
+            tmem_wait_ld();
+          } else {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-          tmem_st32(oc + c, o);
-        }
-      }
-      // P = 2^(S c2 - m c2) (masked entries are -inf: 2^-inf = 0), bf16 over
-      // the first 64 columns of S
-      const float mc = (m_used == -INFINITY) ? 0.f : m_used * c2;
-      const uint64_t c2x2 = f2_pack(c2, c2), nmc2 = f2_pack(-mc, -mc);
-      uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-#pragma unroll
-      for (int c = 0; c < 128; c += 32) {
-        uint32_t keep = 0xffffffffu;
-        if constexpr (DROPOUT) {
-          keep = 0;
-#pragma unroll
-          for (int g = 0; g < 4; ++g)
-            keep |= dropout_keep8(static_cast<uint32_t>((kv0 + c) / 8 + g), static_cast<uint32_t>(qi),
-                                  static_cast<uint32_t>(bh), m.offset, m.rk, m.drop_threshold)
-                    << (8 * g);
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int t = 0; t < 32; t += 4) {
-          float x0, x1, x2, x3;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c + t]), __uint_as_float(sr[c + t + 1])),
-                           c2x2, nmc2), x0, x1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c + t + 2]), __uint_as_float(sr[c + t + 3])),
-                           c2x2, nmc2), x2, x3);
-          float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-          acc0 = f2_add(acc0, f2_pack(p0, p1));
-          acc1 = f2_add(acc1, f2_pack(p2, p3));
-          if constexpr (DROPOUT) {
-            p0 = ((keep >> t) & 1u) ? p0 : 0.f;
-            p1 = ((keep >> (t + 1)) & 1u) ? p1 : 0.f;
-            p2 = ((keep >> (t + 2)) & 1u) ? p2 : 0.f;
-            p3 = ((keep >> (t + 3)) & 1u) ? p3 : 0.f;
+            for (int t = 0; t < 32; ++t) o[t] = 0u;
           }
-          pk[t / 2] = pack_bf16x2(p0, p1);
-          pk[t / 2 + 1] = pack_bf16x2(p2, p3);
+          uint32_t pk[16];
+#pragma unroll
+          for (int t = 0; t < 32; t += 2)
+            pk[t / 2] = pack_bf16x2(__uint_as_float(o[t]) * inv, __uint_as_float(o[t + 1]) * inv);
+          if (qi < m.N) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              dst[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+          }
         }
-        tmem_st16(sc + c / 2, pk);   // S columns [c/2, c/2+16) are already in registers
+        if (qi < m.N) a.lse[static_cast<int64_t>(bh) * m.N + qi] = L;
       }
-      float ls0, ls1, ls2, ls3;
-      f2_unpack(acc0, ls0, ls1);
-      f2_unpack(acc1, ls2, ls3);
-      ls0 += ls2;
-      ls1 += ls3;
-      l_sum += ls0 + ls1;
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.pfull[x]);
-    }
-
-    if (ok && any) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.done, 0, wc, kSiteFwdPvDone));
-      if (ok) tc_fence_after();
-    }
-    if (ok && q0 < m.N) {
-      const bool live = l_sum > 0.f;
-      const float inv = live ? m.drop_scale / l_sum : 0.f;
-      const float L = live ? (m_used * c2 + __log2f(l_sum)) * kLn2 : -INFINITY;
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) + b * a.stride_b + h * a.stride_h +
-                            static_cast<int64_t>(qi) * a.stride_n;
-#pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        if (n > 0) {
-          tmem_ld32(oc + c, o);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int t = 0; t < 32; ++t) o[t] = 0u;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int t = 0; t < 32; t += 2)
-          pk[t / 2] = pack_bf16x2(__uint_as_float(o[t]) * inv, __uint_as_float(o[t + 1]) * inv);
-        if (qi < m.N) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            dst[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
-        }
+      if (any) {   // this tile's O has been read: the next unit may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.oempty[x]);
+        ++kw;
       }
-      if (qi < m.N) a.lse[static_cast<int64_t>(bh) * m.N + qi] = L;
     }
   }
 
@@ -467,7 +740,7 @@ __global__ void __launch_bounds__(384, 1)
 
 template <int D, bool DROP>
 cudaError_t launch_one(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, DROP>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, DROP>,
@@ -479,7 +752,13 @@ cudaError_t launch_one(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
     if (static_cast<uint32_t>(fa.numRegs) < C::kRegsLaunch) return cudaErrorInvalidConfiguration;
     attr_set = true;
   }
-  const unsigned grid = static_cast<unsigned>((a.m.nb + 1) / 2) * a.m.B * a.m.H;
+  // persistent: at most one CTA per SM, each walking its share of the units
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long units = static_cast<long long>((a.m.nb + 1) / 2) * a.m.B * a.m.H;
+  const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
   fwd_bf16_kernel<D, DROP><<<grid, C::kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, a);
   return cudaGetLastError();
 }

@@ -15,7 +15,7 @@ constexpr float kRescaleTau = 8.0f;   // lazy-rescale threshold, log2 units
 // Where a kernel gave up waiting (recorded next to the status code).
 enum WaitSite : int {
   kSiteFwdQ = 1, kSiteFwdK, kSiteFwdV, kSiteFwdKvEmpty, kSiteFwdSFull, kSiteFwdSFree,
-  kSiteFwdPFull, kSiteFwdPvDone,
+  kSiteFwdPFull, kSiteFwdPvDone, kSiteFwdUnit, kSiteFwdMask,
   kSiteBwdLoad = 20, kSiteBwdKV, kSiteBwdQ, kSiteBwdMma, kSiteBwdSoft, kSiteBwdDq,
   kSiteBwdEmpty, kSiteBwdFree, kSiteBwdSmem
 };
@@ -57,6 +57,7 @@ struct FwdArgs {
   float* lse;                     // [B,H,N]
   int64_t stride_b, stride_h, stride_n;
   int* status;                    // workspace status words
+  int* sched;                     // workspace scheduler words: next unit, CTAs finished
   uint64_t timeout_ns;
 };
 

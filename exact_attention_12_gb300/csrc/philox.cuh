@@ -44,22 +44,53 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxRoundKeys& r
   return c;
 }
 
-// Keep bits of eight consecutive keys j = 8g .. 8g+7 of query row i.  Word w
-// of the Philox output holds the 16-bit uniforms of keys 8g+2w (low half)
-// and 8g+2w+1 (high half); key j is kept iff its uniform >= threshold.  Bit t
+// Shifts the keep bits of one Philox output into `acc`, most significant key
+// first: word w holds the 16-bit uniforms of keys 2w (low half) and 2w+1
+// (high half) of its group of eight, and a key is kept iff its uniform is at
+// least the threshold T (1 <= T <= 65535).  With k16 = (2^16 - T) << 16, a
+// half h is >= T exactly when (h << 16) + k16 carries out of 32 bits, and
+// the carry is shifted in by acc + acc + carry.  Afterwards the low eight
+// bits of acc hold keys 0..7 of the group (bit t = key t).
+__device__ __forceinline__ uint32_t push_keep8(uint32_t acc, uint4 u, uint32_t k16) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 3; k >= 0; --k)
+    asm("{\n\t.reg .u32 t;\n\t"
+        "add.cc.u32 t, %1, %2;\n\t"     // high half (key 2k+1)
+        "addc.u32 %0, %0, %0;\n\t"
+        "shl.b32 t, %1, 16;\n\t"
+        "add.cc.u32 t, t, %2;\n\t"      // low half (key 2k)
+        "addc.u32 %0, %0, %0;\n\t}"
+        : "+r"(acc)
+        : "r"(w[k]), "r"(k16));
+  return acc;
+}
+
+__device__ __forceinline__ uint32_t keep_k16(uint32_t threshold) {
+  return (0x10000u - threshold) << 16;
+}
+
+// Keep bits of eight consecutive keys j = 8g .. 8g+7 of query row i: bit t
 // of the result is 1 iff key 8g+t is kept.
 __device__ __forceinline__ uint32_t dropout_keep8(uint32_t g, uint32_t i, uint32_t bh,
                                                   uint32_t offset, const PhiloxRoundKeys& rk,
                                                   uint32_t threshold) {
-  const uint4 u = philox4x32_10(make_uint4(g, i, bh, offset), rk);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-  uint32_t bits = 0;
+  return push_keep8(0u, philox4x32_10(make_uint4(g, i, bh, offset), rk), keep_k16(threshold));
+}
+
+// Keep bits of the 32 keys j = 8g .. 8g+31 of query row i (four Philox
+// calls): bit t of the result is 1 iff key 8g+t is kept.
+__device__ __forceinline__ uint32_t dropout_keep32(uint32_t g, uint32_t i, uint32_t bh,
+                                                   uint32_t offset, const PhiloxRoundKeys& rk,
+                                                   uint32_t threshold) {
+  uint4 u[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    bits |= ((w[k] & 0xFFFFu) >= threshold ? 1u : 0u) << (2 * k);
-    bits |= ((w[k] >> 16) >= threshold ? 1u : 0u) << (2 * k + 1);
-  }
-  return bits;
+  for (uint32_t s = 0; s < 4; ++s) u[s] = philox4x32_10(make_uint4(g + s, i, bh, offset), rk);
+  const uint32_t k16 = keep_k16(threshold);
+  uint32_t acc = 0;
+#pragma unroll
+  for (int s = 3; s >= 0; --s) acc = push_keep8(acc, u[s], k16);
+  return acc;
 }
 
 // Keep bits of the 32 query rows q0 .. q0+31 for key kj, where the eight

@@ -43,8 +43,10 @@
  * Ownership: the caller allocates and owns every buffer, including the
  * workspace `ws` (device memory, at least attn_workspace_size() bytes).  The
  * library allocates nothing and keeps no state between calls.  The first
- * 256 bytes of a workspace hold a device status word and must be zero before
- * the workspace is first used; attn_check() reads and clears it.
+ * 256 bytes of a workspace hold a device status word and the forward's work
+ * counter, and must be zero before the workspace is first used; every
+ * forward leaves the counter at zero when it completes, and attn_check()
+ * reads and clears the status word.
  *
  * Streams: every call only enqueues work on `stream` (a cudaStream_t; NULL is
  * the legacy default stream) and returns.  Argument errors are detected on
