@@ -26,6 +26,14 @@ inputs the GPU sees:
 A row with no allowed key has L = -inf, P = 0, O = 0 and contributes nothing
 to any gradient.
 
+Grouped-query attention ("3.3 Hiểu sâu cơ chế Self-Attention", §9.2 MQA and
+§9.3 GQA): K and V may have H_kv heads, H_kv dividing H; the query heads are
+split into H_kv groups of H / H_kv consecutive heads and every head of a group
+reads the same key/value head, so query head h reads key/value head
+h // (H / H_kv).  H_kv = H is ordinary multi-head attention and H_kv = 1 is
+multi-query attention.  The gradient of a shared key/value head is the sum of
+the per-head gradients over its group.
+
 Backward (the chain rule applied to the definition above; the pages state only
 that S and P are recomputed):
 
@@ -185,11 +193,20 @@ def _bm_for(block_mask, b, h):
     return bm if bm.ndim == 2 else bm[b, h]
 
 
+def _group(q, k):
+    """Query heads per key/value head (H / H_kv)."""
+    H, H_kv = np.shape(q)[1], np.shape(k)[1]
+    if H_kv < 1 or H % H_kv:
+        raise ValueError(f"key/value heads ({H_kv}) must divide query heads ({H})")
+    return H // H_kv
+
+
 def _head(q, k, v, b, h, scale, causal, key_lens, block_mask, dropout_p,
           seed, offset):
     H = q.shape[1]
+    hk = h // _group(q, k)
     kl = None if key_lens is None else int(np.asarray(key_lens)[b])
-    return _Head(q[b, h], k[b, h], v[b, h], scale, causal, kl,
+    return _Head(q[b, h], k[b, hk], v[b, hk], scale, causal, kl,
                  _bm_for(block_mask, b, h), dropout_p, seed, offset, b * H + h)
 
 
@@ -207,25 +224,28 @@ def forward_rows(q, k, v, b, h, rows, scale, causal=False, key_lens=None,
     return O, L
 
 
-def backward_keys(q, k, v, do, b, h, keys, scale, causal=False, key_lens=None,
+def backward_keys(q, k, v, do, b, hk, keys, scale, causal=False, key_lens=None,
                   block_mask=None, dropout_p=0.0, seed=0, offset=0):
-    """dK[b, h, keys] and dV[b, h, keys] for sampled keys of one head.
+    """dK[b, hk, keys] and dV[b, hk, keys] for sampled keys of key/value head hk.
 
-    Only query rows that may attend at least one of `keys` contribute, so
-    only those rows are evaluated (each over its full score row).
+    The query heads of hk's group all contribute.  Only query rows that may
+    attend at least one of `keys` contribute, so only those rows are
+    evaluated (each over its full score row).
     """
-    hd = _head(q, k, v, b, h, scale, causal, key_lens, block_mask, dropout_p,
-               seed, offset)
+    g = _group(q, k)
     keys = np.asarray(keys, dtype=np.int64)
-    A = allowed_mask(np.arange(hd.N), keys, hd.causal, hd.key_len, hd.block_mask)
-    rows = np.nonzero(A.any(axis=1))[0]
-    dK = np.zeros_like(hd.k)
-    dV = np.zeros_like(hd.v)
-    dob = np.asarray(do[b, h], dtype=np.float64)
-    for r in _chunks(rows):
-        _, _, _, dk, dv = hd.backward(r, dob[r])
-        dK += dk
-        dV += dv
+    dK = np.zeros(np.shape(k)[2:])
+    dV = np.zeros(np.shape(v)[2:])
+    for h in range(hk * g, (hk + 1) * g):
+        hd = _head(q, k, v, b, h, scale, causal, key_lens, block_mask, dropout_p,
+                   seed, offset)
+        A = allowed_mask(np.arange(hd.N), keys, hd.causal, hd.key_len, hd.block_mask)
+        rows = np.nonzero(A.any(axis=1))[0]
+        dob = np.asarray(do[b, h], dtype=np.float64)
+        for r in _chunks(rows):
+            _, _, _, dk, dv = hd.backward(r, dob[r])
+            dK += dk
+            dV += dv
     return dK[keys], dV[keys]
 
 
@@ -241,7 +261,8 @@ def backward_rows(q, k, v, do, b, h, rows, scale, causal=False, key_lens=None,
 
 def attention_forward(q, k, v, scale, causal=False, key_lens=None,
                       block_mask=None, dropout_p=0.0, seed=0, offset=0):
-    """Full forward.  q, k, v: [B, H, N, d].  Returns O [B,H,N,d], L [B,H,N] (fp64).
+    """Full forward.  q: [B, H, N, d]; k, v: [B, H_kv, N, d] with H_kv dividing H.
+    Returns O [B,H,N,d], L [B,H,N] (fp64).
 
     block_mask: None, [nb, nb] shared by every (b, h), or [B, H, nb, nb].
     key_lens: None or [B] integers.
@@ -260,13 +281,15 @@ def attention_forward(q, k, v, scale, causal=False, key_lens=None,
 
 def attention_backward(q, k, v, do, scale, causal=False, key_lens=None,
                        block_mask=None, dropout_p=0.0, seed=0, offset=0):
-    """Full forward + backward.  Returns (O, L, dQ, dK, dV) in fp64."""
+    """Full forward + backward.  Returns (O, L, dQ, dK, dV) in fp64; dK and dV
+    have the key/value heads of k and v."""
     B, H, N, d = np.shape(q)
+    g = _group(q, k)
     O = np.zeros((B, H, N, d))
     L = np.zeros((B, H, N))
     dQ = np.zeros((B, H, N, d))
-    dK = np.zeros((B, H, N, d))
-    dV = np.zeros((B, H, N, d))
+    dK = np.zeros(np.shape(k))
+    dV = np.zeros(np.shape(v))
     for b in range(B):
         for h in range(H):
             hd = _head(q, k, v, b, h, scale, causal, key_lens, block_mask,
@@ -275,6 +298,6 @@ def attention_backward(q, k, v, do, scale, causal=False, key_lens=None,
             for r in _chunks(np.arange(N)):
                 o, l, dq, dk, dv = hd.backward(r, dob[r])
                 O[b, h, r], L[b, h, r], dQ[b, h, r] = o, l, dq
-                dK[b, h] += dk
-                dV[b, h] += dv
+                dK[b, h // g] += dk
+                dV[b, h // g] += dv
     return O, L, dQ, dK, dV

@@ -441,3 +441,105 @@ def test_philox_output_bits_are_balanced():
     x = words[0][1:] ^ words[0][:-1]
     flips = np.unpackbits(x.view(np.uint8)).mean()
     assert abs(flips - 0.5) < 0.01
+
+
+# ------------------------------------------------------ grouped-query heads --
+# "3.3 Hiểu sâu cơ chế Self-Attention", §9.2-9.3: groups of query heads share
+# one key/value head; one group per head is MHA, a single group is MQA.
+
+def _rand4(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def test_mqa_equals_every_head_attending_the_same_keys():
+    # one key/value head: each query head is an ordinary single-head problem
+    # against that head, computed here head by head through the MHA path
+    B, H, N, d = 2, 3, 9, 4
+    q = _rand4((B, H, N, d), 1)
+    k, v, do = _rand4((B, 1, N, d), 2), _rand4((B, 1, N, d), 3), _rand4((B, H, N, d), 4)
+    kw = dict(scale=0.6, causal=True, key_lens=[9, 5], dropout_p=0.2, seed=5, offset=1)
+    O, L, dQ, dK, dV = A.attention_backward(q, k, v, do, **kw)
+    dK_sum, dV_sum = np.zeros_like(k), np.zeros_like(v)
+    for h in range(H):
+        # the dropout counter uses the query head's b*H+h: run the single head
+        # inside an H-head problem whose other heads are ignored
+        qh = np.zeros_like(q)
+        qh[:, h] = q[:, h]
+        doh = np.zeros_like(do)
+        doh[:, h] = do[:, h]
+        kh, vh = np.repeat(k, H, axis=1), np.repeat(v, H, axis=1)
+        o, l, dq, dk, dv = A.attention_backward(qh, kh, vh, doh, **kw)
+        np.testing.assert_allclose(O[:, h], o[:, h], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(L[:, h], l[:, h], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(dQ[:, h], dq[:, h], rtol=1e-12, atol=1e-12)
+        dK_sum[:, 0] += dk[:, h]
+        dV_sum[:, 0] += dv[:, h]
+    np.testing.assert_allclose(dK, dK_sum, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dV, dV_sum, rtol=1e-11, atol=1e-12)
+
+
+def test_gqa_reads_key_value_head_of_its_consecutive_group():
+    # H = 6 query heads over H_kv = 2 key/value heads: heads 0-2 read kv head
+    # 0, heads 3-5 kv head 1, i.e. the MHA result on K, V with each key/value
+    # head repeated for its three query heads
+    B, H, Hk, N, d = 1, 6, 2, 11, 3
+    q, do = _rand4((B, H, N, d), 11), _rand4((B, H, N, d), 12)
+    k, v = _rand4((B, Hk, N, d), 13), _rand4((B, Hk, N, d), 14)
+    kw = dict(scale=0.5, causal=False, key_lens=[8])
+    O, L, dQ, dK, dV = A.attention_backward(q, k, v, do, **kw)
+    ke, ve = np.repeat(k, H // Hk, axis=1), np.repeat(v, H // Hk, axis=1)
+    Oe, Le, dQe, dKe, dVe = A.attention_backward(q, ke, ve, do, **kw)
+    np.testing.assert_allclose(O, Oe, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(L, Le, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dQ, dQe, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dK, dKe.reshape(B, Hk, H // Hk, N, d).sum(axis=2),
+                               rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dV, dVe.reshape(B, Hk, H // Hk, N, d).sum(axis=2),
+                               rtol=1e-11, atol=1e-12)
+
+
+def test_gqa_gradients_match_finite_differences():
+    # the shared key/value heads' gradients, including the group sum, against
+    # central differences of sum(O * dO)
+    B, H, Hk, N, d = 1, 4, 2, 5, 2
+    q, do = _rand4((B, H, N, d), 21), _rand4((B, H, N, d), 22)
+    k, v = _rand4((B, Hk, N, d), 23), _rand4((B, Hk, N, d), 24)
+    kw = dict(scale=0.8, causal=True, dropout_p=0.25, seed=3, offset=2)
+    _, _, dQ, dK, dV = A.attention_backward(q, k, v, do, **kw)
+
+    def f(qq, kk, vv):
+        return float((A.attention_forward(qq, kk, vv, **kw)[0] * do).sum())
+
+    eps = 1e-6
+    for name, X, G in (("q", q, dQ), ("k", k, dK), ("v", v, dV)):
+        num = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            args = {"q": q.copy(), "k": k.copy(), "v": v.copy()}
+            args[name][idx] += eps
+            fp = f(args["q"], args["k"], args["v"])
+            args[name][idx] -= 2 * eps
+            fm = f(args["q"], args["k"], args["v"])
+            num[idx] = (fp - fm) / (2 * eps)
+        err = np.linalg.norm(num - G) / max(np.linalg.norm(G), 1e-30)
+        assert err < 1e-6, (name, err)
+
+
+def test_gqa_backward_keys_sums_the_group():
+    B, H, Hk, N, d = 2, 4, 2, 7, 3
+    q, do = _rand4((B, H, N, d), 31), _rand4((B, H, N, d), 32)
+    k, v = _rand4((B, Hk, N, d), 33), _rand4((B, Hk, N, d), 34)
+    kw = dict(scale=0.4, causal=True, key_lens=[7, 6], dropout_p=0.1, seed=1)
+    _, _, _, dK, dV = A.attention_backward(q, k, v, do, **kw)
+    keys = np.array([0, 3, 6])
+    for b in range(B):
+        for hk in range(Hk):
+            dk, dv = A.backward_keys(q, k, v, do, b, hk, keys, **kw)
+            np.testing.assert_allclose(dk, dK[b, hk, keys], rtol=1e-11, atol=1e-12)
+            np.testing.assert_allclose(dv, dV[b, hk, keys], rtol=1e-11, atol=1e-12)
+
+
+def test_key_value_heads_must_divide_query_heads():
+    q = np.zeros((1, 3, 4, 2))
+    k = np.zeros((1, 2, 4, 2))
+    with pytest.raises(ValueError):
+        A.attention_forward(q, k, k, scale=1.0)
