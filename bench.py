@@ -147,14 +147,15 @@ class Step:
         self.q, self.k, self.v, self.do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
         self.key_lens = None if inp["key_lens"] is None else inp["key_lens"].to(dev)
         self.block_mask = None if inp["block_mask"] is None else inp["block_mask"].to(dev)
-        self.p = ea.make_params(self.q, scale=inp["scale"], causal=inp["causal"],
+        self.p = ea.make_params(self.q, k=self.k, scale=inp["scale"], causal=inp["causal"],
                                 key_lens=self.key_lens, dropout_p=inp["dropout_p"],
                                 seed=inp["seed"], offset=inp["offset"],
                                 block_mask=self.block_mask)
         B, H, N, d = self.q.shape
         self.o = torch.empty_like(self.q)
         self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        self.dq = torch.empty_like(self.q)
+        self.dk, self.dv = torch.empty_like(self.k), torch.empty_like(self.k)
         nbytes = max(ea.workspace_size(self.p, True), ea.workspace_size(self.p, False))
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
         self.launches = 1 + 3 + (2 if self.block_mask is not None else 0)
@@ -259,9 +260,13 @@ def measure_e2e(ea, w, dev, steps, warmup):
     kw = dict(scale=inp["scale"], causal=inp["causal"], key_lens=kl, dropout_p=inp["dropout_p"],
               seed=inp["seed"], offset=inp["offset"], block_mask=bm)
     shape, dtype = inp["q"].shape, inp["q"].dtype
-    dev_in = [{n: torch.empty(shape, dtype=dtype, device=dev) for n in names} for _ in range(2)]
-    dev_out = [[torch.empty(shape, dtype=dtype, device=dev) for _ in range(3)] for _ in range(2)]
-    host_out = [[torch.empty(shape, dtype=dtype).pin_memory() for _ in range(3)] for _ in range(2)]
+    shapes = {n: inp[n].shape for n in names}
+    out_shapes = (inp["q"].shape, inp["k"].shape, inp["v"].shape)   # dQ, dK, dV
+    dev_in = [{n: torch.empty(shapes[n], dtype=dtype, device=dev) for n in names}
+              for _ in range(2)]
+    dev_out = [[torch.empty(sh, dtype=dtype, device=dev) for sh in out_shapes] for _ in range(2)]
+    host_out = [[torch.empty(sh, dtype=dtype).pin_memory() for sh in out_shapes]
+                for _ in range(2)]
     up, comp, down = (torch.cuda.Stream(dev) for _ in range(3))
     ev_in = [torch.cuda.Event() for _ in range(2)]        # inputs of buffer set uploaded
     ev_used = [torch.cuda.Event() for _ in range(2)]      # compute done with buffer set
@@ -328,15 +333,18 @@ def oracle_sample(w, inp, budget_s, max_heads=None):
     heads = [(b, h) for b in range(w.B) for h in range(w.H)]
     done, flops = 0, 0.0
     t0 = time.perf_counter()
+    grp = w.H // w.kv_heads
     for b, h in heads:
         sl = (slice(b, b + 1), slice(h, h + 1))
-        qs, ks, vs, dos = (x[sl].double().numpy() for x in (q, k, v, do))
+        skv = (slice(b, b + 1), slice(h // grp, h // grp + 1))   # the head's key/value head
+        qs, dos = (x[sl].double().numpy() for x in (q, do))
+        ks, vs = (x[skv].double().numpy() for x in (k, v))
         kws = dict(kw)
         if kl is not None:
             kws["key_lens"] = np.asarray(kw["key_lens"])[b:b + 1]
         oracle.attention_backward(qs, ks, vs, dos, **kws)
         done += 1
-        wh = workloads.get(w.name, B=1, H=1)
+        wh = workloads.get(w.name, B=1, H=1, H_kv=1)
         flops += 3.5 * fwd_flops(wh, None if kl is None else kl[b:b + 1],
                                  None if bm is None else bm)
         if time.perf_counter() - t0 > budget_s or (max_heads and done >= max_heads):
@@ -372,7 +380,8 @@ def run_reference(args, w):
 
 
 def describe(w):
-    parts = [f"{w.name}: B={w.B} H={w.H} N={w.N} d={w.d} {w.dtype}"]
+    heads = f"H={w.H}" if w.kv_heads == w.H else f"H={w.H} H_kv={w.kv_heads}"
+    parts = [f"{w.name}: B={w.B} {heads} N={w.N} d={w.d} {w.dtype}"]
     parts.append("causal" if w.causal else "non-causal")
     if w.key_len_range:
         parts.append(f"key lengths U{{{w.key_len_range[0]}..{w.key_len_range[1]}}}")

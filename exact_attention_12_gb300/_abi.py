@@ -47,6 +47,9 @@ class AttnParams(ctypes.Structure):
         ("block_mask_head_stride", ctypes.c_int64),
         ("stride_b", ctypes.c_int64), ("stride_h", ctypes.c_int64),
         ("stride_n", ctypes.c_int64),
+        ("H_kv", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("kv_stride_b", ctypes.c_int64), ("kv_stride_h", ctypes.c_int64),
+        ("kv_stride_n", ctypes.c_int64),
     ]
 
 

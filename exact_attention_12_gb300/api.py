@@ -37,9 +37,10 @@ def _stream(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
-def make_params(q, *, scale=None, causal=False, key_lens=None, dropout_p=0.0, seed=0,
+def make_params(q, *, k=None, scale=None, causal=False, key_lens=None, dropout_p=0.0, seed=0,
                 offset=0, block_mask=None):
-    """Fill `attn_params` from the query tensor and the options."""
+    """Fill `attn_params` from the query tensor, the key tensor (for its head
+    count and strides; None = laid out like q) and the options."""
     if q.dim() != 4:
         raise ValueError("tensors must be [B, H, N, d]")
     B, H, N, d = q.shape
@@ -57,6 +58,13 @@ def make_params(q, *, scale=None, causal=False, key_lens=None, dropout_p=0.0, se
     if sd != 1 and d > 1:
         raise ValueError("the head dimension must be contiguous")
     p.stride_b, p.stride_h, p.stride_n = sb, sh, sn
+    if k is not None:
+        if k.dim() != 4 or k.shape[0] != B or k.shape[2:] != q.shape[2:]:
+            raise ValueError("k must be [B, H_kv, N, d] like q")
+        if k.stride(3) != 1 and d > 1:
+            raise ValueError("the head dimension must be contiguous")
+        p.H_kv = k.shape[1]
+        p.kv_stride_b, p.kv_stride_h, p.kv_stride_n = k.stride()[:3]
     if key_lens is not None:
         if key_lens.dtype != torch.int32 or key_lens.device != q.device or key_lens.numel() != B:
             raise ValueError("key_lens must be an int32 tensor [B] on the tensors' device")
@@ -81,7 +89,16 @@ def _same_layout(ref, *ts):
     for t in ts:
         if t.shape != ref.shape or t.stride() != ref.stride() or t.device != ref.device \
                 or t.dtype != ref.dtype:
-            raise ValueError("all attention tensors must share shape, strides, dtype and device")
+            raise ValueError("tensors of one role must share shape, strides, dtype and device")
+
+
+def _check_kv(q, k):
+    if k.device != q.device or k.dtype != q.dtype:
+        raise ValueError("k, v must have q's dtype and device")
+    H, H_kv = q.shape[1], k.shape[1] if k.dim() == 4 else -1
+    divides = H_kv == 0 if H == 0 else (H_kv >= 1 and H % H_kv == 0)
+    if k.dim() != 4 or k.shape[0] != q.shape[0] or k.shape[2:] != q.shape[2:] or not divides:
+        raise ValueError("k, v must be [B, H_kv, N, d] with H_kv dividing q's H")
 
 
 def _like(t):
@@ -99,12 +116,14 @@ def attention_fwd(q, k, v, *, scale=None, causal=False, key_lens=None, dropout_p
                   offset=0, block_mask=None, out=None, lse=None, ws=None):
     """O and the per-row logsumexp L of exact attention (see include/attn.h).
 
-    q, k, v: [B, H, N, d] CUDA tensors (bf16 or fp32) with identical strides.
-    Returns (o, lse) with o like q and lse fp32 [B, H, N].
+    q: [B, H, N, d]; k, v: [B, H_kv, N, d] with H_kv dividing H (grouped-query
+    attention; H_kv = H is multi-head), CUDA tensors (bf16 or fp32); k and v
+    share strides.  Returns (o, lse) with o like q and lse fp32 [B, H, N].
     """
-    _same_layout(q, k, v)
-    p = make_params(q, scale=scale, causal=causal, key_lens=key_lens, dropout_p=dropout_p,
-                    seed=seed, offset=offset, block_mask=block_mask)
+    _check_kv(q, k)
+    _same_layout(k, v)
+    p = make_params(q, k=k, scale=scale, causal=causal, key_lens=key_lens,
+                    dropout_p=dropout_p, seed=seed, offset=offset, block_mask=block_mask)
     o = _like(q) if out is None else out
     _same_layout(q, o)
     B, H, N, _ = q.shape
@@ -121,14 +140,21 @@ def attention_fwd(q, k, v, *, scale=None, causal=False, key_lens=None, dropout_p
 def attention_bwd(dout, q, k, v, o, lse, *, scale=None, causal=False, key_lens=None,
                   dropout_p=0.0, seed=0, offset=0, block_mask=None, dq=None, dk=None, dv=None,
                   ws=None):
-    """dQ, dK, dV of exact attention given the forward's o and lse (bf16)."""
-    _same_layout(q, k, v, o, dout)
-    p = make_params(q, scale=scale, causal=causal, key_lens=key_lens, dropout_p=dropout_p,
-                    seed=seed, offset=offset, block_mask=block_mask)
+    """dQ, dK, dV of exact attention given the forward's o and lse (bf16).
+
+    dq is like q; dk, dv are like k ([B, H_kv, N, d]; a shared key/value
+    head's gradient sums over its group of query heads).
+    """
+    _check_kv(q, k)
+    _same_layout(q, o, dout)
+    _same_layout(k, v)
+    p = make_params(q, k=k, scale=scale, causal=causal, key_lens=key_lens,
+                    dropout_p=dropout_p, seed=seed, offset=offset, block_mask=block_mask)
     dq = _like(q) if dq is None else dq
-    dk = _like(q) if dk is None else dk
-    dv = _like(q) if dv is None else dv
-    _same_layout(q, dq, dk, dv)
+    dk = _like(k) if dk is None else dk
+    dv = _like(k) if dv is None else dv
+    _same_layout(q, dq)
+    _same_layout(k, dk, dv)
     w = workspace(q.device, workspace_size(p, True)) if ws is None else ws
     st = lib().attn_bwd(ctypes.byref(p), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                         lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),

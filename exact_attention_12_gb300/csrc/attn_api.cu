@@ -74,10 +74,31 @@ WsLayout layout(const attn_params* p, bool bwd) {
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+// Key/value heads (H_kv = 0 means H) and the key/value strides (all zero
+// means the query strides).
+int kv_heads(const attn_params* p) { return p->H_kv == 0 ? p->H : p->H_kv; }
+
+bool kv_strides_given(const attn_params* p) {
+  return p->kv_stride_b != 0 || p->kv_stride_h != 0 || p->kv_stride_n != 0;
+}
+
+void kv_strides(const attn_params* p, int64_t* sb, int64_t* sh, int64_t* sn) {
+  const bool own = kv_strides_given(p);
+  *sb = own ? p->kv_stride_b : p->stride_b;
+  *sh = own ? p->kv_stride_h : p->stride_h;
+  *sn = own ? p->kv_stride_n : p->stride_n;
+}
+
 attn_status validate(const attn_params* p, bool bwd) {
   if (p == nullptr) return fail(ATTN_ERR_INVALID_ARG, "params is NULL");
   if (p->B < 0 || p->H < 0 || p->N < 0)
     return fail(ATTN_ERR_INVALID_ARG, "negative shape B=%d H=%d N=%d", p->B, p->H, p->N);
+  if (p->reserved != 0) return fail(ATTN_ERR_INVALID_ARG, "reserved field must be 0");
+  if (p->H_kv < 0 || (p->H > 0 && (kv_heads(p) < 1 || p->H % kv_heads(p) != 0)))
+    return fail(ATTN_ERR_INVALID_ARG, "H_kv=%d must divide H=%d", p->H_kv, p->H);
+  if (!kv_strides_given(p) && kv_heads(p) != p->H)
+    return fail(ATTN_ERR_INVALID_ARG, "H_kv=%d != H=%d needs the key/value strides", p->H_kv,
+                p->H);
   if (p->d != 64 && p->d != 128)
     return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", p->d);
   if (p->dtype != ATTN_BF16 && p->dtype != ATTN_FP32)
@@ -110,6 +131,17 @@ attn_status validate(const attn_params* p, bool bwd) {
                   static_cast<long long>(p->stride_h), static_cast<long long>(p->stride_n));
   }
   if (p->stride_n < p->d) return fail(ATTN_ERR_INVALID_ARG, "stride_n < d");
+  int64_t kst[3];
+  kv_strides(p, &kst[0], &kst[1], &kst[2]);
+  for (int i = 0; i < 3; ++i) {
+    if (kst[i] <= 0 || kst[i] % align != 0)
+      return fail(ATTN_ERR_INVALID_ARG,
+                  "key/value strides must be positive multiples of %lld elements "
+                  "(b=%lld h=%lld n=%lld)",
+                  static_cast<long long>(align), static_cast<long long>(kst[0]),
+                  static_cast<long long>(kst[1]), static_cast<long long>(kst[2]));
+  }
+  if (kst[2] < p->d) return fail(ATTN_ERR_INVALID_ARG, "kv_stride_n < d");
   return ATTN_OK;
 }
 
@@ -179,11 +211,21 @@ attn_status make_bf16_map(CUtensorMap* map, const void* ptr, const attn_params* 
                   p->stride_b, p->stride_h, p->stride_n, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// k or v: [B, H_kv, N, d] with the key/value strides
+attn_status make_kv_map(CUtensorMap* map, const void* ptr, const attn_params* p) {
+  int64_t sb, sh, sn;
+  kv_strides(p, &sb, &sh, &sn);
+  return make_map(map, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->B, kv_heads(p), p->N, p->d,
+                  sb, sh, sn, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 attn::MaskArgs mask_args(const attn_params* p, const WsLayout& L, char* ws, bool by_column) {
   attn::MaskArgs m{};
   m.B = p->B;
   m.H = p->H;
   m.N = p->N;
+  m.H_kv = kv_heads(p);
+  m.kv_group = m.H_kv > 0 ? p->H / m.H_kv : 1;
   m.causal = p->causal != 0;
   m.key_lens = p->key_lens;
   m.nb = (p->N + kTile - 1) / kTile;
@@ -214,13 +256,13 @@ attn::MaskArgs mask_args(const attn_params* p, const WsLayout& L, char* ws, bool
 
 bool empty_problem(const attn_params* p) { return p->B == 0 || p->H == 0 || p->N == 0; }
 
-// Heads per scheduling group: as many as keep `bytes_per_head` of re-read
-// operands within a share of the 129 MB L2.  Causal work is not grouped: its
-// tiles differ in length, and a group's long tiles starting late would leave
-// a tail; longest-first over all heads balances better.
-int head_group(const attn_params* p, double bytes_per_head) {
+// Heads per scheduling group, out of `bh` (b, head) units: as many as keep
+// `bytes_per_head` of re-read operands within a share of the 129 MB L2.
+// Causal work is not grouped: its tiles differ in length, and a group's long
+// tiles starting late would leave a tail; longest-first over all heads
+// balances better.
+int head_group(const attn_params* p, int bh, double bytes_per_head) {
   const double budget = 48.0 * 1024 * 1024;
-  const int bh = p->B * p->H;
   if (p->causal) return bh > 0 ? bh : 1;
   const int g = static_cast<int>(budget / (bytes_per_head > 1.0 ? bytes_per_head : 1.0));
   return g < 1 ? 1 : (g > bh ? bh : g);
@@ -254,7 +296,7 @@ attn_status attn_fwd(const attn_params* p, const void* q, const void* k, const v
 
   attn::FwdArgs a{};
   a.m = mask_args(p, L, w, false);
-  a.m.head_group = head_group(p, 4.0 * p->N * p->d);   // K and V, bf16
+  a.m.head_group = head_group(p, p->B * p->H, 4.0 * p->N * p->d);   // K and V, bf16
   a.d = p->d;
   a.scale = p->scale;
   a.scale_log2 = p->scale * kLog2e;
@@ -263,6 +305,7 @@ attn_status attn_fwd(const attn_params* p, const void* q, const void* k, const v
   a.stride_b = p->stride_b;
   a.stride_h = p->stride_h;
   a.stride_n = p->stride_n;
+  kv_strides(p, &a.kv_stride_b, &a.kv_stride_h, &a.kv_stride_n);
   a.status = reinterpret_cast<int*>(w);
   a.sched = reinterpret_cast<int*>(w + kSchedOffset);
   a.timeout_ns = kTimeoutNs;
@@ -275,8 +318,8 @@ attn_status attn_fwd(const attn_params* p, const void* q, const void* k, const v
   }
   attn::TensorMaps tm{};
   if ((st = make_bf16_map(&tm.q, q, p)) != ATTN_OK) return st;
-  if ((st = make_bf16_map(&tm.k, k, p)) != ATTN_OK) return st;
-  if ((st = make_bf16_map(&tm.v, v, p)) != ATTN_OK) return st;
+  if ((st = make_kv_map(&tm.k, k, p)) != ATTN_OK) return st;
+  if ((st = make_kv_map(&tm.v, v, p)) != ATTN_OK) return st;
   if (p->block_mask != nullptr) {
     e = attn::launch_compact_mask(p->block_mask, p->block_mask_head_stride, num_masks(p), a.m.nb,
                                   0, reinterpret_cast<int32_t*>(w + L.list_cnt),
@@ -301,7 +344,9 @@ attn_status bwd_setup(const attn_params* p, void* ws, size_t ws_bytes, attn::Bwd
   *L = layout(p, true);
   *a = attn::BwdArgs{};
   a->m = mask_args(p, *L, w, true);
-  a->m.head_group = head_group(p, 8.0 * p->N * p->d);   // Q, dO bf16 + dQ accumulator fp32
+  // a key/value head's CTAs re-read the Q, dO (bf16) and dQ accumulator (fp32)
+  // of its group's query heads
+  a->m.head_group = head_group(p, p->B * kv_heads(p), 8.0 * a->m.kv_group * p->N * p->d);
   a->d = p->d;
   a->scale = p->scale;
   a->scale_log2 = p->scale * kLog2e;
@@ -312,6 +357,7 @@ attn_status bwd_setup(const attn_params* p, void* ws, size_t ws_bytes, attn::Bwd
   a->stride_b = p->stride_b;
   a->stride_h = p->stride_h;
   a->stride_n = p->stride_n;
+  kv_strides(p, &a->kv_stride_b, &a->kv_stride_h, &a->kv_stride_n);
   a->status = reinterpret_cast<int*>(w);
   a->timeout_ns = kTimeoutNs;
   return ATTN_OK;
@@ -349,8 +395,8 @@ attn_status attn_bwd_main(const attn_params* p, const void* q, const void* k, co
   a.dv = dv;
   attn::TensorMaps tm{};
   if ((st = make_bf16_map(&tm.q, q, p)) != ATTN_OK) return st;
-  if ((st = make_bf16_map(&tm.k, k, p)) != ATTN_OK) return st;
-  if ((st = make_bf16_map(&tm.v, v, p)) != ATTN_OK) return st;
+  if ((st = make_kv_map(&tm.k, k, p)) != ATTN_OK) return st;
+  if ((st = make_kv_map(&tm.v, v, p)) != ATTN_OK) return st;
   if ((st = make_bf16_map(&tm.dout, dout, p)) != ATTN_OK) return st;
   // fp32 dQ accumulator: contiguous [B, H, N, d]; 32 x 32 boxes, 128-byte swizzle
   const int64_t d64 = p->d;

@@ -11,9 +11,11 @@
 //   bwd_preprocess   D = rowsum(dO * O) per query row; zeroes the fp32 dQ
 //                    accumulator.  Memory-bound.
 //   bwd_kernel       one CTA per 128-row key/value tile K_j, V_j of one
-//                    (b, h); loops over the query tiles Q_i that may attend
-//                    it (all, the causal suffix i >= j, or the block mask's
-//                    column list).  Per query tile, five MMAs:
+//                    (b, key/value head); loops over the query heads that
+//                    share it (one, or a group of H / H_kv) and for each over
+//                    the query tiles Q_i that may attend it (all, the causal
+//                    suffix i >= j, or the block mask's column list), so the
+//                    group's dK, dV sum in TMEM.  Per query tile, five MMAs:
 //                      S^T  = K_j Q_i^T      (TMEM)
 //                      dP^T = V_j dO_i^T     (TMEM)
 //                      dV  += P~^T dO_i      (A = P~^T in TMEM, bf16)
@@ -130,6 +132,27 @@ __device__ __forceinline__ int key_limit(const MaskArgs& m, int b) {
   return limit;
 }
 
+// The (query head, query tile) pairs a key tile of key/value head hk visits:
+// the query heads h0 .. h0 + g - 1 of its group in order, each with its own
+// query-tile list (the block mask may differ per head).
+struct QHeadWalk {
+  const MaskArgs* m;
+  int kt, b, h0, g, limit;
+  int qh = -1;
+  QList list{nullptr, 0, 0};
+  int i = 0;
+  __device__ __forceinline__ bool next(int& h, int& qtile) {
+    while (qh < 0 || i >= list.n) {
+      if (++qh >= g) return false;
+      list = bwd_tiles(*m, kt, b * m->H + h0 + qh, limit);
+      i = 0;
+    }
+    h = h0 + qh;
+    qtile = list[i++];
+    return true;
+  }
+};
+
 // 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled tile of 128-byte rows.
 __device__ __forceinline__ uint32_t swz(int r, int c) {
   return r * 128 + ((c ^ (r & 7)) << 4);
@@ -216,24 +239,27 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const MaskArgs& m = a.m;
-  const int BH = m.B * m.H;
-  // head groups of G consecutive (b, h); within a group, key tiles in
-  // ascending order (heaviest first for causal)
-  int kt, bh;
+  const int BHk = m.B * m.H_kv;
+  // one CTA per (b, key/value head hk, key tile); head groups of G
+  // consecutive (b, hk); within a group, key tiles in ascending order
+  // (heaviest first for causal)
+  int kt, bhk;
   {
-    const int G = m.head_group, per = G * m.nb, nfull = BH / G;
+    const int G = m.head_group, per = G * m.nb, nfull = BHk / G;
     const int w = static_cast<int>(blockIdx.x);
     const int g = w < nfull * per ? w / per : nfull;
-    const int gs = g < nfull ? G : BH - nfull * G;
+    const int gs = g < nfull ? G : BHk - nfull * G;
     const int rem = w - g * per;
     kt = rem / gs;
-    bh = g * G + rem % gs;
+    bhk = g * G + rem % gs;
   }
-  const int b = bh / m.H, h = bh - b * m.H;
+  const int b = bhk / m.H_kv, hk = bhk - b * m.H_kv;
   const int k0 = kt * kTile;
   const int limit = key_limit(m, b);
-  const QList tiles = bwd_tiles(m, kt, bh, limit);
-  const int n = tiles.n;
+  const QHeadWalk walk0{&m, kt, b, hk * m.kv_group, m.kv_group, limit};
+  int n = 0;   // (query head, query tile) pairs of this key tile
+  for (int qh = 0; qh < m.kv_group; ++qh)
+    n += bwd_tiles(m, kt, b * m.H + hk * m.kv_group + qh, limit).n;
 
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
@@ -277,13 +303,16 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive_expect_tx(&ctl.kvfull, 2 * C::kTileBytes);
 #pragma unroll
         for (int x = 0; x < C::kBoxes; ++x) {
-          tma_load_4d(sK + x * C::kBoxBytes, &tk, &ctl.kvfull, x * 64, k0, h, b);
-          tma_load_4d(sV + x * C::kBoxBytes, &tv, &ctl.kvfull, x * 64, k0, h, b);
+          tma_load_4d(sK + x * C::kBoxBytes, &tk, &ctl.kvfull, x * 64, k0, hk, b);
+          tma_load_4d(sV + x * C::kBoxBytes, &tv, &ctl.kvfull, x * 64, k0, hk, b);
         }
         int iq = 0, id = 0;   // Q / dO tiles issued
         bool ok = true;
-        for (int i = 0; ok && i < n; ++i) {
-          const int q0 = tiles[i] * kTile;
+        QHeadWalk walk = walk0;
+        int h, qtile;
+        for (int i = 0; ok && walk.next(h, qtile); ++i) {
+          const int q0 = qtile * kTile;
+          const int bh = b * m.H + h;
           const int sq = i % QS;
           if (i >= QS && !(ok = mbar_wait(&ctl.qempty[sq], ((i / QS) - 1) & 1, wc, kSiteBwdEmpty)))
             break;
@@ -410,10 +439,13 @@ __global__ void __launch_bounds__(384, 1)
     uint8_t* region = sDS + half * C::kBoxBytes + quarter * 4096;
     uint8_t* stage = sStage + warp * 4096;
     bool ok = true;
-    for (int i = 0; i < n; ++i) {
+    QHeadWalk walk = walk0;
+    int h = 0, qtile = 0;
+    int prev_h = 0, prev_q0 = 0;   // the pair whose dQ is drained next
+    for (int i = 0; i < n && walk.next(h, qtile); ++i) {
       const uint32_t ph = i & 1;
-      const int qtile = tiles[i];
       const int q0 = qtile * kTile;
+      const int bh = b * m.H + h;
       // -L (log2 units) and -D of this warp's 64 query rows, staged by the producer
       const float* nLw = sLD + (i % QS) * 2 * kTile + qc0;
       const float* nDw = nLw + kTile;
@@ -487,8 +519,10 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         tc_fence_after();
         drain_dq<D>(tl + C::kDQCol + half * C::kHalf, stage, region, &tdq, &ctl.dqfree,
-                    tiles[i - 1] * kTile + quarter * 32, half * C::kHalf, h, b, lane);
+                    prev_q0 + quarter * 32, half * C::kHalf, prev_h, b, lane);
       }
+      prev_h = h;
+      prev_q0 = q0;
 
       // dS^T = P * (dP~ * Z/(1-p) - D)
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dpfull, ph, wc, kSiteBwdSoft));
@@ -542,7 +576,7 @@ __global__ void __launch_bounds__(384, 1)
       if (ok) {
         tc_fence_after();
         drain_dq<D>(tl + C::kDQCol + half * C::kHalf, stage, region, &tdq, &ctl.dqfree,
-                    tiles[n - 1] * kTile + quarter * 32, half * C::kHalf, h, b, lane);
+                    prev_q0 + quarter * 32, half * C::kHalf, prev_h, b, lane);
       }
     }
 
@@ -552,8 +586,8 @@ __global__ void __launch_bounds__(384, 1)
       if (ok) tc_fence_after();
     }
     if (ok) {
-      const int64_t row_off =
-          b * a.stride_b + h * a.stride_h + static_cast<int64_t>(kj) * a.stride_n + half * C::kHalf;
+      const int64_t row_off = b * a.kv_stride_b + hk * a.kv_stride_h +
+                              static_cast<int64_t>(kj) * a.kv_stride_n + half * C::kHalf;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(which ? a.dk : a.dv) + row_off;
@@ -678,7 +712,8 @@ cudaError_t launch_main(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s) 
     if (static_cast<uint32_t>(fa.numRegs) < C::kRegsLaunch) return cudaErrorInvalidConfiguration;
     attr_set = true;
   }
-  const unsigned grid = static_cast<unsigned>(a.m.nb) * a.m.B * a.m.H;
+  // one CTA per (b, key/value head, key tile)
+  const unsigned grid = static_cast<unsigned>(a.m.nb) * a.m.B * a.m.H_kv;
   bwd_bf16_kernel<D, DROP><<<grid, C::kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, tm.dout,
                                                                  tm.dq_acc, a);
   return cudaGetLastError();

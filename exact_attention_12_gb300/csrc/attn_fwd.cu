@@ -321,6 +321,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
                       (2 * u.pair + 1) * kTile, u.h, u.b);
         }
         ++kw;
+        const int hk = u.h / m.kv_group;   // the key/value head of query head h
         PairWalk walk{listA, listB};
         int j;
         bool na, nb;
@@ -334,11 +335,11 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
           mbar_arrive_expect_tx(&ctl.kfull[s], C::kTileBytes);
 #pragma unroll
           for (int x = 0; x < C::kBoxes; ++x)
-            tma_load_4d(dk + x * C::kBoxBytes, &tk, &ctl.kfull[s], x * 64, kv0, u.h, u.b);
+            tma_load_4d(dk + x * C::kBoxBytes, &tk, &ctl.kfull[s], x * 64, kv0, hk, u.b);
           mbar_arrive_expect_tx(&ctl.vfull[s], C::kTileBytes);
 #pragma unroll
           for (int x = 0; x < C::kBoxes; ++x)
-            tma_load_4d(dv + x * C::kBoxBytes, &tv, &ctl.vfull[s], x * 64, kv0, u.h, u.b);
+            tma_load_4d(dv + x * C::kBoxBytes, &tv, &ctl.vfull[s], x * 64, kv0, hk, u.b);
           ++t;
         }
       }

@@ -43,6 +43,8 @@ __global__ void __launch_bounds__(kRows) fwd_fp32_kernel(const float* __restrict
   const int t = threadIdx.x;
   const int qi = q0 + t;
   const int64_t head = b * a.stride_b + h * a.stride_h;
+  // the key/value head of query head h
+  const int64_t kv_head = b * a.kv_stride_b + (h / m.kv_group) * a.kv_stride_h;
   const float* qrow = sQ + t * (D + 1);
   float* srow = sS + t * (kKeys + 1);
 
@@ -69,7 +71,7 @@ __global__ void __launch_bounds__(kRows) fwd_fp32_kernel(const float* __restrict
     for (int e = t; e < kKeys * D; e += kRows) {
       const int r = e / D, c = e - r * D;
       const bool in = kv0 + r < m.N;
-      const int64_t g = head + static_cast<int64_t>(kv0 + r) * a.stride_n + c;
+      const int64_t g = kv_head + static_cast<int64_t>(kv0 + r) * a.kv_stride_n + c;
       sK[e] = in ? k[g] : 0.f;
       sV[e] = in ? v[g] : 0.f;
     }

@@ -27,6 +27,8 @@ constexpr int kStatusSmemAlign = 3;
 // Per-call mask/dropout settings common to every kernel.
 struct MaskArgs {
   int B, H, N;
+  int H_kv;                       // key/value heads (divides H)
+  int kv_group;                   // H / H_kv: query head h reads key/value head h / kv_group
   int causal;
   const int32_t* key_lens;        // [B] or null
   // block mask, compacted: for mask m and tile t, cnt[m * nb + t] sorted
@@ -55,7 +57,8 @@ struct FwdArgs {
   float scale_log2;               // c * log2(e)
   void* o;                        // [B,H,N,d]
   float* lse;                     // [B,H,N]
-  int64_t stride_b, stride_h, stride_n;
+  int64_t stride_b, stride_h, stride_n;            // q, o
+  int64_t kv_stride_b, kv_stride_h, kv_stride_n;   // k, v
   int* status;                    // workspace status words
   int* sched;                     // workspace scheduler words: next unit, CTAs finished
   uint64_t timeout_ns;
@@ -72,9 +75,10 @@ struct BwdArgs {
   float* dsum;                    // workspace [B*H][npad]: -rowsum(dO * O); 0 on padding
   int npad;                       // nb * 128
   float* dq_acc;                  // [B,H,N,d] fp32, zeroed by the preprocess
-  void* dk;
+  void* dk;                       // [B,H_kv,N,d]
   void* dv;
-  int64_t stride_b, stride_h, stride_n;
+  int64_t stride_b, stride_h, stride_n;            // q, o, dO, dQ
+  int64_t kv_stride_b, kv_stride_h, kv_stride_n;   // k, v, dK, dV
   int* status;
   uint64_t timeout_ns;
 };

@@ -97,7 +97,20 @@ typedef struct attn_params {
                                 NULL = dense.  bf16 only. */
   int64_t block_mask_head_stride; /* bytes between the masks of consecutive
                                 (b * H + h); 0 = one mask for all heads */
-  int64_t stride_b, stride_h, stride_n; /* element strides of the tensors */
+  int64_t stride_b, stride_h, stride_n; /* element strides of q, o, dout,
+                                dq (and of k, v, dk, dv when the kv_stride
+                                fields are 0) */
+  /* Grouped-query attention ("3.3 Hiểu sâu cơ chế Self-Attention", §9.2
+   * MQA and §9.3 GQA): the query heads are split into H_kv groups of H / H_kv
+   * consecutive heads that share one key/value head, so query head h reads
+   * key/value head h / (H / H_kv).  k, v, dk and dv are [B, H_kv, N, d]; dk
+   * and dv of a shared head are the sums over its group.  H_kv = H (or 0) is
+   * ordinary multi-head attention, H_kv = 1 multi-query attention. */
+  int32_t H_kv;              /* key/value heads, dividing H; 0 = H */
+  int32_t reserved;          /* must be 0 */
+  int64_t kv_stride_b, kv_stride_h, kv_stride_n; /* element strides of k, v,
+                                dk, dv; all three 0 = the strides above
+                                (then H_kv must equal H) */
 } attn_params;
 
 /* Bytes of device workspace a forward (for_backward = 0) or backward
@@ -111,7 +124,8 @@ attn_status attn_fwd(const attn_params* p, const void* q, const void* k,
                      size_t ws_bytes, void* stream);
 
 /* Backward (bf16): needs o and lse from attn_fwd with the same parameters
- * (dropout seed and offset included).  Writes dq, dk, dv [B,H,N,d] bf16. */
+ * (dropout seed and offset included).  Writes dq [B,H,N,d] and dk, dv
+ * [B,H_kv,N,d] bf16. */
 attn_status attn_bwd(const attn_params* p, const void* q, const void* k,
                      const void* v, const void* o, const float* lse,
                      const void* dout, void* dq, void* dk, void* dv, void* ws,

@@ -6,6 +6,7 @@ so none of these tests needs a device.
 
 import ctypes
 import os
+import subprocess
 import re
 
 import pytest
@@ -36,11 +37,23 @@ def test_library_exports_every_declared_function(abi):
     assert sorted(declared) == sorted(abi.EXPORTS), (declared, sorted(abi.EXPORTS))
 
 
-def test_params_struct_layout(abi):
+def test_params_struct_layout(abi, tmp_path):
+    # the ctypes mirror against the C compiler's layout of include/attn.h
     p = abi.AttnParams
-    assert ctypes.sizeof(p) == 96
-    assert p.philox_seed.offset == 32 and p.key_lens.offset == 48
-    assert p.stride_n.offset == 88
+    names = [f[0] for f in p._fields_]
+    src = tmp_path / "layout.c"
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "attn.h"', 'int main(void) {',
+             '  printf("size %zu\\n", sizeof(attn_params));']
+    lines += [f'  printf("{n} %zu\\n", offsetof(attn_params, {n}));' for n in names]
+    lines += ['  return 0;', '}']
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.check_call(["gcc", "-std=c11", "-I", inc, str(src), "-o", str(exe)])
+    got = dict(line.split() for line in subprocess.check_output([str(exe)], text=True).splitlines())
+    assert int(got["size"]) == ctypes.sizeof(p) == 128
+    for n in names:
+        assert int(got[n]) == getattr(p, n).offset, n
 
 
 def _params(abi, **kw):
@@ -58,6 +71,7 @@ def _params(abi, **kw):
     ("d", 96, 2), ("d", 32, 2), ("B", -1, 1), ("scale", 0.0, 1), ("scale", -1.0, 1),
     ("scale", float("inf"), 1), ("dropout_p", 1.0, 1), ("dropout_p", -0.1, 1),
     ("philox_offset", 1 << 32, 1), ("stride_n", 60, 1), ("stride_h", 0, 1), ("dtype", 7, 1),
+    ("H_kv", 2, 1), ("H_kv", -1, 1), ("H_kv", 1, 1), ("reserved", 1, 1), ("kv_stride_n", 60, 1),
 ])
 def test_invalid_arguments_are_rejected_on_the_host(abi, field, value, status):
     lib = abi.lib()

@@ -16,10 +16,13 @@ Workloads (shapes of the pages' benchmarks, data synthetic):
   block-sparse-64k    B=1,  H=8,  N=65536, d=64, 128x128 block mask with
                       the diagonal and block column 0 kept and the other
                       blocks kept with Bernoulli(q) so the density is ~0.1
+  gqa-4k              B=2,  H=32 query heads over H_kv=8 key/value heads,
+                      N=4096, d=128, bf16, causal (the head layout of the
+                      GQA comparison on the self-attention tutorial page)
 
 Q, K, V, dO are i.i.d. normal fp32 draws from a CPU torch.Generator seeded
 with 0, in the order Q, K, V, dO, scaled by the workload's std and rounded to
-the workload's dtype.
+the workload's dtype.  K and V have H_kv heads ([B, H_kv, N, d]).
 """
 
 import math
@@ -49,11 +52,16 @@ class Workload:
     block_density: Optional[float] = None   # block-sparse target density
     fwd_only: bool = False
     seed: int = 0
+    H_kv: int = 0                # key/value heads (0 = H)
     extra: dict = field(default_factory=dict)
 
     @property
     def scale(self):
         return 1.0 / math.sqrt(self.d)
+
+    @property
+    def kv_heads(self):
+        return self.H_kv or self.H
 
     @property
     def torch_dtype(self):
@@ -70,6 +78,7 @@ def _all():
         "gpt2-4k": Workload("gpt2-4k", 2, 12, 4096, 64, causal=True),
         "block-sparse-64k": Workload("block-sparse-64k", 1, 8, 65536, 64,
                                      block_density=0.1),
+        "gqa-4k": Workload("gqa-4k", 2, 32, 4096, 128, causal=True, H_kv=8),
     }
     for n in LONG_SWEEP:
         name = f"long-causal-{n}"
@@ -115,13 +124,14 @@ def make_inputs(w: Workload):
     """
     g = torch.Generator().manual_seed(w.seed)
     shape = (w.B, w.H, w.N, w.d)
+    kv_shape = (w.B, w.kv_heads, w.N, w.d)
 
-    def draw():
-        return (torch.randn(shape, generator=g, dtype=torch.float32) * w.std
+    def draw(sh):
+        return (torch.randn(sh, generator=g, dtype=torch.float32) * w.std
                 ).to(w.torch_dtype)
 
-    q, k, v = draw(), draw(), draw()
-    do = None if w.fwd_only else draw()
+    q, k, v = draw(shape), draw(kv_shape), draw(kv_shape)
+    do = None if w.fwd_only else draw(shape)
     key_lens = None
     if w.key_len_range is not None:
         lo, hi = w.key_len_range
@@ -138,8 +148,11 @@ def make_inputs(w: Workload):
                 offset=w.philox_offset)
 
 
-def random_case(B, H, N, d, seed, dtype=torch.bfloat16, std=1.0):
-    """Small i.i.d. normal q, k, v, do for edge-case tests."""
+def random_case(B, H, N, d, seed, dtype=torch.bfloat16, std=1.0, H_kv=None):
+    """Small i.i.d. normal q, k, v, do for edge-case tests (k, v with H_kv
+    heads when given)."""
     g = torch.Generator().manual_seed(seed)
     shape = (B, H, N, d)
-    return [(torch.randn(shape, generator=g) * std).to(dtype) for _ in range(4)]
+    kv_shape = (B, H if H_kv is None else H_kv, N, d)
+    return [(torch.randn(sh, generator=g) * std).to(dtype)
+            for sh in (shape, kv_shape, kv_shape, shape)]
