@@ -359,6 +359,7 @@ attn_status bwd_setup(const attn_params* p, void* ws, size_t ws_bytes, attn::Bwd
   a->stride_n = p->stride_n;
   kv_strides(p, &a->kv_stride_b, &a->kv_stride_h, &a->kv_stride_n);
   a->status = reinterpret_cast<int*>(w);
+  a->sched = reinterpret_cast<int*>(w + kSchedOffset);
   a->timeout_ns = kTimeoutNs;
   return ATTN_OK;
 }

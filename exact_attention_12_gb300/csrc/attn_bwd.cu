@@ -83,15 +83,29 @@ struct BwdCfg {
 // Barriers, TMEM address and the staged row statistics: the kernel's static
 // shared memory, padded to 3 KB so that the dynamic buffers after it start on
 // a 1024-byte boundary.
+constexpr int kBwdUnitRing = 4;   // claimed units not yet handed to every role
+constexpr int kBwdClaimAhead = 2;  // claim the next unit this many query tiles early
+
+// A claimed unit (one key tile of one (b, key/value head)) as the producer
+// publishes it.
+struct BwdUnit {
+  int w;      // unit index; -1: no more units
+  int kt, bhk;
+  int n;      // (query head, query tile) pairs it visits
+};
+
 struct __align__(1024) BwdCtl {
   float ld[2][2 * kTile];   // per Q stage: -L*log2e [0,128), -D [128,256)
-  uint64_t kvfull;
+  uint64_t kvfull, kvempty;
   uint64_t qfull[2], qempty[2], dofull[2], doempty[2];
-  uint64_t sfull, dpfull, pfull, dsfull, dqfull, dqfree, done;
+  uint64_t sfull, dpfull, pfull, dsfull, dqfull, dqfree, done, dkvfree, claim;
+  uint64_t unitfull[kBwdUnitRing], unitempty[kBwdUnitRing];
   uint64_t final_bar;
+  BwdUnit unit[kBwdUnitRing];
   uint32_t tmem_base;
   int abort_flag;
-  uint8_t pad[3072 - 2 * 2 * kTile * 4 - 19 * 8 - 8];
+  uint8_t pad[3072 - 2 * 2 * kTile * 4 - (23 + 2 * kBwdUnitRing) * 8 -
+              kBwdUnitRing * sizeof(BwdUnit) - 8];
 };
 static_assert(sizeof(BwdCtl) == 3072, "static shared block must stay 3 KB");
 
@@ -215,6 +229,19 @@ __device__ __forceinline__ void mma_kt_qt(uint32_t d_tmem, uint32_t a_base, uint
   }
 }
 
+// Unit w -> (key tile, b * H_kv + key/value head): head groups of G
+// consecutive (b, hk); within a group, key tiles in ascending order (heaviest
+// first for causal).
+__device__ __forceinline__ void bwd_unit_of(const MaskArgs& m, int w, int& kt, int& bhk) {
+  const int BHk = m.B * m.H_kv;
+  const int G = m.head_group, per = G * m.nb, nfull = BHk / G;
+  const int g = w < nfull * per ? w / per : nfull;
+  const int gs = g < nfull ? G : BHk - nfull * G;
+  const int rem = w - g * per;
+  kt = rem / gs;
+  bhk = g * G + rem % gs;
+}
+
 template <int D, bool DROPOUT>
 __global__ void __launch_bounds__(384, 1)
     bwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -239,31 +266,20 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const MaskArgs& m = a.m;
-  const int BHk = m.B * m.H_kv;
-  // one CTA per (b, key/value head hk, key tile); head groups of G
-  // consecutive (b, hk); within a group, key tiles in ascending order
-  // (heaviest first for causal)
-  int kt, bhk;
-  {
-    const int G = m.head_group, per = G * m.nb, nfull = BHk / G;
-    const int w = static_cast<int>(blockIdx.x);
-    const int g = w < nfull * per ? w / per : nfull;
-    const int gs = g < nfull ? G : BHk - nfull * G;
-    const int rem = w - g * per;
-    kt = rem / gs;
-    bhk = g * G + rem % gs;
-  }
-  const int b = bhk / m.H_kv, hk = bhk - b * m.H_kv;
-  const int k0 = kt * kTile;
-  const int limit = key_limit(m, b);
-  const QHeadWalk walk0{&m, kt, b, hk * m.kv_group, m.kv_group, limit};
-  int n = 0;   // (query head, query tile) pairs of this key tile
-  for (int qh = 0; qh < m.kv_group; ++qh)
-    n += bwd_tiles(m, kt, b * m.H + hk * m.kv_group + qh, limit).n;
+  // persistent: CTA i starts with unit i (one key tile of one (b, key/value
+  // head)); later units are claimed from the scheduler counter
+  const int total = m.nb * m.B * m.H_kv;
 
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
     mbar_init(&ctl.kvfull, 1);
+    mbar_init(&ctl.kvempty, 1);
+    mbar_init(&ctl.dkvfree, kComputeWarps);
+    mbar_init(&ctl.claim, 1);
+    for (int r = 0; r < kBwdUnitRing; ++r) {
+      mbar_init(&ctl.unitfull[r], 1);
+      mbar_init(&ctl.unitempty[r], 1 + kComputeWarps);   // the MMA thread, the compute warps
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctl.qfull[s], 1);
       mbar_init(&ctl.qempty[s], 1);
@@ -295,48 +311,88 @@ __global__ void __launch_bounds__(384, 1)
     regs_decrease<C::kRegsOther>();
     if (warp == kComputeWarps) {
       // ---------------------------------------------------------- producer
-      if (lane == 0 && n > 0) {
+      if (lane == 0) {
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
         tma_prefetch_desc(&tdo);
-        mbar_arrive_expect_tx(&ctl.kvfull, 2 * C::kTileBytes);
-#pragma unroll
-        for (int x = 0; x < C::kBoxes; ++x) {
-          tma_load_4d(sK + x * C::kBoxBytes, &tk, &ctl.kvfull, x * 64, k0, hk, b);
-          tma_load_4d(sV + x * C::kBoxBytes, &tv, &ctl.kvfull, x * 64, k0, hk, b);
-        }
-        int iq = 0, id = 0;   // Q / dO tiles issued
+        int iq = 0, id = 0;   // Q / dO tiles issued (all units)
+        int kw = 0;           // units with work
         bool ok = true;
-        QHeadWalk walk = walk0;
-        int h, qtile;
-        for (int i = 0; ok && walk.next(h, qtile); ++i) {
-          const int q0 = qtile * kTile;
-          const int bh = b * m.H + h;
-          const int sq = i % QS;
-          if (i >= QS && !(ok = mbar_wait(&ctl.qempty[sq], ((i / QS) - 1) & 1, wc, kSiteBwdEmpty)))
+        for (int pub = 0;; ++pub) {
+          // the current unit is close to its end: claim the next one
+          if (kw >= 1 && !(ok = mbar_wait(&ctl.claim, (kw - 1) & 1, wc, kSiteBwdLoad))) break;
+          const int w = pub == 0 ? static_cast<int>(blockIdx.x)
+                                 : static_cast<int>(gridDim.x) + atomicAdd(a.sched, 1);
+          BwdUnit u{-1, 0, 0, 0};
+          if (w < total) {
+            u.w = w;
+            bwd_unit_of(m, w, u.kt, u.bhk);
+            const int ub = u.bhk / m.H_kv, uhk = u.bhk - ub * m.H_kv;
+            const int ulim = key_limit(m, ub);
+            for (int qh = 0; qh < m.kv_group; ++qh)
+              u.n += bwd_tiles(m, u.kt, ub * m.H + uhk * m.kv_group + qh, ulim).n;
+          }
+          const int r = pub % kBwdUnitRing;
+          if (pub >= kBwdUnitRing &&
+              !(ok = mbar_wait(&ctl.unitempty[r], ((pub / kBwdUnitRing) - 1) & 1, wc,
+                               kSiteBwdLoad)))
             break;
-          mbar_arrive_expect_tx(&ctl.qfull[sq], C::kTileBytes + C::kLDBytes);
+          ctl.unit[r] = u;
+          mbar_arrive(&ctl.unitfull[r]);   // release: the consumers' wait acquires unit[r]
+          if (u.w < 0) break;
+          if (u.n == 0) continue;
+          const int b = u.bhk / m.H_kv, hk = u.bhk - b * m.H_kv;
+          const int k0 = u.kt * kTile;
+          // K_j, V_j: the previous unit's MMAs are done with them
+          if (kw >= 1 && !(ok = mbar_wait(&ctl.kvempty, (kw - 1) & 1, wc, kSiteBwdEmpty))) break;
+          mbar_arrive_expect_tx(&ctl.kvfull, 2 * C::kTileBytes);
 #pragma unroll
-          for (int x = 0; x < C::kBoxes; ++x)
-            tma_load_4d(sQ + sq * C::kTileBytes + x * C::kBoxBytes, &tq, &ctl.qfull[sq], x * 64,
-                        q0, h, b);
-          const int64_t row = static_cast<int64_t>(bh) * a.npad + q0;
-          bulk_load(sLD + sq * 2 * kTile, a.lse2 + row, kTile * 4, &ctl.qfull[sq]);
-          bulk_load(sLD + sq * 2 * kTile + kTile, a.dsum + row, kTile * 4, &ctl.qfull[sq]);
-          ++iq;
-          const int sd = i % DS;
-          if (i >= DS && !(ok = mbar_wait(&ctl.doempty[sd], ((i / DS) - 1) & 1, wc, kSiteBwdEmpty)))
-            break;
-          mbar_arrive_expect_tx(&ctl.dofull[sd], C::kTileBytes);
+          for (int x = 0; x < C::kBoxes; ++x) {
+            tma_load_4d(sK + x * C::kBoxBytes, &tk, &ctl.kvfull, x * 64, k0, hk, b);
+            tma_load_4d(sV + x * C::kBoxBytes, &tv, &ctl.kvfull, x * 64, k0, hk, b);
+          }
+          ++kw;
+          QHeadWalk walk{&m, u.kt, b, hk * m.kv_group, m.kv_group, key_limit(m, b)};
+          int h, qtile;
+          for (int i = 0; ok && walk.next(h, qtile); ++i) {
+            const int q0 = qtile * kTile;
+            const int bh = b * m.H + h;
+            const int sq = iq % QS;
+            if (iq >= QS &&
+                !(ok = mbar_wait(&ctl.qempty[sq], ((iq / QS) - 1) & 1, wc, kSiteBwdEmpty)))
+              break;
+            mbar_arrive_expect_tx(&ctl.qfull[sq], C::kTileBytes + C::kLDBytes);
 #pragma unroll
-          for (int x = 0; x < C::kBoxes; ++x)
-            tma_load_4d(sdO + sd * C::kTileBytes + x * C::kBoxBytes, &tdo, &ctl.dofull[sd],
-                        x * 64, q0, h, b);
-          ++id;
+            for (int x = 0; x < C::kBoxes; ++x)
+              tma_load_4d(sQ + sq * C::kTileBytes + x * C::kBoxBytes, &tq, &ctl.qfull[sq], x * 64,
+                          q0, h, b);
+            const int64_t row = static_cast<int64_t>(bh) * a.npad + q0;
+            bulk_load(sLD + sq * 2 * kTile, a.lse2 + row, kTile * 4, &ctl.qfull[sq]);
+            bulk_load(sLD + sq * 2 * kTile + kTile, a.dsum + row, kTile * 4, &ctl.qfull[sq]);
+            ++iq;
+            const int sd = id % DS;
+            if (id >= DS &&
+                !(ok = mbar_wait(&ctl.doempty[sd], ((id / DS) - 1) & 1, wc, kSiteBwdEmpty)))
+              break;
+            mbar_arrive_expect_tx(&ctl.dofull[sd], C::kTileBytes);
+#pragma unroll
+            for (int x = 0; x < C::kBoxes; ++x)
+              tma_load_4d(sdO + sd * C::kTileBytes + x * C::kBoxBytes, &tdo, &ctl.dofull[sd],
+                          x * 64, q0, h, b);
+            ++id;
+          }
+          if (!ok) break;
+        }
+        // no further claims from this CTA; the last CTA to get here resets the
+        // scheduler words for the next launch
+        __threadfence();
+        if (atomicAdd(a.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+          atomicExch(a.sched, 0);
+          atomicExch(a.sched + 1, 0);
         }
         if (ctl.abort_flag) {   // let issued copies land before the CTA exits
-          mbar_wait_drain(&ctl.kvfull, 0, a.timeout_ns);
+          if (kw >= 1) mbar_wait_drain(&ctl.kvfull, (kw - 1) & 1, a.timeout_ns);
           for (int ii = max(0, iq - QS); ii < iq; ++ii)
             mbar_wait_drain(&ctl.qfull[ii % QS], (ii / QS) & 1, a.timeout_ns);
           for (int ii = max(0, id - DS); ii < id; ++ii)
@@ -349,75 +405,115 @@ __global__ void __launch_bounds__(384, 1)
       //   dV_i, S^T_{i+1}, dK_i, dQ_i, dP^T_{i+1}
       // so S^T_{i+1} runs while the compute warps form dS_i, and dK_i / dQ_i
       // run while they form P_{i+1}.
-      if (lane == 0 && n > 0) {
+      if (lane == 0) {
         constexpr uint32_t kIdKN = idesc_bf16(128, D, false, true);   // K-major A, MN-major B
         constexpr uint32_t kIdNN = idesc_bf16(128, D, true, true);    // MN-major A and B
-        const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), ds_base = smem_u32(sDS);
-        bool ok = mbar_wait(&ctl.kvfull, 0, wc, kSiteBwdKV) &&
-                  mbar_wait(&ctl.qfull[0], 0, wc, kSiteBwdQ) &&
-                  mbar_wait(&ctl.dofull[0], 0, wc, kSiteBwdQ);
-        if (ok) {
+        const uint32_t k_base0 = smem_u32(sK), v_base0 = smem_u32(sV), ds_base0 = smem_u32(sDS);
+        int it = 0;   // query tiles processed (all units): the phase of every per-tile barrier
+        int kw = 0;   // units with work
+        bool ok = true;
+        for (int pub = 0; ok; ++pub) {
+          const int r = pub % kBwdUnitRing;
+          if (!(ok = mbar_wait(&ctl.unitfull[r], (pub / kBwdUnitRing) & 1, wc, kSiteBwdMma)))
+            break;
+          const BwdUnit u = ctl.unit[r];
+          mbar_arrive(&ctl.unitempty[r]);
+          if (u.w < 0) break;
+          const int n = u.n;
+          if (n == 0) continue;
+          ok = mbar_wait(&ctl.kvfull, kw & 1, wc, kSiteBwdKV) &&
+               mbar_wait(&ctl.qfull[it % QS], (it / QS) & 1, wc, kSiteBwdQ) &&
+               mbar_wait(&ctl.dofull[it % DS], (it / DS) & 1, wc, kSiteBwdQ);
+          // at d = 128 the dP^T columns hold the previous unit's last dQ until drained
+          if (ok && C::kDqAliasesDp && it >= 1)
+            ok = mbar_wait(&ctl.dqfree, (it - 1) & 1, wc, kSiteBwdMma);
+          if (!ok) break;
           tc_fence_after();
-          mma_kt_qt<D>(tmem + C::kSCol, k_base, smem_u32(sQ));        // S^T_0
+          mma_kt_qt<D>(tmem + C::kSCol, opaque(k_base0),
+                       smem_u32(sQ + (it % QS) * C::kTileBytes));   // S^T_0
           mma_commit(&ctl.sfull);
-          mma_kt_qt<D>(tmem + C::kDPCol, v_base, smem_u32(sdO));      // dP^T_0
+          mma_kt_qt<D>(tmem + C::kDPCol, opaque(v_base0),
+                       smem_u32(sdO + (it % DS) * C::kTileBytes));  // dP^T_0
           mma_commit(&ctl.dpfull);
+          // dK, dV of the previous unit have been read out by the epilogue
+          if (kw >= 1) {
+            if (!(ok = mbar_wait(&ctl.dkvfree, (kw - 1) & 1, wc, kSiteBwdMma))) break;
+            tc_fence_after();
+          }
+          bool claimed = false;
+          for (int i = 0; ok && i < n; ++i, ++it) {
+            const uint32_t ph = it & 1;
+            const uint32_t q_base = smem_u32(sQ + (it % QS) * C::kTileBytes);
+            const uint32_t do_base = smem_u32(sdO + (it % DS) * C::kTileBytes);
+            // at d = 128 the operand descriptors are rebuilt per tile from these
+            // (a few integer ops per MMA) rather than kept live across both
+            // loops, where they do not fit this warp's registers
+            const uint32_t k_base = D == 128 ? opaque(k_base0) : k_base0;
+            const uint32_t v_base = D == 128 ? opaque(v_base0) : v_base0;
+            const uint32_t ds_base = D == 128 ? opaque(ds_base0) : ds_base0;
+            if (!claimed && n - i <= kBwdClaimAhead) {
+              mbar_arrive(&ctl.claim);   // once per unit; at the latest in its last iteration
+              claimed = true;
+            }
+            // dV += P~^T dO_i; P~^T pairs of query rows 0..63 sit in columns
+            // [0,32), those of rows 64..127 in [64,96)
+            if (!(ok = mbar_wait(&ctl.pfull, ph, wc, kSiteBwdMma))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ts(tmem + C::kDVCol, tmem + C::kSCol + kk * 8 + (kk >= 4 ? 32 : 0),
+                     smem_desc(do_base + kk * 2048, C::kBoxBytes, 1024), kIdKN,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&ctl.doempty[it % DS]);
+            // S^T_{i+1}: the S^T columns were read by the compute warps before
+            // pfull and P~^T_i is consumed by dV_i, issued just before
+            if (i + 1 < n) {
+              if (!(ok = mbar_wait(&ctl.qfull[(it + 1) % QS], ((it + 1) / QS) & 1, wc, kSiteBwdQ)))
+                break;
+              tc_fence_after();
+              mma_kt_qt<D>(tmem + C::kSCol, k_base,
+                           smem_u32(sQ + ((it + 1) % QS) * C::kTileBytes));
+              mma_commit(&ctl.sfull);
+            }
+            // dK += dS^T Q_i
+            if (!(ok = mbar_wait(&ctl.dsfull, ph, wc, kSiteBwdMma))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+              mma_ss(tmem + C::kDKCol, smem_desc(ds_base + off, 16, 1024),
+                     smem_desc(q_base + kk * 2048, C::kBoxBytes, 1024), kIdKN,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+            }
+            // dQ_i = dS K_j (its columns: drained copy of the previous dQ read out)
+            if (!C::kDqAliasesDp && it >= 1) {
+              if (!(ok = mbar_wait(&ctl.dqfree, (it - 1) & 1, wc, kSiteBwdMma))) break;
+              tc_fence_after();
+            }
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ss(tmem + C::kDQCol, smem_desc(ds_base + kk * 2048, C::kBoxBytes, 1024),
+                     smem_desc(k_base + kk * 2048, C::kBoxBytes, 1024), kIdNN, kk > 0 ? 1u : 0u);
+            mma_commit(&ctl.dqfull);
+            mma_commit(&ctl.qempty[it % QS]);
+            // dP^T_{i+1} (for d = 128 its columns hold dQ_i until drained)
+            if (i + 1 < n) {
+              if (C::kDqAliasesDp && !(ok = mbar_wait(&ctl.dqfree, it & 1, wc, kSiteBwdMma)))
+                break;
+              if (!(ok = mbar_wait(&ctl.dofull[(it + 1) % DS], ((it + 1) / DS) & 1, wc,
+                                   kSiteBwdQ)))
+                break;
+              tc_fence_after();
+              mma_kt_qt<D>(tmem + C::kDPCol, v_base,
+                           smem_u32(sdO + ((it + 1) % DS) * C::kTileBytes));
+              mma_commit(&ctl.dpfull);
+            }
+          }
+          if (!ok) break;
+          mma_commit(&ctl.kvempty);   // every MMA reading K_j, V_j of this unit is issued
+          mma_commit(&ctl.done);      // ... and every one writing dK, dV
+          ++kw;
         }
-        for (int i = 0; ok && i < n; ++i) {
-          const uint32_t ph = i & 1;
-          const uint32_t q_base = smem_u32(sQ + (i % QS) * C::kTileBytes);
-          const uint32_t do_base = smem_u32(sdO + (i % DS) * C::kTileBytes);
-          // dV += P~^T dO_i; P~^T pairs of query rows 0..63 sit in columns
-          // [0,32), those of rows 64..127 in [64,96)
-          if (!(ok = mbar_wait(&ctl.pfull, ph, wc, kSiteBwdMma))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + C::kDVCol, tmem + C::kSCol + kk * 8 + (kk >= 4 ? 32 : 0),
-                   smem_desc(do_base + kk * 2048, C::kBoxBytes, 1024), kIdKN,
-                   (i > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&ctl.doempty[i % DS]);
-          // S^T_{i+1}: the S^T columns were read by the compute warps before
-          // pfull and P~^T_i is consumed by dV_i, issued just before
-          if (i + 1 < n) {
-            if (!(ok = mbar_wait(&ctl.qfull[(i + 1) % QS], ((i + 1) / QS) & 1, wc, kSiteBwdQ)))
-              break;
-            tc_fence_after();
-            mma_kt_qt<D>(tmem + C::kSCol, k_base, smem_u32(sQ + ((i + 1) % QS) * C::kTileBytes));
-            mma_commit(&ctl.sfull);
-          }
-          // dK += dS^T Q_i
-          if (!(ok = mbar_wait(&ctl.dsfull, ph, wc, kSiteBwdMma))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-            mma_ss(tmem + C::kDKCol, smem_desc(ds_base + off, 16, 1024),
-                   smem_desc(q_base + kk * 2048, C::kBoxBytes, 1024), kIdKN,
-                   (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          // dQ_i = dS K_j (its columns: drained copy of dQ_{i-1} read out)
-          if (!C::kDqAliasesDp && i >= 1) {
-            if (!(ok = mbar_wait(&ctl.dqfree, (i - 1) & 1, wc, kSiteBwdMma))) break;
-            tc_fence_after();
-          }
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ss(tmem + C::kDQCol, smem_desc(ds_base + kk * 2048, C::kBoxBytes, 1024),
-                   smem_desc(k_base + kk * 2048, C::kBoxBytes, 1024), kIdNN, kk > 0 ? 1u : 0u);
-          mma_commit(&ctl.dqfull);
-          mma_commit(&ctl.qempty[i % QS]);
-          // dP^T_{i+1} (for d = 128 its columns hold dQ_i until drained)
-          if (i + 1 < n) {
-            if (C::kDqAliasesDp && !(ok = mbar_wait(&ctl.dqfree, i & 1, wc, kSiteBwdMma))) break;
-            if (!(ok = mbar_wait(&ctl.dofull[(i + 1) % DS], ((i + 1) / DS) & 1, wc, kSiteBwdQ)))
-              break;
-            tc_fence_after();
-            mma_kt_qt<D>(tmem + C::kDPCol, v_base, smem_u32(sdO + ((i + 1) % DS) * C::kTileBytes));
-            mma_commit(&ctl.dpfull);
-          }
-        }
-        if (ok) mma_commit(&ctl.done);
         mma_commit(&ctl.final_bar);
         mbar_wait_drain(&ctl.final_bar, 0, a.timeout_ns);
       }
@@ -427,9 +523,6 @@ __global__ void __launch_bounds__(384, 1)
     // -------------------------------------------------------------- compute
     const int quarter = warp & 3, half = warp >> 2;
     const int r = quarter * 32 + lane;     // key row within the tile == TMEM lane
-    const int kj = k0 + r;                 // global key index
-    const bool key_ok = kj < limit;
-    const bool tile_keys_ok = k0 + kTile <= limit;   // no key of the tile is masked
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const int qc0 = half * 64;             // this warp's first query column
     const float c2 = a.scale_log2;
@@ -439,15 +532,33 @@ __global__ void __launch_bounds__(384, 1)
     uint8_t* region = sDS + half * C::kBoxBytes + quarter * 4096;
     uint8_t* stage = sStage + warp * 4096;
     bool ok = true;
-    QHeadWalk walk = walk0;
+    int it = 0;   // query tiles processed (all units): the phase of every per-tile barrier
+    int kw = 0;   // units with work
+    for (int pub = 0; ok; ++pub) {
+    const int ur = pub % kBwdUnitRing;
+    ok = __all_sync(0xffffffffu,
+                    mbar_wait(&ctl.unitfull[ur], (pub / kBwdUnitRing) & 1, wc, kSiteBwdSoft));
+    if (!ok) break;
+    const BwdUnit u = ctl.unit[ur];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl.unitempty[ur]);
+    if (u.w < 0) break;
+    const int n = u.n, kt = u.kt;
+    const int b = u.bhk / m.H_kv, hk = u.bhk - b * m.H_kv;
+    const int k0 = kt * kTile;
+    const int limit = key_limit(m, b);
+    const int kj = k0 + r;                 // global key index
+    const bool key_ok = kj < limit;
+    const bool tile_keys_ok = k0 + kTile <= limit;   // no key of the tile is masked
+    QHeadWalk walk{&m, kt, b, hk * m.kv_group, m.kv_group, limit};
     int h = 0, qtile = 0;
     int prev_h = 0, prev_q0 = 0;   // the pair whose dQ is drained next
-    for (int i = 0; i < n && walk.next(h, qtile); ++i) {
-      const uint32_t ph = i & 1;
+    for (int i = 0; i < n && walk.next(h, qtile); ++i, ++it) {
+      const uint32_t ph = it & 1;
       const int q0 = qtile * kTile;
       const int bh = b * m.H + h;
       // -L (log2 units) and -D of this warp's 64 query rows, staged by the producer
-      const float* nLw = sLD + (i % QS) * 2 * kTile + qc0;
+      const float* nLw = sLD + (it % QS) * 2 * kTile + qc0;
       const float* nDw = nLw + kTile;
       const bool diag = m.causal && qtile == kt;   // query q < key: masked
       const bool edge = diag || !tile_keys_ok;
@@ -515,7 +626,7 @@ __global__ void __launch_bounds__(384, 1)
       if (lane == 0) mbar_arrive(&ctl.pfull);
 
       if (i >= 1) {   // dQ of the previous query tile: its dS^T is consumed
-        ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dqfull, (i - 1) & 1, wc, kSiteBwdDq));
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dqfull, (it - 1) & 1, wc, kSiteBwdDq));
         if (!ok) break;
         tc_fence_after();
         drain_dq<D>(tl + C::kDQCol + half * C::kHalf, stage, region, &tdq, &ctl.dqfree,
@@ -571,8 +682,9 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.dsfull);
     }
-    if (ok && n > 0) {   // dQ of the last query tile
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dqfull, (n - 1) & 1, wc, kSiteBwdDq));
+    if (!ok) break;
+    if (n > 0) {   // dQ of the unit's last query tile
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dqfull, (it - 1) & 1, wc, kSiteBwdDq));
       if (ok) {
         tc_fence_after();
         drain_dq<D>(tl + C::kDQCol + half * C::kHalf, stage, region, &tdq, &ctl.dqfree,
@@ -582,7 +694,7 @@ __global__ void __launch_bounds__(384, 1)
 
     // epilogue: dV and c*dK, this warp's rows and half of the columns
     if (ok && n > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.done, 0, wc, kSiteBwdSoft));
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.done, kw & 1, wc, kSiteBwdSoft));
       if (ok) tc_fence_after();
     }
     if (ok) {
@@ -615,6 +727,13 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
+    }
+    if (ok && n > 0) {   // dK, dV read out: the next unit's first dK, dV MMAs may overwrite them
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.dkvfree);
+      ++kw;
+    }
     }
     if (lane == 0) tma_store_wait_all();   // this warp's reduce-adds are complete
   }
@@ -712,8 +831,14 @@ cudaError_t launch_main(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s) 
     if (static_cast<uint32_t>(fa.numRegs) < C::kRegsLaunch) return cudaErrorInvalidConfiguration;
     attr_set = true;
   }
-  // one CTA per (b, key/value head, key tile)
-  const unsigned grid = static_cast<unsigned>(a.m.nb) * a.m.B * a.m.H_kv;
+  // persistent: at most one CTA per SM, each claiming units (one key tile of
+  // one (b, key/value head)) until none are left
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long units = static_cast<long long>(a.m.nb) * a.m.B * a.m.H_kv;
+  const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
   bwd_bf16_kernel<D, DROP><<<grid, C::kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, tm.dout,
                                                                  tm.dq_acc, a);
   return cudaGetLastError();

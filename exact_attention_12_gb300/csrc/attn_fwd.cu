@@ -71,11 +71,11 @@ struct FwdCfg {
   // the keep masks (warp 12 + r: rows 32r .. 32r+31 of both tiles).
   // Registers are re-split after the start: kRegsSoftmax for the softmax
   // warpgroups, kRegsOther for warpgroup 2, kRegsMask for warpgroup 3:
-  // 256 * 208 + 128 * 80 <= 384 * 168 and 256 * 200 + 128 * (56 + 56) <= 512 * 128.
+  // 256 * 216 + 128 * 72 <= 384 * 168 and 256 * 200 + 128 * (56 + 56) <= 512 * 128.
   static constexpr int kThreads = DROPOUT ? 512 : 384;
   static constexpr uint32_t kRegsLaunch = DROPOUT ? 128 : 168;
-  static constexpr uint32_t kRegsSoftmax = DROPOUT ? 200 : 208;
-  static constexpr uint32_t kRegsOther = DROPOUT ? 56 : 80;
+  static constexpr uint32_t kRegsSoftmax = DROPOUT ? 200 : 216;
+  static constexpr uint32_t kRegsOther = DROPOUT ? 56 : 72;
   static constexpr uint32_t kRegsMask = 56;
   static_assert(256 * kRegsSoftmax + 128 * kRegsOther + (DROPOUT ? 128 * kRegsMask : 0) <=
                     kThreads * kRegsLaunch, "register re-split exceeds the launch allocation");
@@ -362,7 +362,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------- MMA issue
     if (lane == 0) {
-      const uint32_t q_base[2] = {smem_u32(sQ), smem_u32(sQ + C::kTileBytes)};
+      const uint32_t q_base0 = smem_u32(sQ);
+      // the Q descriptors are rebuilt where they are used (a few integer ops
+      // per MMA) instead of being kept live through the whole unit loop
+      auto q_base = [&](int x) { return opaque(q_base0) + static_cast<uint32_t>(x) * C::kTileBytes; };
       uint32_t cnt[2] = {0, 0};   // P tiles consumed per query-tile slot (all units)
       uint32_t cs_issued[2] = {0, 0};   // S tiles issued per slot (separate-P pipeline)
       int t = 0;                  // key/value tiles consumed (all units)
@@ -394,7 +397,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
               tc_fence_after();
               ++cs_issued[x];
             }
-            mma_scores<D>(tmem + C::kSCol + 128 * x, q_base[x], smem_u32(sK + (t % ST) * C::kTileBytes));
+            mma_scores<D>(tmem + C::kSCol + 128 * x, q_base(x), smem_u32(sK + (t % ST) * C::kTileBytes));
             mma_commit(&ctl.sfull[x]);
           }
         if (!ok) break;
@@ -430,7 +433,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
                   !(ok = k_next_ready = mbar_wait(&ctl.kfull[s1], ((t + 1) / ST) & 1, wc, kSiteFwdK)))
                 break;
               tc_fence_after();
-              mma_scores<D>(tmem + C::kSCol + 128 * x, q_base[x], smem_u32(sK + s1 * C::kTileBytes));
+              mma_scores<D>(tmem + C::kSCol + 128 * x, q_base(x), smem_u32(sK + s1 * C::kTileBytes));
               mma_commit(&ctl.sfull[x]);
               ++cs_issued[x];
             }
@@ -473,7 +476,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
                   if (!ok) break;
                   tc_fence_after();
                 }
-                mma_scores<D>(tmem + C::kSCol + 128 * x, q_base[x], smem_u32(sK + s1 * C::kTileBytes));
+                mma_scores<D>(tmem + C::kSCol + 128 * x, q_base(x), smem_u32(sK + s1 * C::kTileBytes));
                 mma_commit(&ctl.sfull[x]);
               }
             }

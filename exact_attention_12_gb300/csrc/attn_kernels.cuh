@@ -80,6 +80,7 @@ struct BwdArgs {
   int64_t stride_b, stride_h, stride_n;            // q, o, dO, dQ
   int64_t kv_stride_b, kv_stride_h, kv_stride_n;   // k, v, dK, dV
   int* status;
+  int* sched;                     // workspace scheduler words: next unit, CTAs finished
   uint64_t timeout_ns;
 };
 
