@@ -33,6 +33,7 @@ from .attention import (  # noqa: F401
     allowed_mask,
     attention_forward,
     attention_backward,
+    decode_forward,
     forward_rows,
     backward_keys,
     backward_rows,

@@ -301,3 +301,46 @@ def attention_backward(q, k, v, do, scale, causal=False, key_lens=None,
                 dK[b, h // g] += dk
                 dV[b, h // g] += dv
     return O, L, dQ, dK, dV
+
+
+def decode_forward(q, k, v, scale, cache_lens, causal=True):
+    """Attention of the newest query positions of each sequence against its
+    key/value cache (the decode step of autoregressive generation).
+
+    q: [B, H, N_q, d]; k, v: [B, H_kv, N_kv, d] (H_kv dividing H, grouped as
+    above); cache_lens: [B] integers, 0 <= cache_lens[b] <= N_kv.  Query row t
+    of batch b is the token at position cache_lens[b] - N_q + t, the last N_q
+    positions of the cached sequence; it attends the cached keys
+    j < cache_lens[b], and when `causal` only those with j <= its position
+    (the causal mask of "3.3 Hiểu sâu cơ chế Self-Attention", §10.2, aligned
+    to the end of the cache).  A row with no allowed key has O = 0 and
+    L = -inf.  Returns O [B, H, N_q, d] and L [B, H, N_q] in fp64.
+    """
+    B, H, Nq, d = np.shape(q)
+    g = _group(q, k)
+    Nkv = np.shape(k)[2]
+    lens = np.asarray(cache_lens, dtype=np.int64)
+    c = float(np.float32(scale))
+    O = np.zeros((B, H, Nq, d))
+    L = np.full((B, H, Nq), -np.inf)
+    cols = np.arange(Nkv)
+    for b in range(B):
+        n = int(lens[b])
+        pos = n - Nq + np.arange(Nq)
+        A = np.broadcast_to(cols[None, :] < n, (Nq, Nkv)).copy()
+        if causal:
+            A &= cols[None, :] <= pos[:, None]
+        for h in range(H):
+            qh = np.asarray(q[b, h], dtype=np.float64)
+            kh = np.asarray(k[b, h // g], dtype=np.float64)
+            vh = np.asarray(v[b, h // g], dtype=np.float64)
+            S = np.where(A, c * (qh @ kh.T), -np.inf)
+            live = A.any(axis=1)
+            if not live.any():
+                continue
+            m = S[live].max(axis=1)
+            Lr = m + np.log(np.exp(S[live] - m[:, None]).sum(axis=1))
+            P = np.exp(S[live] - Lr[:, None])
+            O[b, h, live] = P @ vh
+            L[b, h, live] = Lr
+    return O, L

@@ -543,3 +543,54 @@ def test_key_value_heads_must_divide_query_heads():
     k = np.zeros((1, 2, 4, 2))
     with pytest.raises(ValueError):
         A.attention_forward(q, k, k, scale=1.0)
+
+
+# ------------------------------------------------------------ decode step --
+# The newest N_q positions of each sequence against its key/value cache: the
+# same attention as the last N_q rows of the square problem over the cached
+# prefix, computed here through the square (already pinned) path.
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_decode_equals_last_rows_of_the_square_problem(causal):
+    B, H, Hk, Nq, Nkv, d = 3, 4, 2, 3, 40, 5
+    q = _rand4((B, H, Nq, d), 41)
+    k, v = _rand4((B, Hk, Nkv, d), 42), _rand4((B, Hk, Nkv, d), 43)
+    lens = [40, 17, 2]            # the last sequence is shorter than N_q
+    O, L = A.decode_forward(q, k, v, scale=0.45, cache_lens=lens, causal=causal)
+    for b, n in enumerate(lens):
+        # causal: query rows before the start of the sequence see no key; the
+        # others are the last rows of the square causal problem over the n
+        # cached positions.  Non-causal: positions do not matter, so every
+        # row is a row of a square problem of N' = max(n, N_q) positions whose
+        # keys beyond the cache are padding (key_lens = n).
+        rows = min(n, Nq) if causal else Nq
+        Np = n if causal else max(n, Nq)
+        if rows:
+            qs = np.zeros((1, H, Np, d))
+            qs[0, :, Np - rows:] = q[b, :, Nq - rows:]
+            ks, vs = np.zeros((1, Hk, Np, d)), np.zeros((1, Hk, Np, d))
+            ks[0, :, :n], vs[0, :, :n] = k[b, :, :n], v[b, :, :n]
+            Os, Ls = A.attention_forward(qs, ks, vs, scale=0.45, causal=causal, key_lens=[n])
+            np.testing.assert_allclose(O[b, :, Nq - rows:], Os[0, :, Np - rows:], rtol=1e-12,
+                                       atol=1e-12)
+            np.testing.assert_allclose(L[b, :, Nq - rows:], Ls[0, :, Np - rows:], rtol=1e-12,
+                                       atol=1e-12)
+        if rows < Nq:
+            assert np.all(O[b, :, :Nq - rows] == 0) and np.all(np.isneginf(L[b, :, :Nq - rows]))
+
+
+def test_decode_single_query_is_softmax_over_the_cache():
+    # one query per sequence: O = sum_j softmax_j(c q.k_j) v_j over the cached keys
+    B, H, Nkv, d = 2, 2, 9, 3
+    q = _rand4((B, H, 1, d), 51)
+    k, v = _rand4((B, H, Nkv, d), 52), _rand4((B, H, Nkv, d), 53)
+    lens = [9, 4]
+    O, L = A.decode_forward(q, k, v, scale=0.7, cache_lens=lens)
+    for b, n in enumerate(lens):
+        for h in range(H):
+            c = float(np.float32(0.7))   # the scale travels as a float32
+            s = c * np.array([float(np.dot(q[b, h, 0], k[b, h, j])) for j in range(n)])
+            w = scipy.special.softmax(s)
+            np.testing.assert_allclose(O[b, h, 0], (w[:, None] * v[b, h, :n]).sum(axis=0),
+                                       rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(L[b, h, 0], scipy.special.logsumexp(s), rtol=1e-12)
