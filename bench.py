@@ -392,6 +392,130 @@ def describe(w):
     return ", ".join(parts)
 
 
+# ------------------------------------------------------------ decode step --
+
+def decode_flops(w, key_lens):
+    """Matmul FLOPs of one decode step: 4 d per (query row, allowed key)."""
+    n_q = w.decode_n_q
+    total = 0
+    for n in key_lens.tolist():
+        n = max(0, min(int(n), w.N))
+        # query t at position n - n_q + t attends keys j <= its position (causal)
+        allowed = sum(max(0, min(n, n - n_q + t + 1)) for t in range(n_q)) if w.causal \
+            else n_q * n
+        total += allowed
+    return 4.0 * w.d * w.H * total
+
+
+def decode_bytes(w, key_lens):
+    """HBM bytes a decode step must move: the cached keys and values it reads
+    (bf16), the query rows read and the output rows written."""
+    cached = sum(max(0, min(int(n), w.N)) for n in key_lens.tolist())
+    kv = 2 * cached * w.kv_heads * w.d * 2
+    rows = w.B * w.H * w.decode_n_q
+    return kv + 2 * rows * w.d * 2 + rows * 4
+
+
+def measure_decode(ea, w, dev, steps, warmup):
+    """Device-timed decode steps over one resident cache (larger than the L2),
+    plus the e2e leg: each step uploads its query rows from pinned host memory
+    and downloads O, the cache staying resident as it would between tokens."""
+    inp = workloads.make_inputs(w)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    lens = inp["key_lens"].to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        ea.attention_decode(q, k, v, lens, scale=inp["scale"], causal=w.causal, out=o, lse=lse)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.__enter__()
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        ea.attention_decode(q, k, v, lens, scale=inp["scale"], causal=w.causal, out=o, lse=lse)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.__exit__()
+    ea.check()
+    ms = start.elapsed_time(end) / steps
+    # e2e: query rows up, output rows down, every step
+    hq = inp["q"].pin_memory()
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    for _ in range(3):
+        q.copy_(hq, non_blocking=True)
+        ea.attention_decode(q, k, v, lens, scale=inp["scale"], causal=w.causal, out=o, lse=lse)
+        ho.copy_(o, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    n_e2e = max(3, min(steps, 200))
+    for _ in range(n_e2e):
+        q.copy_(hq, non_blocking=True)
+        ea.attention_decode(q, k, v, lens, scale=inp["scale"], causal=w.causal, out=o, lse=lse)
+        ho.copy_(o, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e2e_ms = (time.perf_counter() - t0) / n_e2e * 1e3
+    return dict(inp=inp, ms=ms, e2e_ms=e2e_ms, clocks=sampler.summary(),
+                h2d=hq.numel() * hq.element_size(), d2h=ho.numel() * ho.element_size())
+
+
+def run_decode(args, w):
+    import numpy as np
+    from oracle import attention as oracle
+    inp_cpu = workloads.make_inputs(w)
+    # oracle: sequences timed one by one until the budget is spent
+    t0 = time.perf_counter()
+    done, flops_cpu = 0, 0.0
+    for b in range(w.B):
+        oracle.decode_forward(inp_cpu["q"][b:b + 1].double().numpy(),
+                              inp_cpu["k"][b:b + 1].double().numpy(),
+                              inp_cpu["v"][b:b + 1].double().numpy(), scale=inp_cpu["scale"],
+                              cache_lens=inp_cpu["key_lens"][b:b + 1].numpy(), causal=w.causal)
+        flops_cpu += decode_flops(workloads.get(w.name, B=1), inp_cpu["key_lens"][b:b + 1])
+        done += 1
+        if time.perf_counter() - t0 > args.cpu_budget:
+            break
+    dt_cpu = time.perf_counter() - t0
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import exact_attention_12_gb300 as ea
+    from exact_attention_12_gb300 import build
+    build.build()
+    r = measure_decode(ea, w, dev, args.steps, args.warmup)
+    lens = r["inp"]["key_lens"]
+    flops = decode_flops(w, lens)
+    nbytes = decode_bytes(w, lens)
+    _, _, hbm, src = peaks()
+    gbs = nbytes / (r["ms"] * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": flops / (r["ms"] * 1e-3) / 1e12, "unit": "TFLOPS",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": describe(w), "B": w.B, "H": w.H, "H_kv": w.kv_heads,
+                   "n_q": w.decode_n_q, "cache_capacity": w.N, "d": w.d, "causal": w.causal,
+                   "parallelism": "single GPU",
+                   "l2": f"the resident cache ({nbytes / 2**20:.0f} MiB read per step) is larger "
+                         f"than the 129 MB L2"},
+        "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": gbs, "peak": hbm,
+                     "unit": "GB/s", "frac": gbs / hbm, "peak_source": f"hbm_gbs ({src})",
+                     "traffic": None},
+        "gpu_launches": 2 * args.steps,
+        "clocks": r["clocks"],
+        "cpu_baseline": {"value": flops_cpu / dt_cpu / 1e12, "unit": "TFLOPS",
+                         "cores": _blas_threads(), "kind": "oracle",
+                         "sample": f"{done} of {w.B} sequences of {w.name}, fp64 numpy, "
+                                   f"{dt_cpu:.1f} s"},
+        "e2e": {"value": flops / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOPS",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "ms_per_step": r["e2e_ms"],
+                "note": "query rows up and output rows down per step; the cache stays resident"},
+    }
+    print(json.dumps(line))
+
+
 # ------------------------------------------------------------- profiling --
 
 def profile_steps(w, n):
@@ -430,6 +554,13 @@ def main():
 
     if args.profile_steps > 0:
         profile_steps(w, args.profile_steps)
+        return
+    if w.decode_n_q:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference",
+                              "unavailable": "the reference arm times the training step"}))
+        elif int(os.environ.get("RANK", "0")) == 0:
+            run_decode(args, w)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -8,6 +8,7 @@ PyTorch fallback: calls fail if the library is not built.
 from ._abi import AttnError  # noqa: F401
 from .api import (  # noqa: F401
     attention_bwd,
+    attention_decode,
     attention_fwd,
     check,
     make_params,

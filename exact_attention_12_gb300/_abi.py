@@ -28,6 +28,9 @@ EXPORTS = {
     "attn_bwd_main": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_size_t, ctypes.c_void_p]),
     "attn_bwd_dq": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_size_t, ctypes.c_void_p]),
     "attn_bwd_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 11),
+    "attn_decode_workspace_size": (ctypes.c_size_t, [ctypes.c_void_p, ctypes.c_int32]),
+    "attn_decode": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32] + [ctypes.c_void_p] * 6
+                    + [ctypes.c_size_t, ctypes.c_void_p]),
     "attn_selftest_timeout": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]),
     "attn_check": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),

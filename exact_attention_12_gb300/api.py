@@ -59,7 +59,7 @@ def make_params(q, *, k=None, scale=None, causal=False, key_lens=None, dropout_p
         raise ValueError("the head dimension must be contiguous")
     p.stride_b, p.stride_h, p.stride_n = sb, sh, sn
     if k is not None:
-        if k.dim() != 4 or k.shape[0] != B or k.shape[2:] != q.shape[2:]:
+        if k.dim() != 4 or k.shape[0] != B or k.shape[3] != d:
             raise ValueError("k must be [B, H_kv, N, d] like q")
         if k.stride(3) != 1 and d > 1:
             raise ValueError("the head dimension must be contiguous")
@@ -92,12 +92,13 @@ def _same_layout(ref, *ts):
             raise ValueError("tensors of one role must share shape, strides, dtype and device")
 
 
-def _check_kv(q, k):
+def _check_kv(q, k, same_n=True):
     if k.device != q.device or k.dtype != q.dtype:
         raise ValueError("k, v must have q's dtype and device")
     H, H_kv = q.shape[1], k.shape[1] if k.dim() == 4 else -1
     divides = H_kv == 0 if H == 0 else (H_kv >= 1 and H % H_kv == 0)
-    if k.dim() != 4 or k.shape[0] != q.shape[0] or k.shape[2:] != q.shape[2:] or not divides:
+    if k.dim() != 4 or k.shape[0] != q.shape[0] or k.shape[3] != q.shape[3] or not divides \
+            or (same_n and k.shape[2] != q.shape[2]):
         raise ValueError("k, v must be [B, H_kv, N, d] with H_kv dividing q's H")
 
 
@@ -162,6 +163,38 @@ def attention_bwd(dout, q, k, v, o, lse, *, scale=None, causal=False, key_lens=N
                         _stream(q.device))
     check_status(st, "attn_bwd")
     return dq, dk, dv
+
+
+def attention_decode(q, k, v, cache_lens, *, scale=None, causal=True, out=None, lse=None,
+                     ws=None):
+    """The decode step: the newest n_q query positions of each sequence against
+    its key/value cache (see attn_decode in include/attn.h).
+
+    q: [B, H, n_q, d] bf16; k, v: [B, H_kv, N, d] bf16 caches of capacity N
+    with H_kv dividing H; cache_lens: int32 [B] on the device, keys cached per
+    sequence.  Query row t of sequence b is the token at position
+    cache_lens[b] - n_q + t.  Returns (o, lse) with o like q and lse fp32
+    [B, H, n_q].
+    """
+    _check_kv(q, k, same_n=False)
+    _same_layout(k, v)
+    n_q = q.shape[2]
+    p = make_params(q, k=k, scale=scale, causal=causal, key_lens=cache_lens)
+    p.N = k.shape[2]
+    o = _like(q) if out is None else out
+    _same_layout(q, o)
+    B, H = q.shape[:2]
+    if lse is None:
+        lse = torch.empty((B, H, n_q), dtype=torch.float32, device=q.device)
+    need = lib().attn_decode_workspace_size(ctypes.byref(p), n_q)
+    if need == 0:
+        check_status(_abi.ATTN_ERR_INVALID_ARG, "attn_decode_workspace_size")
+    w = workspace(q.device, need) if ws is None else ws
+    st = lib().attn_decode(ctypes.byref(p), n_q, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                           o.data_ptr(), lse.data_ptr(), w.data_ptr(),
+                           w.numel() * w.element_size(), _stream(q.device))
+    check_status(st, "attn_decode")
+    return o, lse
 
 
 def check(ws=None, device=None):

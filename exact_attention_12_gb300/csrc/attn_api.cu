@@ -443,6 +443,110 @@ attn_status attn_bwd(const attn_params* p, const void* q, const void* k, const v
   return attn_bwd_dq(p, dq, ws, ws_bytes, stream);
 }
 
+// ------------------------------------------------------------ decode step --
+
+namespace {
+
+// Cache keys per split: enough splits that the grid covers every SM about
+// eight times over (short CTAs balance the sequences' different lengths; much
+// shorter ones spend their time in set-up), in multiples of the 64-key tile.
+int decode_chunk(const attn_params* p) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 148;
+  const int64_t heads = static_cast<int64_t>(p->B) * kv_heads(p);
+  const int64_t want = 8LL * sms;
+  int64_t per = heads > 0 ? (static_cast<int64_t>(p->N) * heads + want - 1) / want : p->N;
+  per = (per + 63) / 64 * 64;
+  if (per < 256) per = 256;
+  return static_cast<int>(per);
+}
+
+attn_status validate_decode(const attn_params* p, int32_t n_q) {
+  attn_status st = validate(p, false);
+  if (st != ATTN_OK) return st;
+  if (p->dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "decode is implemented for bf16");
+  if (p->dropout_p != 0.f || p->block_mask != nullptr)
+    return fail(ATTN_ERR_UNSUPPORTED, "decode takes no dropout and no block mask");
+  if (p->key_lens == nullptr) return fail(ATTN_ERR_INVALID_ARG, "decode needs key_lens (cache lengths)");
+  if (n_q < 1) return fail(ATTN_ERR_INVALID_ARG, "n_q=%d must be >= 1", n_q);
+  if (p->H > 0 && static_cast<int64_t>(p->H / kv_heads(p)) * n_q > attn::kDecMaxRows)
+    return fail(ATTN_ERR_UNSUPPORTED, "(H / H_kv) * n_q = %lld exceeds %d",
+                static_cast<long long>(p->H / kv_heads(p)) * n_q, attn::kDecMaxRows);
+  return ATTN_OK;
+}
+
+struct DecodeLayout {
+  size_t part_o = 0, part_l = 0, total = 0;
+  int chunk = 0, splits = 0;
+};
+
+DecodeLayout decode_layout(const attn_params* p, int32_t n_q) {
+  DecodeLayout L;
+  L.chunk = decode_chunk(p);
+  L.splits = p->N > 0 ? (p->N + L.chunk - 1) / L.chunk : 0;
+  const size_t rows = static_cast<size_t>(p->B) * p->H * n_q;
+  size_t off = kHeaderBytes;
+  L.part_o = off;
+  off = round_up(off + static_cast<size_t>(L.splits) * rows * p->d * 4, 256);
+  L.part_l = off;
+  off = round_up(off + static_cast<size_t>(L.splits) * rows * 4, 256);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+size_t attn_decode_workspace_size(const attn_params* p, int32_t n_q) {
+  if (validate_decode(p, n_q) != ATTN_OK) return 0;
+  return decode_layout(p, n_q).total;
+}
+
+attn_status attn_decode(const attn_params* p, int32_t n_q, const void* q, const void* k,
+                        const void* v, void* o, float* lse, void* ws, size_t ws_bytes,
+                        void* stream) {
+  attn_status st = validate_decode(p, n_q);
+  if (st != ATTN_OK) return st;
+  const DecodeLayout L = decode_layout(p, n_q);
+  if (ws == nullptr) return fail(ATTN_ERR_WORKSPACE, "workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(ATTN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < L.total)
+    return fail(ATTN_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes, L.total);
+  if (empty_problem(p)) return ATTN_OK;
+  if ((st = check_ptrs({q, k, v, o, lse})) != ATTN_OK) return st;
+  char* w = static_cast<char*>(ws);
+  attn::DecodeArgs a{};
+  a.m = mask_args(p, WsLayout{}, w, false);
+  a.d = p->d;
+  a.n_q = n_q;
+  a.rows = (p->H / kv_heads(p)) * n_q;
+  a.chunk = L.chunk;
+  a.splits = L.splits;
+  a.scale_log2 = p->scale * kLog2e;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.stride_b = p->stride_b;
+  a.stride_h = p->stride_h;
+  a.stride_n = p->stride_n;
+  a.part_o = reinterpret_cast<float*>(w + L.part_o);
+  a.part_l = reinterpret_cast<float*>(w + L.part_l);
+  a.status = reinterpret_cast<int*>(w);
+  a.timeout_ns = kTimeoutNs;
+  // k, v with 64-key boxes
+  attn::TensorMaps tm{};
+  int64_t sb, sh, sn;
+  kv_strides(p, &sb, &sh, &sn);
+  if ((st = make_map(&tm.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->B, kv_heads(p), p->N,
+                     p->d, sb, sh, sn, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK)
+    return st;
+  if ((st = make_map(&tm.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->B, kv_heads(p), p->N,
+                     p->d, sb, sh, sn, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK)
+    return st;
+  const cudaError_t e = attn::launch_decode(tm, o, lse, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "decode launch");
+}
+
 attn_status attn_check(void* ws, void* stream) {
   if (ws == nullptr) return fail(ATTN_ERR_WORKSPACE, "workspace is NULL");
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cuda_bf16.h>
+
 #include "philox.cuh"
 
 namespace attn {
@@ -17,7 +19,8 @@ enum WaitSite : int {
   kSiteFwdQ = 1, kSiteFwdK, kSiteFwdV, kSiteFwdKvEmpty, kSiteFwdSFull, kSiteFwdSFree,
   kSiteFwdPFull, kSiteFwdPvDone, kSiteFwdUnit, kSiteFwdMask,
   kSiteBwdLoad = 20, kSiteBwdKV, kSiteBwdQ, kSiteBwdMma, kSiteBwdSoft, kSiteBwdDq,
-  kSiteBwdEmpty, kSiteBwdFree, kSiteBwdSmem
+  kSiteBwdEmpty, kSiteBwdFree, kSiteBwdSmem,
+  kSiteDecode = 40
 };
 
 // Device status code for a kernel that found its shared memory misaligned
@@ -84,6 +87,25 @@ struct BwdArgs {
   uint64_t timeout_ns;
 };
 
+// Decode step: query rows per CTA (the key/value group's heads x n_q) at most.
+constexpr int kDecMaxRows = 64;
+
+struct DecodeArgs {
+  MaskArgs m;                     // N = cache capacity, key_lens = cache lengths
+  int d;
+  int n_q;                        // query rows per sequence (the newest positions)
+  int rows;                       // kv_group * n_q: query rows of one CTA
+  int chunk;                      // cache keys per split (multiple of 64)
+  int splits;                     // ceil(N / chunk)
+  float scale_log2;
+  const __nv_bfloat16* q;         // [B, H, n_q, d] with the strides below
+  int64_t stride_b, stride_h, stride_n;   // q and o
+  float* part_o;                  // workspace [splits][B*H*n_q][d]
+  float* part_l;                  // workspace [splits][B*H*n_q]
+  int* status;
+  uint64_t timeout_ns;
+};
+
 // Tensor maps: 4-D {d, N, H, B}, 64-element x 128-row boxes, 128-byte swizzle.
 struct TensorMaps {
   CUtensorMap q, k, v, o, dout, dq_acc;
@@ -99,6 +121,9 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const BwdArgs
                                   cudaStream_t s);
 cudaError_t launch_bwd_bf16(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_dq_convert(void* dq, const BwdArgs& a, cudaStream_t s);
+// k, v maps with 64-row boxes
+cudaError_t launch_decode(const TensorMaps& tm, void* o, float* lse, const DecodeArgs& a,
+                          cudaStream_t s);
 
 // Records `msg` as the calling thread's last error (what attn_last_error()
 // returns) and passes `status` through.

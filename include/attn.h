@@ -176,6 +176,30 @@ attn_status attn_bwd_noalloc(const attn_params* p, const void* q,
                              const float* lse, const void* dout, void* dq,
                              void* dk, void* dv, void* stream);
 
+/* Decode step: the newest n_q query positions of each sequence against its
+ * key/value cache.  The pages' pass is the training forward; this is the
+ * same attention at generation time, where each new token attends the keys
+ * cached so far (the KV cache of "3.3 Hiểu sâu cơ chế Self-Attention", §9).
+ *   p->N          cache capacity: k and v are [B, H_kv, N, d] (key/value
+ *                 strides and grouping as in attn_params)
+ *   p->key_lens   required, device [B]: cached keys per sequence, clamped to
+ *                 [0, N].  Query row t of sequence b is the token at position
+ *                 key_lens[b] - n_q + t.
+ *   p->causal     nonzero: query t attends keys j <= its position; otherwise
+ *                 every cached key
+ *   q, o          [B, H, n_q, d] with the query strides (stride_n steps over
+ *                 the n_q rows); bf16
+ *   lse           fp32 [B, H, n_q] (natural log; -inf for a row with no key)
+ * 1 <= n_q and (H / H_kv) * n_q <= 64; dropout_p must be 0 and block_mask
+ * NULL (ATTN_ERR_UNSUPPORTED otherwise).  The cache is split into chunks
+ * processed in parallel and merged by the logsumexp rule; the workspace
+ * (attn_decode_workspace_size bytes, the same 256-byte header rules as
+ * above) holds the per-chunk partial results. */
+size_t attn_decode_workspace_size(const attn_params* p, int32_t n_q);
+attn_status attn_decode(const attn_params* p, int32_t n_q, const void* q, const void* k,
+                        const void* v, void* o, float* lse, void* ws, size_t ws_bytes,
+                        void* stream);
+
 /* Diagnostic: runs the kernels' time-out path on purpose.  Enqueues one warp
  * that waits on a barrier nothing arrives at, giving up after `limit_ns`
  * (clamped to [1 ms, 2 s]); it records ATTN_ERR_TIMEOUT in the workspace's

@@ -19,6 +19,10 @@ Workloads (shapes of the pages' benchmarks, data synthetic):
   gqa-4k              B=2,  H=32 query heads over H_kv=8 key/value heads,
                       N=4096, d=128, bf16, causal (the head layout of the
                       GQA comparison on the self-attention tutorial page)
+  decode-gqa-8k       decode step: B=16, one new token per sequence, H=32
+                      query heads over H_kv=8 key/value heads, d=128, bf16,
+                      key/value caches of capacity N=8192 holding
+                      U{4096..8192} keys (seed 1), causal
 
 Q, K, V, dO are i.i.d. normal fp32 draws from a CPU torch.Generator seeded
 with 0, in the order Q, K, V, dO, scaled by the workload's std and rounded to
@@ -53,6 +57,7 @@ class Workload:
     fwd_only: bool = False
     seed: int = 0
     H_kv: int = 0                # key/value heads (0 = H)
+    decode_n_q: int = 0          # decode step: query rows per sequence (0 = square problem)
     extra: dict = field(default_factory=dict)
 
     @property
@@ -79,6 +84,8 @@ def _all():
         "block-sparse-64k": Workload("block-sparse-64k", 1, 8, 65536, 64,
                                      block_density=0.1),
         "gqa-4k": Workload("gqa-4k", 2, 32, 4096, 128, causal=True, H_kv=8),
+        "decode-gqa-8k": Workload("decode-gqa-8k", 16, 32, 8192, 128, causal=True, H_kv=8,
+                                  key_len_range=(4096, 8192), fwd_only=True, decode_n_q=1),
     }
     for n in LONG_SWEEP:
         name = f"long-causal-{n}"
@@ -123,7 +130,7 @@ def make_inputs(w: Workload):
     block_mask (uint8 [nb, nb] or None) and the scalar settings.
     """
     g = torch.Generator().manual_seed(w.seed)
-    shape = (w.B, w.H, w.N, w.d)
+    shape = (w.B, w.H, w.decode_n_q or w.N, w.d)
     kv_shape = (w.B, w.kv_heads, w.N, w.d)
 
     def draw(sh):
