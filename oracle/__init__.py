@@ -23,6 +23,9 @@ Modules
                 a vectorised numpy version and an independent scalar one.
   blockwise  -- the pages' tiled online-softmax recurrence, restated; used
                 only to pin the direct definition in tests.
+  fp8        -- E4M3 codes with per-tensor de-scale factors as inputs (OCP
+                OFP8 format), and the terms of the error bound for a kernel
+                that rounds the probabilities to E4M3.
 
 Parity status: the Philox constants are not pinned to published known-answer
 vectors (none are available here); "parity partly unpinned" for `philox`.
@@ -41,3 +44,4 @@ from .attention import (  # noqa: F401
     keep_scale,
     keep_mask,
 )
+from .fp8 import e4m3_value, fp8_forward, rounding_terms  # noqa: F401

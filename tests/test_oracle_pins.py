@@ -594,3 +594,102 @@ def test_decode_single_query_is_softmax_over_the_cache():
             np.testing.assert_allclose(O[b, h, 0], (w[:, None] * v[b, h, :n]).sum(axis=0),
                                        rtol=1e-12, atol=1e-12)
             np.testing.assert_allclose(L[b, h, 0], scipy.special.logsumexp(s), rtol=1e-12)
+
+
+# ------------------------------------------------------------------ FP8 ----
+
+from oracle import fp8 as F  # noqa: E402
+
+
+@pytest.mark.parametrize("code,value", [
+    (0x00, 0.0), (0x38, 1.0), (0x39, 1.125), (0x3F, 1.875), (0x40, 2.0),
+    (0x30, 0.5), (0x08, 2.0 ** -6), (0x07, 0.875 * 2.0 ** -6), (0x01, 2.0 ** -9),
+    (0x77, 240.0), (0x78, 256.0), (0x7E, 448.0), (0xB8, -1.0), (0xFE, -448.0),
+    (0x81, -(2.0 ** -9)),
+])
+def test_e4m3_values_from_the_format_definition(code, value):
+    # sign | 4-bit exponent (bias 7) | 3-bit mantissa, subnormals at exponent 0
+    assert F.e4m3_value([code])[0] == value
+
+
+def test_e4m3_nan_zero_and_ordering():
+    vals = F.e4m3_value(np.arange(256))
+    assert np.isnan(vals[0x7F]) and np.isnan(vals[0xFF])
+    assert np.isnan(vals).sum() == 2
+    assert vals[0x80] == 0.0 and math.copysign(1.0, vals[0x80]) == -1.0
+    pos = vals[:0x7F]
+    assert np.all(np.diff(pos) > 0)                    # codes 0..126 increase strictly
+    assert np.array_equal(vals[0x80:0xFF], -pos)       # the sign bit only negates
+    assert pos.max() == F.E4M3_MAX
+    # spacing: 2^-9 through the subnormals and the first normal binade, then doubling
+    assert np.all(np.diff(pos[:17]) == 2.0 ** -9)
+    assert np.diff(pos[0x38:0x40]).tolist() == [0.125] * 7
+
+
+def test_e4m3_matches_torch_float8():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = F.e4m3_value(np.arange(256))
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all()
+
+
+def test_fp8_forward_descales_each_operand():
+    rng = np.random.default_rng(3)
+    q8 = rng.integers(0, 0x70, (1, 2, 9, 4)).astype(np.uint8)
+    k8 = rng.integers(0, 0x70, (1, 2, 9, 4)).astype(np.uint8)
+    v8 = rng.integers(0x80, 0xF0, (1, 2, 9, 4)).astype(np.uint8)
+    # constant V (all one code): O is that value times v_descale in every row
+    vc = np.full_like(v8, 0x44)                                        # 3.0
+    O, _ = F.fp8_forward(q8, k8, vc, 0.5, 0.25, 0.125, 0.5, causal=True)
+    assert np.allclose(O, 0.375, rtol=0, atol=1e-14)
+    # the scores see q_descale * k_descale * scale as one factor: doubling
+    # q_descale and halving scale leaves O and L unchanged
+    O1, L1 = F.fp8_forward(q8, k8, v8, 0.5, 0.25, 2.0, 0.5)
+    O2, L2 = F.fp8_forward(q8, k8, v8, 1.0, 0.25, 2.0, 0.25)
+    assert np.allclose(O1, O2, atol=1e-12) and np.allclose(L1, L2, atol=1e-12)
+    # N = 1: O = V
+    O, L = F.fp8_forward(q8[:, :, :1], k8[:, :, :1], v8[:, :, :1], 1.0, 1.0, 2.0, 0.5)
+    assert np.array_equal(O, 2.0 * F.e4m3_value(v8[:, :, :1]))
+
+
+def test_rounding_terms_special_cases():
+    rng = np.random.default_rng(4)
+    q, k, v = _rand((1, 1, 6, 3), 5), _rand((1, 1, 6, 3), 6), _rand((1, 1, 6, 3), 7)
+    A_, T_ = F.rounding_terms(q, k, v, 0.75, causal=True)
+    # row 0 attends key 0 only: A = T = |V_0|
+    assert np.allclose(A_[0, 0, 0], np.abs(v[0, 0, 0])) and np.allclose(T_[0, 0, 0], np.abs(v[0, 0, 0]))
+    # |O| <= A (triangle inequality); A and T against scalar loops
+    O, _ = A.attention_forward(q, k, v, 0.75, causal=True)
+    assert np.all(np.abs(O) <= A_ + 1e-12)
+    for i in range(6):
+        s = 0.75 * np.array([q[0, 0, i] @ k[0, 0, j] for j in range(i + 1)])
+        w = np.exp(s - s.max())
+        for c in range(3):
+            a = sum(w[j] * abs(v[0, 0, j, c]) for j in range(i + 1)) / w.sum()
+            t = sum(abs(v[0, 0, j, c]) for j in range(i + 1)) / w.sum()
+            assert abs(A_[0, 0, i, c] - a) < 1e-12 and abs(T_[0, 0, i, c] - t) < 1e-12
+    # a row with no key: both zero
+    A0, T0 = F.rounding_terms(q, k, v, 0.75, key_lens=[0])
+    assert not A0.any() and not T0.any()
+
+
+def test_rounding_bound_holds_for_simulated_e4m3_probabilities():
+    # round the unnormalised weights to the nearest E4M3 value (a brute-force
+    # nearest search over the 127 non-negative codes), with a lazily kept max
+    # (gamma up to 2^8), and check the error against 2^-4 A + 2^-10 T
+    grid = F.e4m3_value(np.arange(0x7F))
+    rng = np.random.default_rng(8)
+    q, k, v = _rand((1, 1, 40, 8), 9, 1.5), _rand((1, 1, 40, 8), 10, 1.5), _rand((1, 1, 40, 8), 11)
+    O, _ = A.attention_forward(q, k, v, 0.5, causal=True)
+    A_, T_ = F.rounding_terms(q, k, v, 0.5, causal=True)
+    for i in range(40):
+        s = 0.5 * (q[0, 0, i] @ k[0, 0, : i + 1].T)
+        gamma = 2.0 ** rng.uniform(0, 8)
+        w = gamma * np.exp(s - s.max())
+        wr = grid[np.abs(grid[None, :] - w[:, None]).argmin(axis=1)]
+        o = (wr @ v[0, 0, : i + 1]) / w.sum()
+        assert np.all(np.abs(o - O[0, 0, i]) <= 2.0 ** -4 * A_[0, 0, i] + 2.0 ** -10 * T_[0, 0, i] + 1e-12)

@@ -23,10 +23,16 @@ Workloads (shapes of the pages' benchmarks, data synthetic):
                       query heads over H_kv=8 key/value heads, d=128, bf16,
                       key/value caches of capacity N=8192 holding
                       U{4096..8192} keys (seed 1), causal
+  fp8-long-causal-<N> the long-context sweep's shapes with E4M3 inputs,
+                      forward only
 
 Q, K, V, dO are i.i.d. normal fp32 draws from a CPU torch.Generator seeded
 with 0, in the order Q, K, V, dO, scaled by the workload's std and rounded to
 the workload's dtype.  K and V have H_kv heads ([B, H_kv, N, d]).
+
+FP8 workloads store each of Q, K, V as E4M3 codes (torch.float8_e4m3fn) with
+one de-scale factor per tensor: descale = amax / 448 of the fp32 draw
+(448 is the largest E4M3 value), codes = round-to-nearest(x / descale).
 """
 
 import math
@@ -46,7 +52,7 @@ class Workload:
     H: int
     N: int
     d: int
-    dtype: str = "bf16"          # "bf16" or "fp32"
+    dtype: str = "bf16"          # "bf16", "fp32" or "fp8" (E4M3 inputs, bf16 output)
     causal: bool = False
     std: float = 1.0
     key_len_range: Optional[tuple] = None   # (lo, hi) inclusive, seed 1
@@ -70,7 +76,7 @@ class Workload:
 
     @property
     def torch_dtype(self):
-        return torch.float32 if self.dtype == "fp32" else torch.bfloat16
+        return {"fp32": torch.float32, "fp8": torch.float8_e4m3fn}.get(self.dtype, torch.bfloat16)
 
 
 def _all():
@@ -90,6 +96,8 @@ def _all():
     for n in LONG_SWEEP:
         name = f"long-causal-{n}"
         w[name] = Workload(name, 1, 16, n, 128, causal=True, std=0.5)
+        w["fp8-" + name] = Workload("fp8-" + name, 1, 16, n, 128, dtype="fp8", causal=True,
+                                    std=0.5, fwd_only=True)
     return w
 
 
@@ -137,7 +145,14 @@ def make_inputs(w: Workload):
         return (torch.randn(sh, generator=g, dtype=torch.float32) * w.std
                 ).to(w.torch_dtype)
 
-    q, k, v = draw(shape), draw(kv_shape), draw(kv_shape)
+    descales = {}
+    if w.dtype == "fp8":
+        q, k, v = [fp8_quantize(torch.randn(sh, generator=g, dtype=torch.float32) * w.std)
+                   for sh in (shape, kv_shape, kv_shape)]
+        descales = dict(q_descale=q[1], k_descale=k[1], v_descale=v[1])
+        q, k, v = q[0], k[0], v[0]
+    else:
+        q, k, v = draw(shape), draw(kv_shape), draw(kv_shape)
     do = None if w.fwd_only else draw(shape)
     key_lens = None
     if w.key_len_range is not None:
@@ -152,7 +167,25 @@ def make_inputs(w: Workload):
     return dict(q=q, k=k, v=v, do=do, key_lens=key_lens,
                 block_mask=block_mask, scale=w.scale, causal=w.causal,
                 dropout_p=w.dropout_p, seed=w.philox_seed,
-                offset=w.philox_offset)
+                offset=w.philox_offset, **descales)
+
+
+def fp8_quantize(x):
+    """E4M3 codes of an fp32 tensor with one de-scale factor: returns
+    (codes as torch.float8_e4m3fn, descale) with descale = amax / 448 (a
+    float32 value; 1 for an all-zero tensor) and codes = x / descale rounded
+    to the nearest E4M3 value."""
+    amax = float(x.abs().max()) if x.numel() else 0.0
+    descale = float(torch.tensor(amax / 448.0 if amax > 0 else 1.0, dtype=torch.float32))
+    return (x / descale).clamp(-448.0, 448.0).to(torch.float8_e4m3fn), descale
+
+
+def random_case_fp8(B, H, N, d, seed, std=1.0, H_kv=None):
+    """Small E4M3 q, k, v with their de-scale factors: [(codes, descale)] * 3."""
+    g = torch.Generator().manual_seed(seed)
+    kv_shape = (B, H if H_kv is None else H_kv, N, d)
+    return [fp8_quantize(torch.randn(sh, generator=g) * std)
+            for sh in ((B, H, N, d), kv_shape, kv_shape)]
 
 
 def random_case(B, H, N, d, seed, dtype=torch.bfloat16, std=1.0, H_kv=None):
