@@ -516,16 +516,157 @@ def run_decode(args, w):
     print(json.dumps(line))
 
 
+# ------------------------------------------------------------- FP8 forward --
+
+FP8_METRIC = "attention fwd TFLOPS (E4M3 Q, K, V; bf16 O) & % of GB300 dense FP8 peak"
+FP8_NOMINAL_RATIO = 2.0   # dense FP8 / dense BF16 tensor throughput (4.5 / 2.25 PFLOP/s)
+
+
+def _fp8_kw(inp):
+    return dict(scale=inp["scale"], causal=inp["causal"], q_descale=inp["q_descale"],
+                k_descale=inp["k_descale"], v_descale=inp["v_descale"])
+
+
+def measure_fp8(ea, w, dev, steps, warmup):
+    """Device-timed forward steps (V transpose + fused forward, one attn_fwd
+    call) over input sets that rotate so each step misses the L2, then the
+    e2e leg: Q, K, V up from pinned host memory and O down, every step."""
+    inp = workloads.make_inputs(w)
+    kw = _fp8_kw(inp)
+
+    def make_set():
+        q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+        o, lse = ea.attention_fwd(q, k, v, **kw)
+        return q, k, v, o, lse
+
+    first = make_set()
+    nbytes = sum(t.numel() * t.element_size() for t in first) + \
+        w.B * w.kv_heads * w.d * ((w.N + 127) // 128 * 128)
+    nsets = max(1, min(8, math.ceil(2 * L2_BYTES / nbytes)))
+    sets = [first] + [make_set() for _ in range(nsets - 1)]
+    ws = ea.workspace(dev, 0)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(warmup):
+        q, k, v, o, lse = sets[i % nsets]
+        ea.attention_fwd(q, k, v, out=o, lse=lse, **kw)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.__enter__()
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        q, k, v, o, lse = sets[i % nsets]
+        ea.attention_fwd(q, k, v, out=o, lse=lse, **kw)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.__exit__()
+    ea.check(ws, dev)
+    ms = start.elapsed_time(end) / steps
+    # e2e
+    host = [inp[n].pin_memory() for n in ("q", "k", "v")]
+    q, k, v, o, lse = first
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+
+    def e2e_step():
+        for d, h in zip((q, k, v), host):
+            d.copy_(h, non_blocking=True)
+        ea.attention_fwd(q, k, v, out=o, lse=lse, **kw)
+        ho.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    n_e2e = max(3, min(steps, 100))
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_ms = (time.perf_counter() - t0) / n_e2e * 1e3
+    return dict(inp=inp, ms=ms, e2e_ms=e2e_ms, clocks=sampler.summary(), nsets=nsets,
+                resident=nbytes, h2d=sum(h.numel() * h.element_size() for h in host),
+                d2h=ho.numel() * ho.element_size())
+
+
+def run_fp8(args, w):
+    """The FP8 forward: fwd TFLOPS against the FP8 tensor peak (the measured
+    BF16 peak times the nominal FP8/BF16 ratio), oracle timed beside it."""
+    import numpy as np
+    from oracle import fp8 as oracle_fp8
+    inp_cpu = workloads.make_inputs(w)
+    ds = (inp_cpu["q_descale"], inp_cpu["k_descale"], inp_cpu["v_descale"])
+    t0 = time.perf_counter()
+    done, flops_cpu = 0, 0.0
+    grp = w.H // w.kv_heads
+    for h in range(w.H):
+        codes = [inp_cpu[n][:, sl].view(torch.uint8).numpy() for n, sl in
+                 (("q", slice(h, h + 1)), ("k", slice(h // grp, h // grp + 1)),
+                  ("v", slice(h // grp, h // grp + 1)))]
+        oracle_fp8.fp8_forward(*codes, *ds, inp_cpu["scale"], causal=w.causal)
+        flops_cpu += fwd_flops(workloads.get(w.name, H=1, H_kv=1))
+        done += 1
+        if time.perf_counter() - t0 > args.cpu_budget:
+            break
+    dt_cpu = time.perf_counter() - t0
+    del inp_cpu
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import exact_attention_12_gb300 as ea
+    from exact_attention_12_gb300 import build
+    build.build()
+    r = measure_fp8(ea, w, dev, args.steps, args.warmup)
+    flops = fwd_flops(w)
+    burst, _, _, src = peaks()
+    peak = FP8_NOMINAL_RATIO * burst
+    tflops = flops / (r["ms"] * 1e-3) / 1e12
+    line = {
+        "metric": FP8_METRIC, "value": tflops, "unit": "TFLOPS", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {"workload": describe(w), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "parallelism": "single GPU",
+                   "l2": f"inputs rotate over {r['nsets']} resident sets of "
+                         f"{r['resident'] / 2**20:.0f} MiB (> 2x the 129 MB L2)"},
+        "roofline": {"kernel": "fwd_fp8_kernel", "bound": "tensor", "achieved": tflops,
+                     "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                     "peak_source": f"bf16_tflops ({src}) x {FP8_NOMINAL_RATIO} "
+                                    f"(nominal dense FP8 / BF16)",
+                     "timed": "the attn_fwd call: V transpose + fused forward",
+                     "traffic": None},
+        "gpu_launches": 2 * args.steps,
+        "clocks": r["clocks"],
+        "cpu_baseline": {"value": flops_cpu / dt_cpu / 1e12, "unit": "TFLOPS",
+                         "cores": _blas_threads(), "kind": "oracle",
+                         "sample": f"{done} of {w.H} heads of {w.name}, fp64 numpy forward, "
+                                   f"{dt_cpu:.1f} s"},
+        "e2e": {"value": flops / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOPS",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "ms_per_step": r["e2e_ms"]},
+    }
+    print(json.dumps(line))
+
+
 # ------------------------------------------------------------- profiling --
 
 def profile_steps(w, n):
     """`n` forward + backward steps of one resident input set, four kernel
-    launches each (six with a block mask), then a status check."""
+    launches each (six with a block mask; two forward-only launches for FP8
+    inputs), then a status check."""
     import exact_attention_12_gb300 as ea
     from exact_attention_12_gb300 import build
     build.build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    if w.dtype == "fp8":   # forward only: V transpose + fused forward per step
+        inp = workloads.make_inputs(w)
+        q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+        for _ in range(n):
+            ea.attention_fwd(q, k, v, **_fp8_kw(inp))
+        torch.cuda.synchronize(dev)
+        ea.check()
+        print(f"profile-steps: {n} steps of {w.name} done")
+        return
     step = Step(ea, workloads.make_inputs(w), dev)
     stream = torch.cuda.current_stream(dev)
     for _ in range(n):
@@ -554,6 +695,13 @@ def main():
 
     if args.profile_steps > 0:
         profile_steps(w, args.profile_steps)
+        return
+    if w.dtype == "fp8":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference",
+                              "unavailable": "the reference arm times the bf16 training step"}))
+        elif int(os.environ.get("RANK", "0")) == 0:
+            run_fp8(args, w)
         return
     if w.decode_n_q:
         if args.impl == "reference":

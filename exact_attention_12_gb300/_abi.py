@@ -18,6 +18,7 @@ ATTN_ERR_WORKSPACE = 5
 
 ATTN_BF16 = 0
 ATTN_FP32 = 1
+ATTN_FP8_E4M3 = 2
 
 # every function the header declares, with its ctypes signature
 EXPORTS = {
@@ -53,6 +54,8 @@ class AttnParams(ctypes.Structure):
         ("H_kv", ctypes.c_int32), ("reserved", ctypes.c_int32),
         ("kv_stride_b", ctypes.c_int64), ("kv_stride_h", ctypes.c_int64),
         ("kv_stride_n", ctypes.c_int64),
+        ("q_descale", ctypes.c_float), ("k_descale", ctypes.c_float),
+        ("v_descale", ctypes.c_float), ("reserved2", ctypes.c_int32),
     ]
 
 

@@ -15,6 +15,9 @@ from . import _abi
 from ._abi import AttnParams, check_status, lib
 
 _DTYPES = {torch.bfloat16: _abi.ATTN_BF16, torch.float32: _abi.ATTN_FP32}
+_FP8 = getattr(torch, "float8_e4m3fn", None)
+if _FP8 is not None:
+    _DTYPES[_FP8] = _abi.ATTN_FP8_E4M3
 _workspaces = {}
 
 
@@ -38,9 +41,10 @@ def _stream(device):
 
 
 def make_params(q, *, k=None, scale=None, causal=False, key_lens=None, dropout_p=0.0, seed=0,
-                offset=0, block_mask=None):
+                offset=0, block_mask=None, q_descale=None, k_descale=None, v_descale=None):
     """Fill `attn_params` from the query tensor, the key tensor (for its head
-    count and strides; None = laid out like q) and the options."""
+    count and strides; None = laid out like q) and the options.  The
+    de-scale factors apply to E4M3 inputs only (None = 1)."""
     if q.dim() != 4:
         raise ValueError("tensors must be [B, H, N, d]")
     B, H, N, d = q.shape
@@ -54,6 +58,9 @@ def make_params(q, *, k=None, scale=None, causal=False, key_lens=None, dropout_p
     p.dropout_p = float(dropout_p)
     p.philox_seed = int(seed) & 0xFFFFFFFFFFFFFFFF
     p.philox_offset = int(offset)
+    p.q_descale = 0.0 if q_descale is None else float(q_descale)
+    p.k_descale = 0.0 if k_descale is None else float(k_descale)
+    p.v_descale = 0.0 if v_descale is None else float(v_descale)
     sb, sh, sn, sd = q.stride()
     if sd != 1 and d > 1:
         raise ValueError("the head dimension must be contiguous")
@@ -114,19 +121,30 @@ def workspace_size(params, backward):
 
 
 def attention_fwd(q, k, v, *, scale=None, causal=False, key_lens=None, dropout_p=0.0, seed=0,
-                  offset=0, block_mask=None, out=None, lse=None, ws=None):
+                  offset=0, block_mask=None, out=None, lse=None, ws=None, q_descale=None,
+                  k_descale=None, v_descale=None):
     """O and the per-row logsumexp L of exact attention (see include/attn.h).
 
     q: [B, H, N, d]; k, v: [B, H_kv, N, d] with H_kv dividing H (grouped-query
-    attention; H_kv = H is multi-head), CUDA tensors (bf16 or fp32); k and v
-    share strides.  Returns (o, lse) with o like q and lse fp32 [B, H, N].
+    attention; H_kv = H is multi-head), CUDA tensors (bf16, fp32, or
+    float8_e4m3fn with the de-scale factors: the real values are
+    descale * tensor); k and v share strides.  Returns (o, lse) with o like q
+    (bf16 for E4M3 inputs) and lse fp32 [B, H, N].
     """
     _check_kv(q, k)
     _same_layout(k, v)
     p = make_params(q, k=k, scale=scale, causal=causal, key_lens=key_lens,
-                    dropout_p=dropout_p, seed=seed, offset=offset, block_mask=block_mask)
-    o = _like(q) if out is None else out
-    _same_layout(q, o)
+                    dropout_p=dropout_p, seed=seed, offset=offset, block_mask=block_mask,
+                    q_descale=q_descale, k_descale=k_descale, v_descale=v_descale)
+    if _FP8 is not None and q.dtype == _FP8:
+        o = torch.empty_strided(q.shape, q.stride(), dtype=torch.bfloat16,
+                                device=q.device) if out is None else out
+        if o.dtype != torch.bfloat16 or o.shape != q.shape or o.stride() != q.stride() \
+                or o.device != q.device:
+            raise ValueError("out must be bf16 with q's shape and strides")
+    else:
+        o = _like(q) if out is None else out
+        _same_layout(q, o)
     B, H, N, _ = q.shape
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)

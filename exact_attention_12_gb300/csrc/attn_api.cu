@@ -39,6 +39,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
   size_t list_cnt = 0, list_idx = 0;   // compacted block mask (0 = none)
+  size_t vt = 0;                       // FP8 forward: V^T [B * H_kv][d][nb * 128]
   size_t lse2 = 0, dsum = 0, dq_acc = 0;   // backward only
   size_t total = 0;
 };
@@ -52,12 +53,17 @@ WsLayout layout(const attn_params* p, bool bwd) {
   size_t off = kHeaderBytes;
   const size_t nb = (static_cast<size_t>(p->N) + kTile - 1) / kTile;
   const size_t bhn = static_cast<size_t>(p->B) * p->H * p->N;
-  if (p->block_mask != nullptr && p->dtype == ATTN_BF16) {
+  if (p->block_mask != nullptr && p->dtype != ATTN_FP32) {
     const size_t masks = static_cast<size_t>(num_masks(p));
     L.list_cnt = off;
     off = round_up(off + masks * nb * sizeof(int32_t), 256);
     L.list_idx = off;
     off = round_up(off + masks * nb * nb * sizeof(uint16_t), 256);
+  }
+  if (p->dtype == ATTN_FP8_E4M3 && !bwd) {
+    L.vt = off;
+    const size_t H_kv = static_cast<size_t>(p->H_kv == 0 ? p->H : p->H_kv);
+    off = round_up(off + static_cast<size_t>(p->B) * H_kv * p->d * nb * kTile, 256);
   }
   if (bwd) {
     const size_t bhpad = static_cast<size_t>(p->B) * p->H * nb * kTile;
@@ -101,10 +107,19 @@ attn_status validate(const attn_params* p, bool bwd) {
                 p->H);
   if (p->d != 64 && p->d != 128)
     return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", p->d);
-  if (p->dtype != ATTN_BF16 && p->dtype != ATTN_FP32)
+  if (p->dtype != ATTN_BF16 && p->dtype != ATTN_FP32 && p->dtype != ATTN_FP8_E4M3)
     return fail(ATTN_ERR_INVALID_ARG, "dtype %d", p->dtype);
   if (bwd && p->dtype != ATTN_BF16)
     return fail(ATTN_ERR_UNSUPPORTED, "backward is implemented for bf16 only");
+  if (p->reserved2 != 0) return fail(ATTN_ERR_INVALID_ARG, "reserved2 field must be 0");
+  if (p->dtype == ATTN_FP8_E4M3) {
+    if (p->d != 128) return fail(ATTN_ERR_UNSUPPORTED, "fp8 forward needs d=128 (got %d)", p->d);
+    if (p->dropout_p != 0.f) return fail(ATTN_ERR_UNSUPPORTED, "fp8 forward without dropout only");
+    const float ds[3] = {p->q_descale, p->k_descale, p->v_descale};
+    for (float x : ds)
+      if (!std::isfinite(x) || x < 0.f)
+        return fail(ATTN_ERR_INVALID_ARG, "fp8 de-scale factors must be finite and >= 0 (0 = 1)");
+  }
   if (!std::isfinite(p->scale) || !(p->scale > 0.f))
     return fail(ATTN_ERR_INVALID_ARG, "scale must be positive and finite (got %g)", p->scale);
   if (!(p->dropout_p >= 0.f && p->dropout_p < 1.f))
@@ -121,7 +136,8 @@ attn_status validate(const attn_params* p, bool bwd) {
     if (num_masks(p) > 65535)
       return fail(ATTN_ERR_UNSUPPORTED, "more than 65535 per-head block masks");
   }
-  const int64_t align = p->dtype == ATTN_BF16 ? 8 : 4;   // elements per 16 bytes
+  // elements per 16 bytes (fp8: 16, which also aligns the bf16 output)
+  const int64_t align = p->dtype == ATTN_BF16 ? 8 : (p->dtype == ATTN_FP32 ? 4 : 16);
   const int64_t st[3] = {p->stride_b, p->stride_h, p->stride_n};
   for (int i = 0; i < 3; ++i) {
     if (st[i] <= 0 || st[i] % align != 0)
@@ -219,6 +235,8 @@ attn_status make_kv_map(CUtensorMap* map, const void* ptr, const attn_params* p)
                   sb, sh, sn, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+float descale_or_one(float x) { return x == 0.f ? 1.f : x; }
+
 attn::MaskArgs mask_args(const attn_params* p, const WsLayout& L, char* ws, bool by_column) {
   attn::MaskArgs m{};
   m.B = p->B;
@@ -300,6 +318,7 @@ attn_status attn_fwd(const attn_params* p, const void* q, const void* k, const v
   a.d = p->d;
   a.scale = p->scale;
   a.scale_log2 = p->scale * kLog2e;
+  a.o_scale = 1.f;
   a.o = o;
   a.lse = lse;
   a.stride_b = p->stride_b;
@@ -317,16 +336,45 @@ attn_status attn_fwd(const attn_params* p, const void* q, const void* k, const v
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "forward (fp32) launch");
   }
   attn::TensorMaps tm{};
-  if ((st = make_bf16_map(&tm.q, q, p)) != ATTN_OK) return st;
-  if ((st = make_kv_map(&tm.k, k, p)) != ATTN_OK) return st;
-  if ((st = make_kv_map(&tm.v, v, p)) != ATTN_OK) return st;
+  const bool fp8 = p->dtype == ATTN_FP8_E4M3;
+  const int npad = a.m.nb * kTile;
+  if (fp8) {
+    // E4M3 q, k with 128 x 128-byte boxes; v goes through V^T in the workspace
+    int64_t sb, sh, sn;
+    kv_strides(p, &sb, &sh, &sn);
+    const int H_kv = kv_heads(p);
+    if ((st = make_map(&tm.q, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p->B, p->H, p->N, p->d,
+                       p->stride_b, p->stride_h, p->stride_n, kTile, kTile,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK)
+      return st;
+    if ((st = make_map(&tm.k, k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p->B, H_kv, p->N, p->d, sb,
+                       sh, sn, kTile, kTile, CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK)
+      return st;
+    // V^T [B, H_kv, d, N]: rows of npad keys, N of them valid (the rest read as 0)
+    const int64_t dn = static_cast<int64_t>(p->d) * npad;
+    if ((st = make_map(&tm.v, w + L.vt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p->B, H_kv, p->d, p->N,
+                       static_cast<int64_t>(H_kv) * dn, dn, npad, kTile, kTile,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK)
+      return st;
+    const float qs = descale_or_one(p->q_descale), ks = descale_or_one(p->k_descale);
+    a.scale = p->scale * qs * ks;
+    a.scale_log2 = a.scale * kLog2e;
+    a.o_scale = descale_or_one(p->v_descale);
+    e = attn::launch_fp8_transpose_v(static_cast<const uint8_t*>(v), sb, sh, sn, p->B, H_kv, p->N,
+                                     p->d, npad, reinterpret_cast<uint8_t*>(w + L.vt), s);
+    if (e != cudaSuccess) return cuda_fail(e, "fp8 V transpose launch");
+  } else {
+    if ((st = make_bf16_map(&tm.q, q, p)) != ATTN_OK) return st;
+    if ((st = make_kv_map(&tm.k, k, p)) != ATTN_OK) return st;
+    if ((st = make_kv_map(&tm.v, v, p)) != ATTN_OK) return st;
+  }
   if (p->block_mask != nullptr) {
     e = attn::launch_compact_mask(p->block_mask, p->block_mask_head_stride, num_masks(p), a.m.nb,
                                   0, reinterpret_cast<int32_t*>(w + L.list_cnt),
                                   reinterpret_cast<uint16_t*>(w + L.list_idx), s);
     if (e != cudaSuccess) return cuda_fail(e, "block-mask compaction launch");
   }
-  e = attn::launch_fwd_bf16(tm, a, s);
+  e = fp8 ? attn::launch_fwd_fp8(tm, a, s) : attn::launch_fwd_bf16(tm, a, s);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "forward launch");
 }
 

@@ -49,12 +49,14 @@ namespace {
 
 constexpr float kLn2 = 0.693147180559945309f;
 
-template <int D, bool DROPOUT = false>
+template <int D, bool DROPOUT = false, bool FP8 = false>
 struct FwdCfg {
-  static constexpr int kBoxes = D / 64;               // 64-column TMA boxes per tile
+  static constexpr int kElem = FP8 ? 1 : 2;           // bytes per operand element
+  static constexpr int kBoxCols = 128 / kElem;        // elements per 128-byte box row
+  static constexpr int kBoxes = D * kElem / 128;      // 128-byte-wide TMA boxes per tile
   static constexpr int kBoxBytes = kTile * 128;       // 128 rows x 128 bytes
-  static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kTileBytes = kTile * D * kElem;
+  static constexpr int kStages = (D == 64 || FP8) ? 4 : 2;
   // dropout keep masks: per query tile a ring of kMaskStages 128 x 128-bit tiles
   static constexpr int kMaskStages = 2;
   static constexpr int kMaskTileBytes = kTile * 16;
@@ -176,32 +178,49 @@ struct PairWalk {
   }
 };
 
-template <int D>
+// S = Q K^T: both operands K-major; one instruction per 32 bytes of d
+// (16 bf16 or 32 E4M3 elements).
+template <int D, bool FP8>
 __device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint32_t q_base, uint32_t k_base) {
-  constexpr uint32_t kId = idesc_bf16(128, 128, false, false);
+  constexpr int kSteps = D * FwdCfg<D, false, FP8>::kElem / 32;
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
+  for (int kk = 0; kk < kSteps; ++kk) {
     const uint32_t off = (kk >> 2) * FwdCfg<D>::kBoxBytes + (kk & 3) * 32;
-    mma_ss(d_tmem, smem_desc(q_base + off, 16, 1024), smem_desc(k_base + off, 16, 1024), kId,
-           kk > 0 ? 1u : 0u);
+    const uint64_t da = smem_desc(q_base + off, 16, 1024), db = smem_desc(k_base + off, 16, 1024);
+    if constexpr (FP8)
+      mma_ss_f8(d_tmem, da, db, idesc_e4m3(128, 128, false, false), kk > 0 ? 1u : 0u);
+    else
+      mma_ss(d_tmem, da, db, idesc_bf16(128, 128, false, false), kk > 0 ? 1u : 0u);
   }
 }
 
-template <int D>
+// O (+)= P V with P in TMEM.  bf16: V [keys, d] is the MN-major B operand,
+// 16 keys per instruction.  E4M3: the B operand is the transposed tile V^T
+// [d, keys] (K-major), 32 keys per instruction; P holds four keys per column.
+template <int D, bool FP8>
 __device__ __forceinline__ void mma_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_base,
                                        bool accumulate) {
-  constexpr uint32_t kId = idesc_bf16(128, D, false, true);
+  if constexpr (FP8) {
+    constexpr uint32_t kId = idesc_e4m3(128, D, false, false);
 #pragma unroll
-  for (int kk = 0; kk < kTile / 16; ++kk)
-    mma_ts(o_tmem, p_tmem + kk * 8, smem_desc(v_base + kk * 2048, FwdCfg<D>::kBoxBytes, 1024),
-           kId, (accumulate || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < kTile / 32; ++kk)
+      mma_ts_f8(o_tmem, p_tmem + kk * 8, smem_desc(v_base + kk * 32, 16, 1024), kId,
+                (accumulate || kk > 0) ? 1u : 0u);
+  } else {
+    constexpr uint32_t kId = idesc_bf16(128, D, false, true);
+#pragma unroll
+    for (int kk = 0; kk < kTile / 16; ++kk)
+      mma_ts(o_tmem, p_tmem + kk * 8, smem_desc(v_base + kk * 2048, FwdCfg<D>::kBoxBytes, 1024),
+             kId, (accumulate || kk > 0) ? 1u : 0u);
+  }
 }
 
-template <int D, bool DROPOUT>
-__global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
-    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
-  using C = FwdCfg<D, DROPOUT>;
+// The forward of one CTA.  FP8: q, k are E4M3 [B,H,N,d] / [B,H_kv,N,d] maps
+// with 128 x 128-byte boxes and tv maps the transposed V^T [B,H_kv,d,N].
+template <int D, bool DROPOUT, bool FP8>
+__device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMap& tk,
+                                         const CUtensorMap& tv, const FwdArgs& a) {
+  using C = FwdCfg<D, DROPOUT, FP8>;
   constexpr int ST = C::kStages;
   constexpr int MS = C::kMaskStages;
   extern __shared__ uint8_t smem_raw[];
@@ -315,9 +334,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
         mbar_arrive_expect_tx(&ctl.qfull, 2 * C::kTileBytes);
 #pragma unroll
         for (int x = 0; x < C::kBoxes; ++x) {
-          tma_load_4d(sQ + x * C::kBoxBytes, &tq, &ctl.qfull, x * 64, 2 * u.pair * kTile, u.h,
-                      u.b);
-          tma_load_4d(sQ + C::kTileBytes + x * C::kBoxBytes, &tq, &ctl.qfull, x * 64,
+          tma_load_4d(sQ + x * C::kBoxBytes, &tq, &ctl.qfull, x * C::kBoxCols,
+                      2 * u.pair * kTile, u.h, u.b);
+          tma_load_4d(sQ + C::kTileBytes + x * C::kBoxBytes, &tq, &ctl.qfull, x * C::kBoxCols,
                       (2 * u.pair + 1) * kTile, u.h, u.b);
         }
         ++kw;
@@ -335,11 +354,15 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
           mbar_arrive_expect_tx(&ctl.kfull[s], C::kTileBytes);
 #pragma unroll
           for (int x = 0; x < C::kBoxes; ++x)
-            tma_load_4d(dk + x * C::kBoxBytes, &tk, &ctl.kfull[s], x * 64, kv0, hk, u.b);
+            tma_load_4d(dk + x * C::kBoxBytes, &tk, &ctl.kfull[s], x * C::kBoxCols, kv0, hk, u.b);
           mbar_arrive_expect_tx(&ctl.vfull[s], C::kTileBytes);
+          if constexpr (FP8) {   // V^T: d rows of 128 keys
+            tma_load_4d(dv, &tv, &ctl.vfull[s], kv0, 0, hk, u.b);
+          } else {
 #pragma unroll
-          for (int x = 0; x < C::kBoxes; ++x)
-            tma_load_4d(dv + x * C::kBoxBytes, &tv, &ctl.vfull[s], x * 64, kv0, hk, u.b);
+            for (int x = 0; x < C::kBoxes; ++x)
+              tma_load_4d(dv + x * C::kBoxBytes, &tv, &ctl.vfull[s], x * 64, kv0, hk, u.b);
+          }
           ++t;
         }
       }
@@ -397,7 +420,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
               tc_fence_after();
               ++cs_issued[x];
             }
-            mma_scores<D>(tmem + C::kSCol + 128 * x, q_base(x), smem_u32(sK + (t % ST) * C::kTileBytes));
+            mma_scores<D, FP8>(tmem + C::kSCol + 128 * x, q_base(x), smem_u32(sK + (t % ST) * C::kTileBytes));
             mma_commit(&ctl.sfull[x]);
           }
         if (!ok) break;
@@ -433,7 +456,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
                   !(ok = k_next_ready = mbar_wait(&ctl.kfull[s1], ((t + 1) / ST) & 1, wc, kSiteFwdK)))
                 break;
               tc_fence_after();
-              mma_scores<D>(tmem + C::kSCol + 128 * x, q_base(x), smem_u32(sK + s1 * C::kTileBytes));
+              mma_scores<D, FP8>(tmem + C::kSCol + 128 * x, q_base(x), smem_u32(sK + s1 * C::kTileBytes));
               mma_commit(&ctl.sfull[x]);
               ++cs_issued[x];
             }
@@ -447,7 +470,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
               if (ok && !v_ready) ok = v_ready = mbar_wait(&ctl.vfull[s], (t / ST) & 1, wc, kSiteFwdV);
               if (!ok) break;
               tc_fence_after();
-              mma_pv<D>(tmem + C::kOCol + D * x, tmem + C::kPCol + 64 * x,
+              mma_pv<D, FP8>(tmem + C::kOCol + D * x, tmem + C::kPCol + 64 * x,
                         smem_u32(sV + s * C::kTileBytes), !first[x]);
               mma_commit(&ctl.pvdone[x]);
               first[x] = false;
@@ -464,7 +487,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
                 if (ok && !v_ready) ok = v_ready = mbar_wait(&ctl.vfull[s], (t / ST) & 1, wc, kSiteFwdV);
                 if (!ok) break;
                 tc_fence_after();
-                mma_pv<D>(tmem + C::kOCol + D * x, tmem + C::kSCol + 128 * x,
+                mma_pv<D, FP8>(tmem + C::kOCol + D * x, tmem + C::kSCol + 128 * x,
                           smem_u32(sV + s * C::kTileBytes), !first[x]);
                 first[x] = false;
                 ++cnt[x];
@@ -476,7 +499,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
                   if (!ok) break;
                   tc_fence_after();
                 }
-                mma_scores<D>(tmem + C::kSCol + 128 * x, q_base(x), smem_u32(sK + s1 * C::kTileBytes));
+                mma_scores<D, FP8>(tmem + C::kSCol + 128 * x, q_base(x), smem_u32(sK + s1 * C::kTileBytes));
                 mma_commit(&ctl.sfull[x]);
               }
             }
@@ -633,7 +656,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
           }
         }
         // P = 2^(S c2 - m c2) (masked entries are -inf: 2^-inf = 0), bf16 over
-        // the first 64 columns of S
+        // the first 64 columns of S (E4M3: the first 32)
         const float mc = (m_used == -INFINITY) ? 0.f : m_used * c2;
         const uint64_t c2x2 = f2_pack(c2, c2), nmc2 = f2_pack(-mc, -mc);
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
@@ -671,10 +694,16 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
               p2 = ((keep >> (t + 2)) & 1u) ? p2 : 0.f;
               p3 = ((keep >> (t + 3)) & 1u) ? p3 : 0.f;
             }
-            pk[t / 2] = pack_bf16x2(p0, p1);
-            pk[t / 2 + 1] = pack_bf16x2(p2, p3);
+            if constexpr (FP8) {
+              pk[t / 4] = pack_e4m3x4(p0, p1, p2, p3);
+            } else {
+              pk[t / 2] = pack_bf16x2(p0, p1);
+              pk[t / 2 + 1] = pack_bf16x2(p2, p3);
+            }
           }
-          if constexpr (C::kSepP)
+          if constexpr (FP8)
+            tmem_st8(sc + c / 4, pk);
+          else if constexpr (C::kSepP)
             tmem_st16(pc + c / 2, pk);
           else
             tmem_st16(sc + c / 2, pk);   // S columns [c/2, c/2+16) are already in registers
@@ -698,7 +727,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
       }
       if (q0 < m.N) {
         const bool live = l_sum > 0.f;
-        const float inv = live ? m.drop_scale / l_sum : 0.f;
+        const float inv = live ? a.o_scale * (m.drop_scale / l_sum) : 0.f;
         const float L = live ? (m_used * c2 + __log2f(l_sum)) * kLn2 : -INFINITY;
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) + b * a.stride_b + h * a.stride_h +
                               static_cast<int64_t>(qi) * a.stride_n;
@@ -742,17 +771,35 @@ __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
   }
 }
 
-template <int D, bool DROP>
+template <int D, bool DROPOUT>
+__global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
+    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
+  fwd_body<D, DROPOUT, false>(tq, tk, tv, a);
+}
+
+template <int D>
+__global__ void __launch_bounds__(FwdCfg<D, false, true>::kThreads, 1)
+    fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tvt, const FwdArgs a) {
+  fwd_body<D, false, true>(tq, tk, tvt, a);
+}
+
+template <int D, bool DROP, bool FP8>
 cudaError_t launch_one(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
-  using C = FwdCfg<D, DROP>;
+  using C = FwdCfg<D, DROP, FP8>;
+  auto kernel = [] {
+    if constexpr (FP8) return fwd_fp8_kernel<D>;
+    else return fwd_bf16_kernel<D, DROP>;
+  }();
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, DROP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmem);
     if (e != cudaSuccess) return e;
     // the register re-split inside the kernel assumes the launch allocation
     cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, fwd_bf16_kernel<D, DROP>)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, kernel)) != cudaSuccess) return e;
     if (static_cast<uint32_t>(fa.numRegs) < C::kRegsLaunch) return cudaErrorInvalidConfiguration;
     attr_set = true;
   }
@@ -763,16 +810,72 @@ cudaError_t launch_one(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const long long units = static_cast<long long>((a.m.nb + 1) / 2) * a.m.B * a.m.H;
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
-  fwd_bf16_kernel<D, DROP><<<grid, C::kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, a);
+  kernel<<<grid, C::kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, a);
   return cudaGetLastError();
+}
+
+// V [B, H_kv, N, d] E4M3 -> V^T [B * H_kv][d][npad]: one CTA per 64 keys of
+// one head; keys past N are written as zeros.
+constexpr int kTrKeys = 64;
+
+template <int D>
+__global__ void __launch_bounds__(256) fp8_transpose_v_kernel(const uint8_t* __restrict__ v,
+                                                              int64_t sb, int64_t sh, int64_t sn,
+                                                              int H_kv, int N, int npad,
+                                                              uint8_t* __restrict__ vt) {
+  __shared__ uint8_t tile[kTrKeys][D + 16];
+  const int bh = blockIdx.y, b = bh / H_kv, h = bh - b * H_kv;
+  const int k0 = blockIdx.x * kTrKeys;
+  const uint8_t* src = v + b * sb + h * sh;
+  constexpr int kRowVecs = D / 16;   // 16-byte vectors per key row
+  for (int i = threadIdx.x; i < kTrKeys * kRowVecs; i += blockDim.x) {
+    const int r = i / kRowVecs, c = (i % kRowVecs) * 16;
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (k0 + r < N) x = *reinterpret_cast<const uint4*>(src + static_cast<int64_t>(k0 + r) * sn + c);
+    uint32_t* t = reinterpret_cast<uint32_t*>(&tile[r][c]);
+    t[0] = x.x;
+    t[1] = x.y;
+    t[2] = x.z;
+    t[3] = x.w;
+  }
+  __syncthreads();
+  uint8_t* dst = vt + static_cast<int64_t>(bh) * D * npad;
+  constexpr int kColVecs = kTrKeys / 16;   // 16-byte vectors per output row
+  for (int i = threadIdx.x; i < D * kColVecs; i += blockDim.x) {
+    const int c = i / kColVecs, r0 = (i % kColVecs) * 16;
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      w[q] = static_cast<uint32_t>(tile[r0 + 4 * q][c]) |
+             (static_cast<uint32_t>(tile[r0 + 4 * q + 1][c]) << 8) |
+             (static_cast<uint32_t>(tile[r0 + 4 * q + 2][c]) << 16) |
+             (static_cast<uint32_t>(tile[r0 + 4 * q + 3][c]) << 24);
+    *reinterpret_cast<uint4*>(dst + static_cast<int64_t>(c) * npad + k0 + r0) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
   const bool drop = a.m.drop_threshold != 0;
-  if (a.d == 64) return drop ? launch_one<64, true>(tm, a, s) : launch_one<64, false>(tm, a, s);
-  return drop ? launch_one<128, true>(tm, a, s) : launch_one<128, false>(tm, a, s);
+  if (a.d == 64)
+    return drop ? launch_one<64, true, false>(tm, a, s) : launch_one<64, false, false>(tm, a, s);
+  return drop ? launch_one<128, true, false>(tm, a, s) : launch_one<128, false, false>(tm, a, s);
+}
+
+cudaError_t launch_fp8_transpose_v(const uint8_t* v, int64_t sb, int64_t sh, int64_t sn, int B,
+                                   int H_kv, int N, int d, int npad, uint8_t* vt, cudaStream_t s) {
+  if (d != 128) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>((npad + kTrKeys - 1) / kTrKeys),
+                  static_cast<unsigned>(B * H_kv));
+  fp8_transpose_v_kernel<128><<<grid, 256, 0, s>>>(v, sb, sh, sn, H_kv, N, npad, vt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_fp8(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
+  if (a.d != 128 || a.m.drop_threshold != 0) return cudaErrorInvalidValue;
+  return launch_one<128, false, true>(tm, a, s);
 }
 
 }  // namespace attn

@@ -57,7 +57,8 @@ struct FwdArgs {
   MaskArgs m;
   int d;
   float scale;                    // c
-  float scale_log2;               // c * log2(e)
+  float scale_log2;               // c * log2(e) (FP8: times q_descale * k_descale)
+  float o_scale;                  // factor on O: 1, or v_descale for FP8 inputs
   void* o;                        // [B,H,N,d]
   float* lse;                     // [B,H,N]
   int64_t stride_b, stride_h, stride_n;            // q, o
@@ -113,6 +114,11 @@ struct TensorMaps {
 
 // Launchers (return the cudaGetLastError() of their launches).
 cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s);
+// E4M3 forward (d = 128, no dropout); tm.v maps V^T [B, H_kv, d, N] with
+// 128 x 128-byte boxes, written by launch_fp8_transpose_v.
+cudaError_t launch_fwd_fp8(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_fp8_transpose_v(const uint8_t* v, int64_t sb, int64_t sh, int64_t sn, int B,
+                                   int H_kv, int N, int d, int npad, uint8_t* vt, cudaStream_t s);
 cudaError_t launch_fwd_fp32(const float* q, const float* k, const float* v, const FwdArgs& a,
                             cudaStream_t s);
 cudaError_t launch_compact_mask(const uint8_t* mask, int64_t head_stride, int masks, int nb,

@@ -77,13 +77,15 @@ typedef enum {
   ATTN_ERR_WORKSPACE = 5      /* workspace missing, misaligned or too small */
 } attn_status;
 
-typedef enum { ATTN_BF16 = 0, ATTN_FP32 = 1 } attn_dtype;
+typedef enum { ATTN_BF16 = 0, ATTN_FP32 = 1, ATTN_FP8_E4M3 = 2 } attn_dtype;
 
 typedef struct attn_params {
   int32_t B, H, N, d;        /* batch, heads, sequence length, head dim.
                                 d in {64, 128}.  B, H or N = 0: no work. */
   int32_t dtype;             /* attn_dtype.  bf16: forward and backward;
-                                fp32: forward only. */
+                                fp32: forward only; fp8 (E4M3 q, k, v with
+                                the de-scale factors below, bf16 o):
+                                forward only, d = 128, no dropout. */
   float scale;               /* score scale, e.g. 1/sqrt(d); finite */
   int32_t causal;            /* nonzero: keep j <= i (top-left aligned) */
   float dropout_p;           /* drop probability in [0, 1); 0 = no dropout */
@@ -111,6 +113,22 @@ typedef struct attn_params {
   int64_t kv_stride_b, kv_stride_h, kv_stride_n; /* element strides of k, v,
                                 dk, dv; all three 0 = the strides above
                                 (then H_kv must equal H) */
+  /* FP8 inputs (dtype ATTN_FP8_E4M3).  The FlashAttention explainer
+   * (azimuth.plus, timeline entry "FlashAttention-3") names FP8 as the
+   * Hopper successor's step to higher throughput; the format is E4M3 of the
+   * OCP 8-bit floating point specification (bias 7, largest value 448, no
+   * infinities).  The attention is that of the real values
+   *   Q = q_descale * q,  K = k_descale * k,  V = v_descale * v,
+   * so the scores are scale * q_descale * k_descale * (q k^T).  The kernel
+   * rounds the probabilities to E4M3 for the P V product (the row sums
+   * that normalise O are taken before rounding), so O carries an error of
+   * at most 2^-4 * sum_j P_ij |V_jc| + 2^-10 * max_j P_ij * sum_j |V_jc|
+   * beyond the bf16 rounding of O; L is exact up to fp32 arithmetic.
+   * o is bf16 [B, H, N, d] with the query strides.  Strides are in
+   * elements and must be multiples of 16.  0 means 1 for each factor;
+   * ignored for the other dtypes. */
+  float q_descale, k_descale, v_descale;
+  int32_t reserved2;         /* must be 0 */
 } attn_params;
 
 /* Bytes of device workspace a forward (for_backward = 0) or backward
@@ -118,7 +136,9 @@ typedef struct attn_params {
  * (the call itself then reports why). */
 size_t attn_workspace_size(const attn_params* p, int for_backward);
 
-/* Forward: O [B,H,N,d] (same dtype as q) and lse [B,H,N] fp32. */
+/* Forward: O [B,H,N,d] (same dtype as q; bf16 for fp8 inputs) and lse
+ * [B,H,N] fp32.  For fp8 the workspace also holds a transposed copy of v
+ * ([B, H_kv, d, N] padded to a multiple of 128 keys), written by the call. */
 attn_status attn_fwd(const attn_params* p, const void* q, const void* k,
                      const void* v, void* o, float* lse, void* ws,
                      size_t ws_bytes, void* stream);

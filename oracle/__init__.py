@@ -44,4 +44,4 @@ from .attention import (  # noqa: F401
     keep_scale,
     keep_mask,
 )
-from .fp8 import e4m3_value, fp8_forward, rounding_terms  # noqa: F401
+from .fp8 import e4m3_value, fp8_forward, rounding_terms, rounding_terms_rows  # noqa: F401

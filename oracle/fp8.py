@@ -57,6 +57,36 @@ def fp8_forward(q8, k8, v8, q_descale, k_descale, v_descale, scale, causal=False
                              block_mask=block_mask)
 
 
+def rounding_terms_rows(q, k, v, b, h, rows, scale, causal=False, key_lens=None,
+                        block_mask=None):
+    """The terms of `rounding_terms` for the query rows `rows` of head (b, h)
+    only: (A, T), each [len(rows), d].  q, k, v: real values, [B,H,N,d] and
+    [B,H_kv,N,d]."""
+    N, d = np.shape(q)[2], np.shape(q)[3]
+    g = _group(q, k)
+    c = float(np.float32(scale))
+    rows = np.asarray(rows, dtype=np.int64)
+    kl = None if key_lens is None else int(np.asarray(key_lens)[b])
+    bm = None
+    if block_mask is not None:
+        bm = np.asarray(block_mask)
+        bm = bm if bm.ndim == 2 else bm[b, h]
+    allow = allowed_mask(rows, np.arange(N), causal, kl, bm)
+    qh = np.asarray(q[b, h], dtype=np.float64)[rows]
+    kh = np.asarray(k[b, h // g], dtype=np.float64)
+    vh = np.abs(np.asarray(v[b, h // g], dtype=np.float64))
+    A = np.zeros((rows.size, d))
+    T = np.zeros((rows.size, d))
+    live = allow.any(axis=1)
+    if live.any():
+        S = np.where(allow[live], c * (qh[live] @ kh.T), -np.inf)
+        E = np.exp(S - S.max(axis=1, keepdims=True))
+        l0 = E.sum(axis=1, keepdims=True)
+        A[live] = (E / l0) @ vh
+        T[live] = (allow[live].astype(np.float64) @ vh) / l0
+    return A, T
+
+
 def rounding_terms(q, k, v, scale, causal=False, key_lens=None, block_mask=None):
     """Per output element (b, h, i, c), the two sums the E4M3 rounding of the
     probabilities is bounded by.  q, k, v are real (de-scaled) values.
@@ -72,32 +102,11 @@ def rounding_terms(q, k, v, scale, causal=False, key_lens=None, block_mask=None)
     most 2^-4 A + 2^-10 T: max_j P_ij = exp(m_i - L_i) = 1 / sum_j exp(S_ij - m_i).
     Rows with no allowed key get 0.
     """
-    q = np.asarray(q, dtype=np.float64)
-    k = np.asarray(k, dtype=np.float64)
-    v = np.asarray(v, dtype=np.float64)
-    B, H, N, d = q.shape
-    g = _group(q, k)
-    c = float(np.float32(scale))
+    B, H, N, d = np.shape(q)
     A = np.zeros((B, H, N, d))
     T = np.zeros((B, H, N, d))
-    rows = np.arange(N)
     for b in range(B):
-        kl = None if key_lens is None else int(np.asarray(key_lens)[b])
         for h in range(H):
-            bm = None
-            if block_mask is not None:
-                bm = np.asarray(block_mask)
-                bm = bm if bm.ndim == 2 else bm[b, h]
-            allow = allowed_mask(rows, rows, causal, kl, bm)
-            qh, kh, vh = q[b, h], k[b, h // g], np.abs(v[b, h // g])
-            S = np.where(allow, c * (qh @ kh.T), -np.inf)
-            live = allow.any(axis=1)
-            if not live.any():
-                continue
-            Sl = S[live]
-            m = Sl.max(axis=1, keepdims=True)
-            E = np.exp(Sl - m)
-            l0 = E.sum(axis=1, keepdims=True)
-            A[b, h, live] = (E / l0) @ vh
-            T[b, h, live] = (allow[live].astype(np.float64) @ vh) / l0
+            A[b, h], T[b, h] = rounding_terms_rows(q, k, v, b, h, np.arange(N), scale,
+                                                   causal, key_lens, block_mask)
     return A, T

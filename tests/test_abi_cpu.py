@@ -51,7 +51,7 @@ def test_params_struct_layout(abi, tmp_path):
     inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
     subprocess.check_call(["gcc", "-std=c11", "-I", inc, str(src), "-o", str(exe)])
     got = dict(line.split() for line in subprocess.check_output([str(exe)], text=True).splitlines())
-    assert int(got["size"]) == ctypes.sizeof(p) == 128
+    assert int(got["size"]) == ctypes.sizeof(p) == 144
     for n in names:
         assert int(got[n]) == getattr(p, n).offset, n
 
@@ -81,6 +81,31 @@ def test_invalid_arguments_are_rejected_on_the_host(abi, field, value, status):
     st = lib.attn_fwd(ctypes.byref(p), fake, fake, fake, fake, fake, fake, 1 << 20, None)
     assert st == status, lib.attn_last_error()
     assert lib.attn_last_error()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=64), 2), (dict(d=128, dropout_p=0.1), 2), (dict(d=128, q_descale=-1.0), 1),
+    (dict(d=128, v_descale=float("nan")), 1), (dict(d=128, stride_n=136), 1),
+    (dict(d=128, reserved2=1), 1),
+])
+def test_fp8_forward_options_checked_on_the_host(abi, kw, status):
+    lib = abi.lib()
+    base = dict(dtype=abi.ATTN_FP8_E4M3, stride_b=3 * 256 * 128, stride_h=256 * 128,
+                stride_n=128)
+    base.update(kw)
+    p = _params(abi, **base)
+    fake = ctypes.c_void_p(0x1000)
+    st = lib.attn_fwd(ctypes.byref(p), fake, fake, fake, fake, fake, fake, 1 << 30, None)
+    assert st == status, lib.attn_last_error()
+
+
+def test_fp8_workspace_holds_the_transposed_values(abi):
+    lib = abi.lib()
+    p = _params(abi, dtype=abi.ATTN_FP8_E4M3, d=128, N=200, stride_b=3 * 200 * 128,
+                stride_h=200 * 128, stride_n=128)
+    # header + V^T [B * H][d][256 keys] bytes
+    assert lib.attn_workspace_size(ctypes.byref(p), 0) == 256 + 2 * 3 * 128 * 256
+    assert lib.attn_workspace_size(ctypes.byref(p), 1) == 0       # no fp8 backward
 
 
 def test_fp32_backward_is_unsupported(abi):

@@ -693,3 +693,12 @@ def test_rounding_bound_holds_for_simulated_e4m3_probabilities():
         wr = grid[np.abs(grid[None, :] - w[:, None]).argmin(axis=1)]
         o = (wr @ v[0, 0, : i + 1]) / w.sum()
         assert np.all(np.abs(o - O[0, 0, i]) <= 2.0 ** -4 * A_[0, 0, i] + 2.0 ** -10 * T_[0, 0, i] + 1e-12)
+
+
+def test_rounding_terms_rows_match_the_full_evaluation():
+    q, k, v = _rand((2, 4, 20, 3), 12), _rand((2, 2, 20, 3), 13), _rand((2, 2, 20, 3), 14)
+    A_, T_ = F.rounding_terms(q, k, v, 0.5, causal=True, key_lens=[20, 7])
+    rows = np.array([0, 6, 7, 19])
+    for b, h in [(0, 3), (1, 1)]:
+        a, t = F.rounding_terms_rows(q, k, v, b, h, rows, 0.5, causal=True, key_lens=[20, 7])
+        assert np.allclose(a, A_[b, h, rows], atol=1e-13) and np.allclose(t, T_[b, h, rows], atol=1e-13)
