@@ -652,12 +652,22 @@ def run_fp8(args, w):
 def profile_steps(w, n):
     """`n` forward + backward steps of one resident input set, four kernel
     launches each (six with a block mask; two forward-only launches for FP8
-    inputs), then a status check."""
+    inputs or a decode step), then a status check."""
     import exact_attention_12_gb300 as ea
     from exact_attention_12_gb300 import build
     build.build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    if w.decode_n_q:   # decode steps: split-KV kernel + merge per step
+        inp = workloads.make_inputs(w)
+        q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+        lens = inp["key_lens"].to(dev)
+        for _ in range(n):
+            ea.attention_decode(q, k, v, lens, scale=inp["scale"], causal=w.causal)
+        torch.cuda.synchronize(dev)
+        ea.check()
+        print(f"profile-steps: {n} steps of {w.name} done")
+        return
     if w.dtype == "fp8":   # forward only: V transpose + fused forward per step
         inp = workloads.make_inputs(w)
         q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
