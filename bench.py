@@ -499,7 +499,8 @@ def run_decode(args, w):
                    "parallelism": "single GPU",
                    "l2": f"the resident cache ({nbytes / 2**20:.0f} MiB read per step) is larger "
                          f"than the 129 MB L2"},
-        "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": gbs, "peak": hbm,
+        "roofline": {"kernel": "decode_mma_kernel" if (w.H // w.kv_heads) * w.decode_n_q <= 16
+                     else "decode_kernel", "bound": "hbm", "achieved": gbs, "peak": hbm,
                      "unit": "GB/s", "frac": gbs / hbm, "peak_source": f"hbm_gbs ({src})",
                      "traffic": None},
         "gpu_launches": 2 * args.steps,

@@ -495,16 +495,18 @@ attn_status attn_bwd(const attn_params* p, const void* q, const void* k, const v
 
 namespace {
 
-// Cache keys per split: enough splits that the grid covers every SM about
-// eight times over (short CTAs balance the sequences' different lengths; much
-// shorter ones spend their time in set-up), in multiples of the 64-key tile.
-int decode_chunk(const attn_params* p) {
+// Cache keys per split, in multiples of the 64-key tile: enough splits that
+// the grid covers every SM several times over (short CTAs balance the
+// sequences' different lengths; much shorter ones spend their time in
+// set-up).  The warp-MMA kernel (rows <= 16, two CTAs of four streaming
+// warps per SM) takes chunks twice as long as the FMA kernel.
+int decode_chunk(const attn_params* p, int rows) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 148;
   const int64_t heads = static_cast<int64_t>(p->B) * kv_heads(p);
-  const int64_t want = 8LL * sms;
+  const int64_t want = (rows <= 16 ? 4LL : 8LL) * sms;
   int64_t per = heads > 0 ? (static_cast<int64_t>(p->N) * heads + want - 1) / want : p->N;
   per = (per + 63) / 64 * 64;
   if (per < 256) per = 256;
@@ -532,7 +534,7 @@ struct DecodeLayout {
 
 DecodeLayout decode_layout(const attn_params* p, int32_t n_q) {
   DecodeLayout L;
-  L.chunk = decode_chunk(p);
+  L.chunk = decode_chunk(p, p->H > 0 ? (p->H / kv_heads(p)) * n_q : 1);
   L.splits = p->N > 0 ? (p->N + L.chunk - 1) / L.chunk : 0;
   const size_t rows = static_cast<size_t>(p->B) * p->H * n_q;
   size_t off = kHeaderBytes;

@@ -43,7 +43,10 @@ def _check(ea, q, k, v, lens, causal, kv_dev=None):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("H,H_kv,n_q", [(8, 8, 1), (8, 2, 1), (8, 1, 4), (6, 3, 3)])
+# group rows (H / H_kv) * n_q: 1, 4, 32, 6, 16, 16, 24 -- both sides of the
+# 16-row switch between the warp-MMA and the FMA kernels
+@pytest.mark.parametrize("H,H_kv,n_q", [(8, 8, 1), (8, 2, 1), (8, 1, 4), (6, 3, 3), (16, 1, 1),
+                                         (4, 1, 4), (24, 1, 1)])
 @pytest.mark.parametrize("causal", [True, False])
 def test_decode_small(ea, d, H, H_kv, n_q, causal):
     q, k, v, lens = _case(3, H, H_kv, n_q, 700, d, [700, 333, 2], seed=H * 7 + n_q + d)
