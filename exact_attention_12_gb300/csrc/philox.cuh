@@ -96,26 +96,31 @@ __device__ __forceinline__ uint32_t dropout_keep32(uint32_t g, uint32_t i, uint3
 // Keep bits of the 32 query rows q0 .. q0+31 for key kj, where the eight
 // lanes of an aligned lane octet hold the keys 8g .. 8g+7 (kj mod 8 ==
 // lane mod 8).  One Philox call at query q yields the uniforms of all eight
-// keys, so each lane evaluates the 4 queries q0 + 8s + (lane mod 8) and the
-// octet exchanges the results: 4 calls per lane instead of 32.  Bit t of the
-// result is 1 iff (q0 + t, kj) is kept.  All 32 lanes must call it.
+// keys, so each lane evaluates the 4 queries q0 + 8s + (lane mod 8): byte s
+// of its word holds the keep bits of keys 8g .. 8g+7 at that query.  Per
+// byte, the octet then holds an 8 x 8 bit matrix (row = lane, column = key)
+// and each lane needs one column: three butterfly stages transpose it, each
+// exchanging words with lane ^ k (k = 4, 2, 1) and swapping the off-diagonal
+// k x k bit blocks (the recursive block transpose; all four bytes at once).
+// Bit t of the result is 1 iff (q0 + t, kj) is kept.  All 32 lanes must call it.
 __device__ __forceinline__ uint32_t dropout_keep32_by_key(uint32_t kj, uint32_t q0, uint32_t bh,
                                                           uint32_t offset,
                                                           const PhiloxRoundKeys& rk,
                                                           uint32_t threshold, uint32_t lane) {
   const uint32_t u = lane & 7u;
-  uint32_t mine = 0;   // bit 8s + x: key 8g+x kept at query q0 + 8s + u
+  uint32_t x = 0;
 #pragma unroll
   for (uint32_t s = 0; s < 4; ++s)
-    mine |= dropout_keep8(kj >> 3, q0 + 8 * s + u, bh, offset, rk, threshold) << (8 * s);
-  uint32_t keep = 0;
+    x |= dropout_keep8(kj >> 3, q0 + 8 * s + u, bh, offset, rk, threshold) << (8 * s);
+  constexpr uint32_t kHigh[3] = {0xF0F0F0F0u, 0xCCCCCCCCu, 0xAAAAAAAAu};
 #pragma unroll
-  for (uint32_t src = 0; src < 8; ++src) {
-    const uint32_t m = __shfl_sync(0xffffffffu, mine, (lane & ~7u) | src);
-#pragma unroll
-    for (uint32_t s = 0; s < 4; ++s) keep |= ((m >> (8 * s + u)) & 1u) << (8 * s + src);
+  for (int i = 0; i < 3; ++i) {
+    const uint32_t k = 4u >> i;
+    const uint32_t p = __shfl_xor_sync(0xffffffffu, x, static_cast<int>(k));
+    x = (u & k) ? ((x & kHigh[i]) | ((p >> k) & ~kHigh[i]))
+                : ((x & ~kHigh[i]) | ((p << k) & kHigh[i]));
   }
-  return keep;
+  return x;
 }
 
 }  // namespace attn
