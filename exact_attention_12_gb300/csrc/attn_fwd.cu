@@ -28,7 +28,12 @@
 //                exact either way); then forms P = 2^(S c log2e - m c log2e)
 //                (packed f32x2 FMA, ex2), applies the dropout keep mask and
 //                writes P as bf16 over the first 64 columns of S, where
-//                O += P V reads it.
+//                O += P V reads it.  With dropout the thread evaluates its
+//                row's 128 keep bits (16 Philox calls) before it waits for
+//                the tile's scores, so the random numbers overlap the score
+//                MMA.
+//   * warps 10-11 idle (they complete the third warpgroup, whose registers
+//                go to the softmax warps).
 //   Because every tcgen05.commit covers all earlier MMAs of the issuing
 //   thread, "S_X(t+1) is complete" already implies "O_X += P_X V_t is
 //   complete": the softmax may then overwrite P_X and rescale O_X.
@@ -57,30 +62,24 @@ struct FwdCfg {
   static constexpr int kBoxBytes = kTile * 128;       // 128 rows x 128 bytes
   static constexpr int kTileBytes = kTile * D * kElem;
   static constexpr int kStages = (D == 64 || FP8) ? 4 : 2;
-  // dropout keep masks: per query tile a ring of kMaskStages 128 x 128-bit tiles
-  static constexpr int kMaskStages = 2;
-  static constexpr int kMaskTileBytes = kTile * 16;
-  static constexpr int kMaskBytes = DROPOUT ? 2 * kMaskStages * kMaskTileBytes : 0;
-  static constexpr int kSmem = 1024 + kTileBytes * (2 + 2 * kStages) + kMaskBytes;
+  static constexpr int kSmem = 1024 + kTileBytes * (2 + 2 * kStages);
   static constexpr uint32_t kSCol = 0, kOCol = 256;   // S_X at kSCol + 128X, O_X at kOCol + D*X
   // At d = 64 the bf16 P_X has columns of its own (kPCol + 64X), so the
   // scores of the next key tile can be computed while the softmax still
   // works on P; at d = 128 the TMEM is full and P_X overwrites S_X.
   static constexpr bool kSepP = (D == 64);
   static constexpr uint32_t kPCol = 384;
-  // warpgroups 0, 1: softmax of tiles A, B; warpgroup 2: producer (warp 8),
-  // MMA issuer (warp 9), two idle warps; with dropout, warpgroup 3 computes
-  // the keep masks (warp 12 + r: rows 32r .. 32r+31 of both tiles).
-  // Registers are re-split after the start: kRegsSoftmax for the softmax
-  // warpgroups, kRegsOther for warpgroup 2, kRegsMask for warpgroup 3:
-  // 256 * 216 + 128 * 72 <= 384 * 168 and 256 * 200 + 128 * (56 + 56) <= 512 * 128.
-  static constexpr int kThreads = DROPOUT ? 512 : 384;
-  static constexpr uint32_t kRegsLaunch = DROPOUT ? 128 : 168;
-  static constexpr uint32_t kRegsSoftmax = DROPOUT ? 200 : 216;
-  static constexpr uint32_t kRegsOther = DROPOUT ? 56 : 72;
-  static constexpr uint32_t kRegsMask = 56;
-  static_assert(256 * kRegsSoftmax + 128 * kRegsOther + (DROPOUT ? 128 * kRegsMask : 0) <=
-                    kThreads * kRegsLaunch, "register re-split exceeds the launch allocation");
+  // warpgroups 0, 1: softmax of tiles A, B (with dropout each thread also
+  // evaluates its row's keep bits); warpgroup 2: producer (warp 8), MMA
+  // issuer (warp 9), two idle warps.  Registers are re-split after the
+  // start: kRegsSoftmax for the softmax warpgroups, kRegsOther for
+  // warpgroup 2: 256 * 216 + 128 * 72 <= 384 * 168.
+  static constexpr int kThreads = 384;
+  static constexpr uint32_t kRegsLaunch = 168;
+  static constexpr uint32_t kRegsSoftmax = 216;
+  static constexpr uint32_t kRegsOther = 72;
+  static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= kThreads * kRegsLaunch,
+                "register re-split exceeds the launch allocation");
 };
 
 // A claimed unit as the producer publishes it to the other roles.
@@ -95,7 +94,7 @@ struct UnitInfo {
 constexpr int kUnitRing = 4;
 constexpr int kClaimAhead = 2;
 
-template <int ST, int MS>
+template <int ST>
 struct FwdCtl {
   uint64_t qfull, qempty, claim;
   uint64_t kfull[ST], vfull[ST], kvempty[ST];
@@ -103,9 +102,6 @@ struct FwdCtl {
   uint64_t sfree[2], pvdone[2];   // separate-P pipeline only
   uint64_t done, final_bar;
   uint64_t unitfull[kUnitRing], unitempty[kUnitRing];
-  // keep-mask ring, per query tile, stage and 32-row group (mask warp r
-  // feeds softmax warps r and 4 + r)
-  uint64_t maskfull[2][MS][4], maskempty[2][MS][4];
   UnitInfo unit[kUnitRing];
   uint32_t tmem_base;
   int abort_flag;
@@ -222,15 +218,13 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
                                          const CUtensorMap& tv, const FwdArgs& a) {
   using C = FwdCfg<D, DROPOUT, FP8>;
   constexpr int ST = C::kStages;
-  constexpr int MS = C::kMaskStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;                          // Q_A, Q_B
   uint8_t* sK = smem + 2 * C::kTileBytes;
   uint8_t* sV = sK + ST * C::kTileBytes;
-  uint4* sMask = reinterpret_cast<uint4*>(sV + ST * C::kTileBytes);   // [2][MS][128 rows]
-  __shared__ FwdCtl<ST, MS> ctl;
+  __shared__ FwdCtl<ST> ctl;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const MaskArgs& m = a.m;
@@ -272,15 +266,8 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
     mbar_init(&ctl.final_bar, 1);
     for (int r = 0; r < kUnitRing; ++r) {
       mbar_init(&ctl.unitfull[r], 1);
-      // the MMA thread, the eight softmax warps and the four mask warps
-      mbar_init(&ctl.unitempty[r], DROPOUT ? 13 : 9);
+      mbar_init(&ctl.unitempty[r], 9);   // the MMA thread and the eight softmax warps
     }
-    for (int x = 0; x < 2; ++x)
-      for (int st = 0; st < MS; ++st)
-        for (int g = 0; g < 4; ++g) {
-          mbar_init(&ctl.maskfull[x][st][g], 1);
-          mbar_init(&ctl.maskempty[x][st][g], 1);
-        }
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -516,55 +503,6 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
       mbar_wait_drain(&ctl.final_bar, 0, a.timeout_ns);
     }
   }
-  } else if (wg == 3) {
-    if constexpr (DROPOUT) {
-      regs_decrease<C::kRegsMask>();
-      // ------------------------------------------------------ dropout masks
-      // Rows 32r .. 32r+31 of both query tiles, one row per lane; the tiles
-      // in the order the softmax warps consume them.
-      const int grp = warp - 12;
-      const int row = grp * 32 + lane;
-      uint32_t mc[2] = {0, 0};   // mask tiles produced per query-tile slot (all units)
-      bool ok = true;
-      for (int pub = 0; ok; ++pub) {
-        const int r = pub % kUnitRing;
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(&ctl.unitfull[r], (pub / kUnitRing) & 1, wc, kSiteFwdUnit));
-        if (!ok) break;
-        const UnitInfo ui = ctl.unit[r];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.unitempty[r]);
-        if (ui.w < 0) break;
-        const int pair = ui.pair, bh = ui.bh;
-        PairWalk walk{TileList{ui.idx[0], ui.n[0]}, TileList{ui.idx[1], ui.n[1]}};
-        int j;
-        bool need[2];
-        while (ok && walk.next(j, need[0], need[1])) {
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (!need[x]) continue;
-            const int st = mc[x] % MS;
-            if (mc[x] >= MS) {
-              ok = __all_sync(0xffffffffu, mbar_wait(&ctl.maskempty[x][st][grp],
-                                                     ((mc[x] / MS) - 1) & 1, wc, kSiteFwdMask));
-              if (!ok) break;
-            }
-            const uint32_t qi = static_cast<uint32_t>((2 * pair + x) * kTile + row);
-            // one 32-key word per iteration; the loop stays rolled to keep the
-            // kernel's code within the instruction cache
-            uint32_t* dst = reinterpret_cast<uint32_t*>(&sMask[(x * MS + st) * kTile + row]);
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q)
-              dst[q] = dropout_keep32(static_cast<uint32_t>(j * (kTile / 8) + 4 * q), qi,
-                                      static_cast<uint32_t>(bh), m.offset, m.rk,
-                                      m.drop_threshold);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.maskfull[x][st][grp]);
-            ++mc[x];
-          }
-        }
-      }
-    }
   } else {
     regs_increase<C::kRegsSoftmax>();
     // ---------------------------------------------------- softmax, epilogue
@@ -596,6 +534,16 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
       float m_used = -INFINITY;      // raw-score max the exponentials are taken against
       float l_sum = 0.f;
       for (int jj = 0; jj < n; ++jj, ++cs) {
+        // this row's 128 keep bits, evaluated while the tensor core forms the
+        // scores (bit t of word q: key 32q + t of the tile is kept)
+        uint32_t keepw[4] = {~0u, ~0u, ~0u, ~0u};
+        if constexpr (DROPOUT) {
+          const uint32_t j8 = static_cast<uint32_t>(tiles[jj] * (kTile / 8));
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            keepw[q] = dropout_keep32(j8 + 4 * q, static_cast<uint32_t>(qi),
+                                      static_cast<uint32_t>(bh), m.offset, m.rk, m.drop_threshold);
+        }
         ok = __all_sync(0xffffffffu, mbar_wait(&ctl.sfull[x], cs & 1, wc, kSiteFwdSFull));
         if (!ok) break;
         tc_fence_after();
@@ -660,20 +608,6 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
         const float mc = (m_used == -INFINITY) ? 0.f : m_used * c2;
         const uint64_t c2x2 = f2_pack(c2, c2), nmc2 = f2_pack(-mc, -mc);
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-        uint32_t keepw[4] = {~0u, ~0u, ~0u, ~0u};
-        if constexpr (DROPOUT) {   // this row's 128 keep bits, from the mask warps
-          const int st = cs % MS, grp = warp & 3;
-          ok = __all_sync(0xffffffffu, mbar_wait(&ctl.maskfull[x][st][grp], (cs / MS) & 1, wc,
-                                                 kSiteFwdMask));
-          if (!ok) break;
-          const uint4 kb = sMask[(x * MS + st) * kTile + row];
-          keepw[0] = kb.x;
-          keepw[1] = kb.y;
-          keepw[2] = kb.z;
-          keepw[3] = kb.w;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl.maskempty[x][st][grp]);
-        }
   #pragma unroll
         for (int c = 0; c < 128; c += 32) {
           const uint32_t keep = keepw[c / 32];
