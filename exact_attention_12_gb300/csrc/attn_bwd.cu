@@ -563,12 +563,24 @@ __global__ void __launch_bounds__(384, 1)
       const bool diag = m.causal && qtile == kt;   // query q < key: masked
       const bool edge = diag || !tile_keys_ok;
 
+      // this row's keep bits for the warp's 64 query columns, evaluated
+      // before the scores are waited for, so they overlap the S^T MMA.
+      // Element (query q, key kj): 16-bit half kj mod 2 of word (kj mod 8)/2
+      // of the counter (kj/8, q, bh, offset).
+      uint32_t keepbits[2] = {0xffffffffu, 0xffffffffu};
+      if constexpr (DROPOUT) {
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+          keepbits[cc] = dropout_keep32_by_key(static_cast<uint32_t>(kj),
+                                               static_cast<uint32_t>(q0 + qc0 + cc * 32),
+                                               static_cast<uint32_t>(bh), m.offset, m.rk,
+                                               m.drop_threshold, static_cast<uint32_t>(lane));
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl.sfull, ph, wc, kSiteBwdSoft));
       if (!ok) break;
       tc_fence_after();
       // P^T = 2^(S^T c log2e - L log2e), kept in fp32 for dS; P~^T into TMEM
       float p[64];
-      uint32_t keepbits[2];
       {
         uint32_t srr[64];
         tmem_ld32(tl + C::kSCol + qc0, srr);
@@ -596,16 +608,7 @@ __global__ void __launch_bounds__(384, 1)
       }
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        uint32_t keep = 0xffffffffu;
-        if constexpr (DROPOUT) {
-          // element (query q, key kj): 16-bit half kj mod 2 of word (kj mod 8)/2
-          // of the counter (kj/8, q, bh, offset)
-          keep = dropout_keep32_by_key(static_cast<uint32_t>(kj),
-                                       static_cast<uint32_t>(q0 + qc0 + cc * 32),
-                                       static_cast<uint32_t>(bh), m.offset, m.rk,
-                                       m.drop_threshold, static_cast<uint32_t>(lane));
-        }
-        keepbits[cc] = keep;
+        const uint32_t keep = keepbits[cc];
         uint32_t pk[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
@@ -764,6 +767,10 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
   const bool real = row < rows && n < a.m.N;
   float s = 0.f;
   if (real) {
+    // zero this thread's 8 elements of the dQ accumulator ([B, H, N, d])
+    float4* acc = reinterpret_cast<float4*>(a.dq_acc + (bh * a.m.N + n) * D + part * 8);
+    acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     const int64_t b = bh / a.m.H, h = bh % a.m.H;
     const int64_t off = b * a.stride_b + h * a.stride_h + n * a.stride_n + part * 8;
     const uint4 ov = *reinterpret_cast<const uint4*>(o + off);
@@ -788,11 +795,6 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
     a.dsum[row] = -s;
     a.lse2[row] = nl2;
   }
-  // zero the dQ accumulator
-  const int64_t n4 = static_cast<int64_t>(a.m.B) * a.m.H * a.m.N * D / 4;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  float4* acc = reinterpret_cast<float4*>(a.dq_acc);
-  for (int64_t e = gtid; e < n4; e += stride) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 template <int D>
