@@ -38,7 +38,7 @@ SECONDARY = ("long-causal-16384",)
 # DRAM bytes (read + write) per launch of the backward main kernel, from the
 # ncu capture summarised in profiles/bwd_bf16_kernel_bert-large.md; absent
 # (reported as null) for other workloads or once the kernel has changed
-BWD_MAIN_TRAFFIC = {"bert-large": 112.7e6}
+BWD_MAIN_TRAFFIC = {"bert-large": 112.9e6}
 
 
 # ----------------------------------------------------------------- FLOPs --
