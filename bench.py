@@ -39,6 +39,9 @@ SECONDARY = ("long-causal-16384",)
 # ncu capture summarised in profiles/bwd_bf16_kernel_bert-large.md; absent
 # (reported as null) for other workloads or once the kernel has changed
 BWD_MAIN_TRAFFIC = {"bert-large": 112.9e6}
+# buffer sets of the e2e leg: step k uploads into set k mod E2E_SETS while
+# step k-1 computes and step k-2 downloads, so the three overlap fully
+E2E_SETS = 3
 
 
 # ----------------------------------------------------------------- FLOPs --
@@ -248,7 +251,7 @@ def measure_e2e(ea, w, dev, steps, warmup):
 
     Every step copies its inputs host -> device, runs the forward and the
     backward, and copies dQ, dK, dV device -> host.  Steps are pipelined over
-    three streams (uploads, compute, downloads) with two buffer sets, so the
+    three streams (uploads, compute, downloads) with E2E_SETS buffer sets, so the
     copies of one step overlap the compute of its neighbours; the time is
     taken from the first upload to the last download.
     """
@@ -263,16 +266,17 @@ def measure_e2e(ea, w, dev, steps, warmup):
     shapes = {n: inp[n].shape for n in names}
     out_shapes = (inp["q"].shape, inp["k"].shape, inp["v"].shape)   # dQ, dK, dV
     dev_in = [{n: torch.empty(shapes[n], dtype=dtype, device=dev) for n in names}
-              for _ in range(2)]
-    dev_out = [[torch.empty(sh, dtype=dtype, device=dev) for sh in out_shapes] for _ in range(2)]
+              for _ in range(E2E_SETS)]
+    dev_out = [[torch.empty(sh, dtype=dtype, device=dev) for sh in out_shapes]
+               for _ in range(E2E_SETS)]
     host_out = [[torch.empty(sh, dtype=dtype).pin_memory() for sh in out_shapes]
-                for _ in range(2)]
+                for _ in range(E2E_SETS)]
     up, comp, down = (torch.cuda.Stream(dev) for _ in range(3))
-    ev_in = [torch.cuda.Event() for _ in range(2)]        # inputs of buffer set uploaded
-    ev_used = [torch.cuda.Event() for _ in range(2)]      # compute done with buffer set
-    ev_out = [torch.cuda.Event() for _ in range(2)]       # downloads of buffer set done
+    ev_in = [torch.cuda.Event() for _ in range(E2E_SETS)]     # inputs of buffer set uploaded
+    ev_used = [torch.cuda.Event() for _ in range(E2E_SETS)]   # compute done with buffer set
+    ev_out = [torch.cuda.Event() for _ in range(E2E_SETS)]    # downloads of buffer set done
     def step(k):
-        b = k % 2
+        b = k % E2E_SETS
         with torch.cuda.stream(up):
             up.wait_event(ev_used[b])
             for n in names:
@@ -305,7 +309,7 @@ def measure_e2e(ea, w, dev, steps, warmup):
     d2h = sum(t.numel() * t.element_size() for t in host_out[0])
     return {"value": flops / dt / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3,
-            "pipelining": "uploads, compute and downloads on three streams, two buffer sets"}
+            "pipelining": f"uploads, compute and downloads on three streams, {E2E_SETS} buffer sets"}
 
 
 # ---------------------------------------------------------- oracle (CPU) --
