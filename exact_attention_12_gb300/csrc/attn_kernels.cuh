@@ -17,7 +17,7 @@ constexpr float kRescaleTau = 8.0f;   // lazy-rescale threshold, log2 units
 // Where a kernel gave up waiting (recorded next to the status code).
 enum WaitSite : int {
   kSiteFwdQ = 1, kSiteFwdK, kSiteFwdV, kSiteFwdKvEmpty, kSiteFwdSFull, kSiteFwdSFree,
-  kSiteFwdPFull, kSiteFwdPvDone, kSiteFwdUnit, kSiteFwdMask,
+  kSiteFwdPFull, kSiteFwdPvDone, kSiteFwdUnit,
   kSiteBwdLoad = 20, kSiteBwdKV, kSiteBwdQ, kSiteBwdMma, kSiteBwdSoft, kSiteBwdDq,
   kSiteBwdEmpty, kSiteBwdFree, kSiteBwdSmem,
   kSiteDecode = 40
