@@ -110,7 +110,7 @@ def _sample(N, seed, k=10):
 
 
 @pytest.mark.parametrize("name", ["bert-large", "gpt2-1k", "gpt2-4k", "long-causal-4096",
-                                  "long-causal-16384", "block-sparse-64k"])
+                                  "long-causal-8192", "long-causal-16384", "block-sparse-64k"])
 def test_full_size_workload_sampled(ea, name):
     w = workloads.get(name)
     inp = workloads.make_inputs(w)

@@ -176,8 +176,8 @@ def _sampled_rows(N, seed):
 
 
 @pytest.mark.parametrize("name", ["bert-large", "gpt2-1k", "gpt2-4k", "long-causal-512",
-                                  "long-causal-4096", "long-causal-16384",
-                                  "block-sparse-64k"])
+                                  "long-causal-1024", "long-causal-2048", "long-causal-4096",
+                                  "long-causal-8192", "long-causal-16384", "block-sparse-64k"])
 def test_full_size_workload_sampled(ea, name):
     w = workloads.get(name)
     inp = workloads.make_inputs(w)
