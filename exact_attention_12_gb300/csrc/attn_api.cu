@@ -583,15 +583,16 @@ attn_status attn_decode(const attn_params* p, int32_t n_q, const void* q, const 
   a.part_l = reinterpret_cast<float*>(w + L.part_l);
   a.status = reinterpret_cast<int*>(w);
   a.timeout_ns = kTimeoutNs;
-  // k, v with 64-key boxes
+  // k, v with boxes of the tile the chosen kernel streams
   attn::TensorMaps tm{};
   int64_t sb, sh, sn;
   kv_strides(p, &sb, &sh, &sn);
+  const int box_rows = a.rows <= attn::kDecMmaRows ? attn::kDecMmaKeys : 64;
   if ((st = make_map(&tm.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->B, kv_heads(p), p->N,
-                     p->d, sb, sh, sn, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK)
+                     p->d, sb, sh, sn, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK)
     return st;
   if ((st = make_map(&tm.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->B, kv_heads(p), p->N,
-                     p->d, sb, sh, sn, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK)
+                     p->d, sb, sh, sn, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK)
     return st;
   const cudaError_t e = attn::launch_decode(tm, o, lse, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "decode launch");

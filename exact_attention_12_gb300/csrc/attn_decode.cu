@@ -331,14 +331,20 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 
 constexpr int kMmaWarps = 3;
 constexpr int kMmaThreads = 32 * kMmaWarps;
-constexpr int kMmaRows = 16;
+constexpr int kMmaRows = kDecMmaRows;
+constexpr int kMaxStagesPerWarp = 4;
 
+// Tiles of kDecMmaKeys keys, two (d = 128) or four (d = 64) stages per warp:
+// 96 KB of ring, two CTAs per SM, and each warp reads one tile while its
+// next copy is in flight.
 template <int D>
 struct DecMmaCfg {
+  static constexpr int kKeys = kDecMmaKeys;
   static constexpr int kBoxes = D / 64;
-  static constexpr int kBoxBytes = kDecKeys * 128;       // 64 keys x 128 bytes
-  static constexpr int kTileBytes = kDecKeys * D * 2;
-  static constexpr int kStagesPerWarp = D == 128 ? 1 : 2;   // 96 KB: two CTAs per SM
+  static constexpr int kBoxBytes = kKeys * 128;           // kKeys rows x 128 bytes
+  static constexpr int kTileBytes = kKeys * D * 2;
+  static constexpr int kStagesPerWarp = D == 128 ? 2 : 4;
+  static_assert(kStagesPerWarp <= kMaxStagesPerWarp, "barrier array");
   static constexpr int kStages = kMmaWarps * kStagesPerWarp;
   static constexpr int kRingBytes = 2 * kStages * kTileBytes;
   static constexpr int kSmem = 1024 + kRingBytes;
@@ -346,7 +352,7 @@ struct DecMmaCfg {
 };
 
 struct DecMmaShared {
-  uint64_t full[2 * kMmaWarps];
+  uint64_t full[kMaxStagesPerWarp * kMmaWarps];
   float m[kMmaWarps][kMmaRows], l[kMmaWarps][kMmaRows];
   int abort_flag;
 };
@@ -403,7 +409,8 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
   const int len = min(max(m.key_lens[b], 0), m.N);
   const int k_begin = split * a.chunk;
   const int k_end = min(len, k_begin + a.chunk);
-  const int ntiles = k_end > k_begin ? (k_end - k_begin + kDecKeys - 1) / kDecKeys : 0;
+  constexpr int KT = C::kKeys;
+  const int ntiles = k_end > k_begin ? (k_end - k_begin + KT - 1) / KT : 0;
   auto sK = [&](int s) { return smem + s * 2 * C::kTileBytes; };
   auto sV = [&](int s) { return smem + s * 2 * C::kTileBytes + C::kTileBytes; };
 
@@ -420,7 +427,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
   const int my_tiles = ntiles > warp ? (ntiles - warp + kMmaWarps - 1) / kMmaWarps : 0;
   auto issue = [&](int u) {   // lane 0: K and V of the warp's tile u
     const int st = warp * SPW + u % SPW;
-    const int k0 = k_begin + (warp + kMmaWarps * u) * kDecKeys;
+    const int k0 = k_begin + (warp + kMmaWarps * u) * KT;
     mbar_arrive_expect_tx(&sh.full[st], 2 * C::kTileBytes);
 #pragma unroll
     for (int x = 0; x < C::kBoxes; ++x) {
@@ -470,16 +477,16 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
     if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sh.full[s], (u / SPW) & 1, wc, kSiteDecode))))
       break;
     const uint32_t kb = smem_u32(sK(s)), vb = smem_u32(sV(s));
-    const int k0 = k_begin + tile * kDecKeys;
-    // S = Q K^T: 8 key blocks of 8; per 16 columns of d, one ldmatrix.x4
+    const int k0 = k_begin + tile * KT;
+    // S = Q K^T: KT/8 key blocks of 8; per 16 columns of d, one ldmatrix.x4
     // gives the B fragments of two key blocks
-    float sc[8][4];
+    float sc[KT / 8][4];
 #pragma unroll
-    for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+    for (int n = 0; n < KT / 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
 #pragma unroll
-      for (int n = 0; n < 8; n += 2) {
+      for (int n = 0; n < KT / 8; n += 2) {
         // blocks: (keys 8n, d 16kk), (8n, 16kk+8), (8n+8, 16kk), (8n+8, 16kk+8)
         const int key = 8 * n + 8 * (lb >> 1) + lr, col = 16 * kk + 8 * (lb & 1);
         uint32_t b0, b1, b2, b3;
@@ -490,7 +497,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
     // mask, scale to log2 units, running max
     float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
+    for (int n = 0; n < KT / 8; ++n)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = e >> 1;
@@ -510,10 +517,10 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
       mrow[i] = mn;
     }
     // P = 2^(S - m) as bf16 A fragments; row sums from the same fp32 values
-    uint32_t pa[4][4];
+    uint32_t pa[KT / 16][4];
     float psum[2] = {0.f, 0.f};
 #pragma unroll
-    for (int n = 0; n < 8; ++n) {
+    for (int n = 0; n < KT / 8; ++n) {
       const float p0 = exp2f(sc[n][0] - base[0]), p1 = exp2f(sc[n][1] - base[0]);
       const float p2 = exp2f(sc[n][2] - base[1]), p3 = exp2f(sc[n][3] - base[1]);
       psum[0] += p0 + p1;
@@ -536,7 +543,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
     // O += P V: per 16 keys and 16 columns of d, one ldmatrix.x4.trans gives
     // the B fragments of two 8-column tiles
 #pragma unroll
-    for (int kp = 0; kp < 4; ++kp)
+    for (int kp = 0; kp < KT / 16; ++kp)
 #pragma unroll
       for (int n = 0; n < NT; n += 2) {
         // blocks: (keys 16kp, d 8n), (16kp+8, 8n), (16kp, 8n+8), (16kp+8, 8n+8)

@@ -90,6 +90,11 @@ struct BwdArgs {
 
 // Decode step: query rows per CTA (the key/value group's heads x n_q) at most.
 constexpr int kDecMaxRows = 64;
+// Up to kDecMmaRows rows the warp-MMA kernel runs, on tiles of kDecMmaKeys
+// keys (its k, v tensor maps have boxes of that many rows); above it the FMA
+// kernel, on 64-key tiles.
+constexpr int kDecMmaRows = 16;
+constexpr int kDecMmaKeys = 32;
 
 struct DecodeArgs {
   MaskArgs m;                     // N = cache capacity, key_lens = cache lengths
@@ -127,7 +132,7 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const BwdArgs
                                   cudaStream_t s);
 cudaError_t launch_bwd_bf16(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_dq_convert(void* dq, const BwdArgs& a, cudaStream_t s);
-// k, v maps with 64-row boxes
+// k, v maps with boxes of kDecMmaKeys rows (rows <= kDecMmaRows) or 64 rows
 cudaError_t launch_decode(const TensorMaps& tm, void* o, float* lse, const DecodeArgs& a,
                           cudaStream_t s);
 
