@@ -175,18 +175,22 @@ struct PairWalk {
 };
 
 // S = Q K^T: both operands K-major; one instruction per 32 bytes of d
-// (16 bf16 or 32 E4M3 elements).
+// (16 bf16 or 32 E4M3 elements).  The descriptors are built once per group
+// and stepped by adding the (compile-time) offset to their address field:
+// the issuing thread spends its time issuing, not rebuilding descriptors
+// (shared-memory addresses stay below 256 KB, so the 14-bit field cannot
+// carry into the next one).
 template <int D, bool FP8>
 __device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint32_t q_base, uint32_t k_base) {
   constexpr int kSteps = D * FwdCfg<D, false, FP8>::kElem / 32;
+  const uint64_t da0 = smem_desc(q_base, 16, 1024), db0 = smem_desc(k_base, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < kSteps; ++kk) {
-    const uint32_t off = (kk >> 2) * FwdCfg<D>::kBoxBytes + (kk & 3) * 32;
-    const uint64_t da = smem_desc(q_base + off, 16, 1024), db = smem_desc(k_base + off, 16, 1024);
+    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * FwdCfg<D>::kBoxBytes + (kk & 3) * 32) >> 4);
     if constexpr (FP8)
-      mma_ss_f8(d_tmem, da, db, idesc_e4m3(128, 128, false, false), kk > 0 ? 1u : 0u);
+      mma_ss_f8(d_tmem, da0 + off, db0 + off, idesc_e4m3(128, 128, false, false), kk > 0 ? 1u : 0u);
     else
-      mma_ss(d_tmem, da, db, idesc_bf16(128, 128, false, false), kk > 0 ? 1u : 0u);
+      mma_ss(d_tmem, da0 + off, db0 + off, idesc_bf16(128, 128, false, false), kk > 0 ? 1u : 0u);
   }
 }
 
@@ -198,16 +202,18 @@ __device__ __forceinline__ void mma_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_
                                        bool accumulate) {
   if constexpr (FP8) {
     constexpr uint32_t kId = idesc_e4m3(128, D, false, false);
+    const uint64_t dv0 = smem_desc(v_base, 16, 1024);
 #pragma unroll
     for (int kk = 0; kk < kTile / 32; ++kk)
-      mma_ts_f8(o_tmem, p_tmem + kk * 8, smem_desc(v_base + kk * 32, 16, 1024), kId,
+      mma_ts_f8(o_tmem, p_tmem + kk * 8, dv0 + static_cast<uint64_t>((kk * 32) >> 4), kId,
                 (accumulate || kk > 0) ? 1u : 0u);
   } else {
     constexpr uint32_t kId = idesc_bf16(128, D, false, true);
+    const uint64_t dv0 = smem_desc(v_base, FwdCfg<D>::kBoxBytes, 1024);
 #pragma unroll
     for (int kk = 0; kk < kTile / 16; ++kk)
-      mma_ts(o_tmem, p_tmem + kk * 8, smem_desc(v_base + kk * 2048, FwdCfg<D>::kBoxBytes, 1024),
-             kId, (accumulate || kk > 0) ? 1u : 0u);
+      mma_ts(o_tmem, p_tmem + kk * 8, dv0 + static_cast<uint64_t>((kk * 2048) >> 4), kId,
+             (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
