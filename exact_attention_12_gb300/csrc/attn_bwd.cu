@@ -217,15 +217,24 @@ __device__ __forceinline__ void drain_dq(uint32_t tl_dq, uint8_t* stage, uint8_t
   }
 }
 
+// Shared-memory descriptor of `base` + `off` bytes, from the descriptor of
+// `base`: the offset goes into the 14-bit address field (addresses stay below
+// 256 KB, so it cannot carry).  The MMA groups below build one descriptor
+// per operand and step it this way, so the issuing thread issues instead of
+// rebuilding descriptors.
+__device__ __forceinline__ uint64_t desc_plus(uint64_t desc, uint32_t off) {
+  return desc + static_cast<uint64_t>(off >> 4);
+}
+
 template <int D>
 __device__ __forceinline__ void mma_kt_qt(uint32_t d_tmem, uint32_t a_base, uint32_t b_base) {
   // D[128 x 128] = A[128 x D] B[128 x D]^T, both K-major (K = D)
   constexpr uint32_t kId = idesc_bf16(128, 128, false, false);
+  const uint64_t da = smem_desc(a_base, 16, 1024), db = smem_desc(b_base, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk >> 2) * BwdCfg<D>::kBoxBytes + (kk & 3) * 32;
-    mma_ss(d_tmem, smem_desc(a_base + off, 16, 1024), smem_desc(b_base + off, 16, 1024), kId,
-           kk > 0 ? 1u : 0u);
+    mma_ss(d_tmem, desc_plus(da, off), desc_plus(db, off), kId, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -445,12 +454,12 @@ __global__ void __launch_bounds__(384, 1)
             const uint32_t ph = it & 1;
             const uint32_t q_base = smem_u32(sQ + (it % QS) * C::kTileBytes);
             const uint32_t do_base = smem_u32(sdO + (it % DS) * C::kTileBytes);
-            // at d = 128 the operand descriptors are rebuilt per tile from these
-            // (a few integer ops per MMA) rather than kept live across both
+            // the operand descriptors are rebuilt per tile from these (a few
+            // integer ops per MMA group) rather than kept live across both
             // loops, where they do not fit this warp's registers
-            const uint32_t k_base = D == 128 ? opaque(k_base0) : k_base0;
-            const uint32_t v_base = D == 128 ? opaque(v_base0) : v_base0;
-            const uint32_t ds_base = D == 128 ? opaque(ds_base0) : ds_base0;
+            const uint32_t k_base = opaque(k_base0);
+            const uint32_t v_base = opaque(v_base0);
+            const uint32_t ds_base = opaque(ds_base0);
             if (!claimed && n - i <= kBwdClaimAhead) {
               mbar_arrive(&ctl.claim);   // once per unit; at the latest in its last iteration
               claimed = true;
@@ -459,11 +468,13 @@ __global__ void __launch_bounds__(384, 1)
             // [0,32), those of rows 64..127 in [64,96)
             if (!(ok = mbar_wait(&ctl.pfull, ph, wc, kSiteBwdMma))) break;
             tc_fence_after();
+            {
+              const uint64_t ddo = smem_desc(do_base, C::kBoxBytes, 1024);
 #pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_ts(tmem + C::kDVCol, tmem + C::kSCol + kk * 8 + (kk >= 4 ? 32 : 0),
-                     smem_desc(do_base + kk * 2048, C::kBoxBytes, 1024), kIdKN,
-                     (i > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                mma_ts(tmem + C::kDVCol, tmem + C::kSCol + kk * 8 + (kk >= 4 ? 32 : 0),
+                       desc_plus(ddo, kk * 2048), kIdKN, (i > 0 || kk > 0) ? 1u : 0u);
+            }
             mma_commit(&ctl.doempty[it % DS]);
             // S^T_{i+1}: the S^T columns were read by the compute warps before
             // pfull and P~^T_i is consumed by dV_i, issued just before
@@ -478,22 +489,29 @@ __global__ void __launch_bounds__(384, 1)
             // dK += dS^T Q_i
             if (!(ok = mbar_wait(&ctl.dsfull, ph, wc, kSiteBwdMma))) break;
             tc_fence_after();
+            {
+              const uint64_t dds = smem_desc(ds_base, 16, 1024);
+              const uint64_t dq = smem_desc(q_base, C::kBoxBytes, 1024);
 #pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-              mma_ss(tmem + C::kDKCol, smem_desc(ds_base + off, 16, 1024),
-                     smem_desc(q_base + kk * 2048, C::kBoxBytes, 1024), kIdKN,
-                     (i > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < kTile / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+                mma_ss(tmem + C::kDKCol, desc_plus(dds, off), desc_plus(dq, kk * 2048), kIdKN,
+                       (i > 0 || kk > 0) ? 1u : 0u);
+              }
             }
             // dQ_i = dS K_j (its columns: drained copy of the previous dQ read out)
             if (!C::kDqAliasesDp && it >= 1) {
               if (!(ok = mbar_wait(&ctl.dqfree, (it - 1) & 1, wc, kSiteBwdMma))) break;
               tc_fence_after();
             }
+            {
+              const uint64_t dds = smem_desc(ds_base, C::kBoxBytes, 1024);
+              const uint64_t dk = smem_desc(k_base, C::kBoxBytes, 1024);
 #pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_ss(tmem + C::kDQCol, smem_desc(ds_base + kk * 2048, C::kBoxBytes, 1024),
-                     smem_desc(k_base + kk * 2048, C::kBoxBytes, 1024), kIdNN, kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                mma_ss(tmem + C::kDQCol, desc_plus(dds, kk * 2048), desc_plus(dk, kk * 2048), kIdNN,
+                       kk > 0 ? 1u : 0u);
+            }
             mma_commit(&ctl.dqfull);
             mma_commit(&ctl.qempty[it % QS]);
             // dP^T_{i+1} (for d = 128 its columns hold dQ_i until drained)
