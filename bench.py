@@ -195,6 +195,42 @@ class Step:
         return sum(x.numel() * x.element_size() for x in t)
 
 
+class StepGraphs:
+    """The step captured in CUDA graphs, for timing without host launch cost.
+
+    `enqueue(k, stream)` enqueues one step on input set k.  `block` holds
+    `per` consecutive steps (the sets in rotation; `per` is a multiple of
+    `nsets`), `one[k]` a single step on set k, so that `replay(n)` enqueues
+    exactly n steps in rotation order on the current stream.  Nothing is
+    allocated inside the captures: every step writes into buffers that exist
+    before them.
+    """
+
+    def __init__(self, enqueue, nsets, dev, per_target=16):
+        self.nsets = nsets
+        self.per = max(1, per_target // nsets) * nsets
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        self.block = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.block, stream=side):
+            for i in range(self.per):
+                enqueue(i % nsets, torch.cuda.current_stream(dev))
+        self.one = []
+        for k in range(nsets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                enqueue(k, torch.cuda.current_stream(dev))
+            self.one.append(g)
+        torch.cuda.synchronize(dev)
+
+    def replay(self, steps):
+        blocks, rest = divmod(steps, self.per)
+        for _ in range(blocks):
+            self.block.replay()
+        for i in range(rest):
+            self.one[i % self.nsets].replay()
+
+
 def _barrier(dist):
     if dist is not None:
         dist.barrier()
@@ -219,7 +255,20 @@ def measure_device(ea, w, dev, steps, warmup, dist=None, sample_clocks=True):
     for i in range(warmup):
         sets[i % nsets].run(stream)
     torch.cuda.synchronize(dev)
+    # kernel times: the same steps launched one by one, an event around each
+    # launch (the events cost ~10 us per step, so the step itself is timed
+    # below without them)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    for i in range(steps):
+        sets[i % nsets].run(stream, evs[i])
+    torch.cuda.synchronize(dev)
+    stage = [sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
+             for j in range(4)]
+    # the step: replayed from CUDA graphs (the host launch cost of four ctypes
+    # calls is not the kernels'), input sets in rotation as above
+    graphs = StepGraphs(lambda k, s: sets[k].run(s), nsets, dev)
+    graphs.replay(nsets)
+    torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     _barrier(dist)
     torch.cuda.synchronize(dev)
@@ -228,8 +277,7 @@ def measure_device(ea, w, dev, steps, warmup, dist=None, sample_clocks=True):
         time.sleep(0.3)       # let the sampler start before the timed region
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    for i in range(steps):
-        sets[i % nsets].run(stream, evs[i])
+    graphs.replay(steps)
     end.record(stream)
     torch.cuda.synchronize(dev)
     _barrier(dist)
@@ -237,8 +285,6 @@ def measure_device(ea, w, dev, steps, warmup, dist=None, sample_clocks=True):
         sampler.__exit__()
     ea.check(first.ws, dev)
     total_ms = _max_over_ranks(dist, start.elapsed_time(end), dev)
-    stage = [sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
-             for j in range(4)]
     flops_f = fwd_flops(w, inp["key_lens"], inp["block_mask"])
     return dict(inp=inp, total_ms=total_ms, ms_per_step=total_ms / steps, stage_ms=stage,
                 fwd_flops=flops_f, bwd_flops=2.5 * flops_f, nsets=nsets,
@@ -433,13 +479,17 @@ def measure_decode(ea, w, dev, steps, warmup):
     for _ in range(warmup):
         ea.attention_decode(q, k, v, lens, scale=inp["scale"], causal=w.causal, out=o, lse=lse)
     torch.cuda.synchronize(dev)
+    graphs = StepGraphs(lambda _k, _s: ea.attention_decode(q, k, v, lens, scale=inp["scale"],
+                                                          causal=w.causal, out=o, lse=lse),
+                        1, dev)
+    graphs.replay(1)
+    torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.__enter__()
     time.sleep(0.3)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    for _ in range(steps):
-        ea.attention_decode(q, k, v, lens, scale=inp["scale"], causal=w.causal, out=o, lse=lse)
+    graphs.replay(steps)
     end.record(stream)
     torch.cuda.synchronize(dev)
     sampler.__exit__()
@@ -502,7 +552,8 @@ def run_decode(args, w):
                    "n_q": w.decode_n_q, "cache_capacity": w.N, "d": w.d, "causal": w.causal,
                    "parallelism": "single GPU",
                    "l2": f"the resident cache ({nbytes / 2**20:.0f} MiB read per step) is larger "
-                         f"than the 129 MB L2"},
+                         f"than the 129 MB L2",
+                   "timing": "decode calls captured in a CUDA graph, replayed; CUDA events"},
         "roofline": {"kernel": "decode_mma_kernel" if (w.H // w.kv_heads) * w.decode_n_q <= 16
                      else "decode_kernel", "bound": "hbm", "achieved": gbs, "peak": hbm,
                      "unit": "GB/s", "frac": gbs / hbm, "peak_source": f"hbm_gbs ({src})",
@@ -555,14 +606,19 @@ def measure_fp8(ea, w, dev, steps, warmup):
         q, k, v, o, lse = sets[i % nsets]
         ea.attention_fwd(q, k, v, out=o, lse=lse, **kw)
     torch.cuda.synchronize(dev)
+    def enqueue(i, s):
+        q, k, v, o, lse = sets[i]
+        ea.attention_fwd(q, k, v, out=o, lse=lse, **kw)
+
+    graphs = StepGraphs(enqueue, nsets, dev)
+    graphs.replay(nsets)
+    torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.__enter__()
     time.sleep(0.3)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    for i in range(steps):
-        q, k, v, o, lse = sets[i % nsets]
-        ea.attention_fwd(q, k, v, out=o, lse=lse, **kw)
+    graphs.replay(steps)
     end.record(stream)
     torch.cuda.synchronize(dev)
     sampler.__exit__()
@@ -632,7 +688,8 @@ def run_fp8(args, w):
         "config": {"workload": describe(w), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                    "causal": w.causal, "parallelism": "single GPU",
                    "l2": f"inputs rotate over {r['nsets']} resident sets of "
-                         f"{r['resident'] / 2**20:.0f} MiB (> 2x the 129 MB L2)"},
+                         f"{r['resident'] / 2**20:.0f} MiB (> 2x the 129 MB L2)",
+                   "timing": "attn_fwd calls captured in CUDA graphs, replayed; CUDA events"},
         "roofline": {"kernel": "fwd_fp8_kernel", "bound": "tensor", "achieved": tflops,
                      "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
                      "peak_source": f"bf16_tflops ({src}) x {FP8_NOMINAL_RATIO} "
@@ -780,7 +837,11 @@ def main():
                    "causal": w.causal, "dropout_p": w.dropout_p,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"inputs rotate over {r['nsets']} resident sets of "
-                         f"{r['resident_bytes'] / 2**20:.0f} MiB (> 2x the 129 MB L2)"},
+                         f"{r['resident_bytes'] / 2**20:.0f} MiB (> 2x the 129 MB L2)",
+                   "timing": "steps captured in CUDA graphs and replayed, CUDA events around "
+                             "the K steps; stage_ms and the roofline kernel time from a "
+                             "separate pass of K steps launched one by one with an event "
+                             "around each launch"},
         "fwd_tflops": r["fwd_flops"] / (fwd_ms * 1e-3) / 1e12,
         "bwd_tflops": r["bwd_flops"] / ((pre_ms + main_ms + dq_ms) * 1e-3) / 1e12,
         "stage_ms": {"fwd": fwd_ms, "bwd_preprocess": pre_ms, "bwd_main": main_ms,
