@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ BwdCtl ctl;
   if ((smem_u32(smem_raw) & 1023u) != 0) {   // buffers need 1024-byte alignment
+    grid_dep_wait();
     if (threadIdx.x == 0 && atomicCAS(a.status, 0, kStatusSmemAlign) == 0)
       atomicExch(a.status + 1, kSiteBwdSmem);
     return;
@@ -312,6 +313,10 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the set-up above touched no global memory: from here on the previous
+  // kernel of the stream (the preprocess) must be complete
+  grid_dep_wait();
+  grid_dep_launch();
   const uint32_t tmem = ctl.tmem_base;
   const WaitCtx wc{&ctl.abort_flag, a.status, a.timeout_ns};
   const int wg = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 128, 0);
@@ -775,6 +780,8 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                             const __nv_bfloat16* __restrict__ dout,
                                                             const BwdArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
   constexpr int kLanes = D / 8;                 // lanes per row
   const int64_t rows = static_cast<int64_t>(a.m.B) * a.m.H * a.npad;
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -818,6 +825,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
 template <int D>
 __global__ void __launch_bounds__(256) dq_convert_kernel(__nv_bfloat16* __restrict__ dq,
                                                         const BwdArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int64_t rows = static_cast<int64_t>(a.m.B) * a.m.H * a.m.N;
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t row = gtid / (D / 8);
@@ -859,9 +868,8 @@ cudaError_t launch_main(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s) 
   if (e != cudaSuccess) return e;
   const long long units = static_cast<long long>(a.m.nb) * a.m.B * a.m.H_kv;
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
-  bwd_bf16_kernel<D, DROP><<<grid, C::kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, tm.dout,
-                                                                 tm.dq_acc, a);
-  return cudaGetLastError();
+  return launch_pdl(bwd_bf16_kernel<D, DROP>, dim3(grid), dim3(C::kThreads), C::kSmem, s, tm.q,
+                    tm.k, tm.v, tm.dout, tm.dq_acc, a);
 }
 
 unsigned blocks_for(int64_t threads) {
@@ -875,13 +883,11 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const BwdArgs
                                   cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(a.m.B) * a.m.H * a.npad;
   const unsigned grid = blocks_for(rows * (a.d / 8));
-  if (a.d == 64)
-    bwd_preprocess_kernel<64><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
-                                                   static_cast<const __nv_bfloat16*>(dout), a);
-  else
-    bwd_preprocess_kernel<128><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
-                                                    static_cast<const __nv_bfloat16*>(dout), a);
-  return cudaGetLastError();
+  const auto* o16 = static_cast<const __nv_bfloat16*>(o);
+  const auto* g16 = static_cast<const __nv_bfloat16*>(dout);
+  return a.d == 64 ? launch_pdl(bwd_preprocess_kernel<64>, dim3(grid), dim3(256), 0, s, o16, g16, a)
+                   : launch_pdl(bwd_preprocess_kernel<128>, dim3(grid), dim3(256), 0, s, o16, g16,
+                                a);
 }
 
 cudaError_t launch_bwd_bf16(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s) {
@@ -893,11 +899,9 @@ cudaError_t launch_bwd_bf16(const TensorMaps& tm, const BwdArgs& a, cudaStream_t
 cudaError_t launch_dq_convert(void* dq, const BwdArgs& a, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(a.m.B) * a.m.H * a.m.N;
   const unsigned grid = blocks_for(rows * (a.d / 8));
-  if (a.d == 64)
-    dq_convert_kernel<64><<<grid, 256, 0, s>>>(static_cast<__nv_bfloat16*>(dq), a);
-  else
-    dq_convert_kernel<128><<<grid, 256, 0, s>>>(static_cast<__nv_bfloat16*>(dq), a);
-  return cudaGetLastError();
+  auto* dq16 = static_cast<__nv_bfloat16*>(dq);
+  return a.d == 64 ? launch_pdl(dq_convert_kernel<64>, dim3(grid), dim3(256), 0, s, dq16, a)
+                   : launch_pdl(dq_convert_kernel<128>, dim3(grid), dim3(256), 0, s, dq16, a);
 }
 
 }  // namespace attn

@@ -283,6 +283,10 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the set-up above touched no global memory: from here on the previous
+  // kernel of the stream must be complete
+  grid_dep_wait();
+  grid_dep_launch();
   const uint32_t tmem = ctl.tmem_base;
   const WaitCtx wc{&ctl.abort_flag, a.status, a.timeout_ns};
   const int wg = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 128, 0);
@@ -750,8 +754,7 @@ cudaError_t launch_one(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const long long units = static_cast<long long>((a.m.nb + 1) / 2) * a.m.B * a.m.H;
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
-  kernel<<<grid, C::kThreads, C::kSmem, s>>>(tm.q, tm.k, tm.v, a);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(grid), dim3(C::kThreads), C::kSmem, s, tm.q, tm.k, tm.v, a);
 }
 
 // V [B, H_kv, N, d] E4M3 -> V^T [B * H_kv][d][npad]: one CTA per 64 keys of

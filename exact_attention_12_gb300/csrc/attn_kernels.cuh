@@ -7,9 +7,33 @@
 
 #include <cuda_bf16.h>
 
+#include <utility>
+
 #include "philox.cuh"
 
 namespace attn {
+
+// Launch with programmatic stream serialisation: the kernel's CTAs may start
+// while the previous kernel of the stream is still running (its prologue
+// overlaps that kernel's tail, and the launch latency is hidden).  Every
+// kernel launched this way calls grid_dep_wait() before touching global
+// memory.  Captured into a CUDA graph the dependency becomes a programmatic
+// edge.
+template <typename... P, typename... A>
+inline cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, A&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
 
 constexpr int kTile = 128;            // query/key tile rows == block-mask granularity
 constexpr float kRescaleTau = 8.0f;   // lazy-rescale threshold, log2 units

@@ -139,6 +139,24 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
   return true;
 }
 
+// ------------------------------------------- programmatic dependent launch --
+
+// Wait until the grids this one depends on have completed and their writes
+// are visible.  A no-op for a launch without programmatic stream
+// serialisation; with it, every thread calls this before its first access to
+// global memory, so that transitively every earlier kernel in the stream is
+// complete too.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next kernel of the stream (launched with programmatic stream
+// serialisation) start its CTAs as resources free up; they wait in
+// grid_dep_wait() for this grid to complete.
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
