@@ -315,6 +315,10 @@ attn_status attn_fwd(const attn_params* p, const void* q, const void* k, const v
   attn::FwdArgs a{};
   a.m = mask_args(p, L, w, false);
   a.m.head_group = head_group(p, p->B * p->H, 4.0 * p->N * p->d);   // K and V, bf16
+  // key padding makes the units' costs differ by sequence: claim the
+  // longest first so that the last claims are short
+  a.len_order = (p->key_lens != nullptr && !p->causal && p->B <= attn::kLenOrderMaxB) ? 1 : 0;
+  if (a.len_order) a.m.head_group = 1;   // each head's pairs together, heads in ranked order
   a.d = p->d;
   a.scale = p->scale;
   a.scale_log2 = p->scale * kLog2e;

@@ -105,7 +105,12 @@ struct FwdCtl {
   UnitInfo unit[kUnitRing];
   uint32_t tmem_base;
   int abort_flag;
+  int16_t len_order[kLenOrderMaxB];   // sequences by descending key length (len_order mode)
 };
+
+// Named barrier between softmax warp 0 (ranks the sequences) and the
+// producer warp (reads the ranking), in len_order mode.
+constexpr int kBarLenOrder = 1;
 
 // One unit of work: a pair of query tiles of one (b, h) and their key-tile
 // lists.  Units are numbered in head groups of G consecutive (b, h), within
@@ -247,6 +252,10 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
     u.bh = g * G + rem % gs;
     u.b = u.bh / m.H;
     u.h = u.bh - u.b * m.H;
+    if (a.len_order) {   // (groups of one head) the sequences in their ranked order
+      u.b = ctl.len_order[u.b];
+      u.bh = u.b * m.H + u.h;
+    }
     u.limit = key_limit(m, u.b);
     return u;
   };
@@ -295,6 +304,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
     regs_decrease<C::kRegsOther>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
+    if (a.len_order) named_barrier_sync(kBarLenOrder, 64);   // warp 0 has ranked the sequences
     if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
@@ -515,6 +525,19 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
   }
   } else {
     regs_increase<C::kRegsSoftmax>();
+    if (a.len_order && warp == 0) {
+      // rank the sequences by descending key length (ties: lower index
+      // first) for the producer's unit_of: lane l ranks sequence l
+      const int lb = lane < m.B ? key_limit(m, lane) : -1;
+      int rank = 0;
+#pragma unroll
+      for (int o = 0; o < 32; ++o) {
+        const int lo = __shfl_sync(0xffffffffu, lb, o);
+        rank += (lo > lb || (lo == lb && o < lane)) ? 1 : 0;
+      }
+      if (lane < m.B) ctl.len_order[rank] = static_cast<int16_t>(lane);
+      named_barrier_arrive(kBarLenOrder, 64);
+    }
     // ---------------------------------------------------- softmax, epilogue
     const int x = warp >> 2;                        // query tile: 0 = A, 1 = B
     const int row = (warp & 3) * 32 + lane;         // TMEM lane == row within the tile

@@ -90,7 +90,15 @@ struct FwdArgs {
   int* status;                    // workspace status words
   int* sched;                     // workspace scheduler words: next unit, CTAs finished
   uint64_t timeout_ns;
+  // nonzero (with head_group = 1): number the units longest key range first,
+  // the sequences in descending key length (ties by index), each head's
+  // query-tile pairs together (key padding, not causal, B <= kLenOrderMaxB)
+  int len_order;
 };
+
+// Largest batch whose sequences the forward orders by key length (one warp
+// ranks them at the start of the kernel, a lane per sequence).
+constexpr int kLenOrderMaxB = 32;
 
 struct BwdArgs {
   MaskArgs m;
