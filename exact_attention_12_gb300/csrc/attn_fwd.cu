@@ -624,18 +624,6 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
             tc_fence_after();
           }
         }
-        if (jj >= 1 && __any_sync(0xffffffffu, need)) {
-          // O holds the sum through the previous key tile (complete: see above)
-  #pragma unroll
-          for (int c = 0; c < D; c += 32) {
-            uint32_t o[32];
-            tmem_ld32(oc + c, o);
-            tmem_wait_ld();
-  #pragma unroll
-            for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-            tmem_st32(oc + c, o);
-          }
-        }
         // P = 2^(S c2 - m c2) (masked entries are -inf: 2^-inf = 0), bf16 over
         // the first 64 columns of S (E4M3: the first 32)
         const float mc = (m_used == -INFINITY) ? 0.f : m_used * c2;
@@ -674,6 +662,20 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
             tmem_st16(pc + c / 2, pk);
           else
             tmem_st16(sc + c / 2, pk);   // S columns [c/2, c/2+16) are already in registers
+        }
+        if (jj >= 1 && __any_sync(0xffffffffu, need)) {
+          // O holds the sum through the previous key tile (complete: see
+          // above).  Rescaled after P is formed, so that the O columns'
+          // registers are not live together with the S row's.
+  #pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(oc + c, o);
+            tmem_wait_ld();
+  #pragma unroll
+            for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+            tmem_st32(oc + c, o);
+          }
         }
         float ls0, ls1, ls2, ls3;
         f2_unpack(acc0, ls0, ls1);
