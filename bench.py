@@ -38,7 +38,7 @@ SECONDARY = ("long-causal-16384",)
 # DRAM bytes (read + write) per launch of the backward main kernel, from the
 # ncu capture summarised in profiles/bwd_bf16_kernel_bert-large.md; absent
 # (reported as null) for other workloads or once the kernel has changed
-BWD_MAIN_TRAFFIC = {"bert-large": 112.9e6}
+BWD_MAIN_TRAFFIC = {"bert-large": 113.3e6}
 # buffer sets of the e2e leg: step k uploads into set k mod E2E_SETS while
 # step k-1 computes and step k-2 downloads, so the three overlap fully
 E2E_SETS = 3
