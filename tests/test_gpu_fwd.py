@@ -60,6 +60,18 @@ def test_key_padding_and_dropout(ea, d):
     _check_full(ea, _inputs(3, 2, 390, d, seed=11, key_lens=[390, 200, 129], dropout_p=0.1))
 
 
+@pytest.mark.parametrize("B", [32, 33])
+def test_key_padding_longest_first_order(ea, B):
+    # Non-causal key padding with up to 32 sequences numbers the forward's
+    # units longest sequence first (ranked inside the kernel); 33 sequences
+    # take the head-group order.  Tied, empty and one-key sequences, so the
+    # ranking's tie-break and the empty units are exercised.
+    g = torch.Generator().manual_seed(B)
+    choices = torch.tensor([0, 1, 128, 129, 200, 260, 260])
+    lens = choices[torch.randint(0, len(choices), (B,), generator=g)].tolist()
+    _check_full(ea, _inputs(B, 2, 260, 64, seed=14 + B, key_lens=lens, dropout_p=0.1))
+
+
 def test_padding_with_empty_and_short_rows(ea):
     # key_lens 0: every row is empty (O = 0, L = -inf); 1: one key
     _check_full(ea, _inputs(3, 1, 260, 64, seed=12, key_lens=[0, 1, 128], causal=True))
