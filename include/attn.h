@@ -55,6 +55,14 @@
  * bounded wait and records ATTN_ERR_TIMEOUT in the workspace status word,
  * which attn_check() returns.
  *
+ * CUDA graphs: attn_fwd, attn_bwd and attn_decode neither synchronise nor
+ * allocate, and every launch argument (tensor maps included) is passed by
+ * value, so the calls can be captured into a CUDA graph and replayed.  Make
+ * one uncaptured call of each kind first: it sets the kernels' attributes.
+ * The forward and backward kernels are launched with programmatic stream
+ * serialisation; each waits for the preceding work in the stream to complete
+ * before it reads or writes global memory.
+ *
  * Thread safety: calls on different workspaces may run concurrently; two
  * calls in flight on the same workspace race.
  */
