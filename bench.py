@@ -224,11 +224,18 @@ class StepGraphs:
         torch.cuda.synchronize(dev)
 
     def replay(self, steps):
-        blocks, rest = divmod(steps, self.per)
-        for _ in range(blocks):
-            self.block.replay()
-        for i in range(rest):
-            self.one[i % self.nsets].replay()
+        for kind, k in replay_plan(steps, self.per, self.nsets):
+            (self.block if kind == "block" else self.one[k]).replay()
+
+
+def replay_plan(steps, per, nsets):
+    """The graph launches that enqueue exactly `steps` steps with the input
+    sets in rotation: ("block", None) for a graph of `per` steps (a multiple
+    of `nsets`, starting at set 0), ("one", k) for a single step on set k."""
+    if per % nsets:
+        raise ValueError("a block must hold whole rotations of the input sets")
+    blocks, rest = divmod(steps, per)
+    return [("block", None)] * blocks + [("one", i % nsets) for i in range(rest)]
 
 
 def _barrier(dist):
