@@ -35,7 +35,7 @@ def _rank_main(rank, world, port, out):
 def test_two_ranks_take_the_slowest_time():
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:   # no fork of a threaded process
         out = mgr.dict()
         mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
         assert dict(out) == {0: 15.0, 1: 15.0}
