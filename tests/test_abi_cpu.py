@@ -1,7 +1,9 @@
 """The C library's host side, without a GPU: symbols, struct layout, argument checks.
 
 Every call here fails validation before anything touches the CUDA runtime,
-so none of these tests needs a device.
+or (the decode workspace size) only asks the runtime for the SM count and
+falls back to a fixed count without a device, so none of these tests needs
+a device.
 """
 
 import ctypes
@@ -158,3 +160,44 @@ def test_status_strings(abi):
     for s in range(6):
         assert lib.attn_status_string(s)
     assert lib.attn_status_string(99) == b"unknown status"
+
+
+def _decode_params(abi, **kw):
+    # 2 sequences, 8 query heads over 2 key/value heads, caches of 1000 keys
+    p = _params(abi, B=2, H=8, N=1000, d=128, H_kv=2, causal=1, key_lens=0x3000,
+                stride_b=8 * 128, stride_h=128, stride_n=128,
+                kv_stride_b=2 * 1000 * 128, kv_stride_h=1000 * 128, kv_stride_n=128)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_decode_workspace_holds_the_split_partials(abi):
+    # 4 (b, kv head) pairs x 1000 keys is far below any split target, so the
+    # cache splits into 256-key chunks whatever the device: 4 chunks, each
+    # leaving fp32 O (d) and L per query row
+    lib = abi.lib()
+    p = _decode_params(abi)
+
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    for n_q in (1, 4, 16):
+        rows = 2 * 8 * n_q
+        want = 256 + up(4 * rows * 128 * 4) + up(4 * rows * 4)
+        assert lib.attn_decode_workspace_size(ctypes.byref(p), n_q) == want, n_q
+
+
+@pytest.mark.parametrize("kw,n_q,status", [
+    (dict(dropout_p=0.1), 1, 2), (dict(block_mask=0x2000), 1, 2), (dict(key_lens=None), 1, 1),
+    (dict(), 0, 1), (dict(), 17, 2),            # (H / H_kv) * n_q = 68 > 64 rows
+    (dict(dtype=1), 1, 2), (dict(d=96), 1, 2),
+])
+def test_decode_options_checked_on_the_host(abi, kw, n_q, status):
+    lib = abi.lib()
+    p = _decode_params(abi, **kw)
+    assert lib.attn_decode_workspace_size(ctypes.byref(p), n_q) == 0
+    fake = ctypes.c_void_p(0x1000)
+    st = lib.attn_decode(ctypes.byref(p), n_q, fake, fake, fake, fake, fake, fake, 1 << 30, None)
+    assert st == status, lib.attn_last_error()
+    assert lib.attn_last_error()
