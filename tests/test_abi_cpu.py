@@ -201,3 +201,20 @@ def test_decode_options_checked_on_the_host(abi, kw, n_q, status):
     st = lib.attn_decode(ctypes.byref(p), n_q, fake, fake, fake, fake, fake, fake, 1 << 30, None)
     assert st == status, lib.attn_last_error()
     assert lib.attn_last_error()
+
+
+def test_noalloc_backward_checks_on_the_host(abi):
+    lib = abi.lib()
+    fake = ctypes.c_void_p(0x1000)
+    # invalid parameters: the ordinary backward's status and message
+    p = _params(abi, d=96)
+    assert lib.attn_bwd_noalloc(ctypes.byref(p), *([fake] * 10), None) == \
+        abi.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_last_error()
+    # a problem whose scratch (here the 64 MiB fp32 dQ accumulator alone)
+    # exceeds the built-in 64 MiB is refused before anything is enqueued
+    p = _params(abi, B=1, H=16, N=8192, d=128, stride_b=16 * 8192 * 128, stride_h=8192 * 128,
+                stride_n=128)
+    assert lib.attn_workspace_size(ctypes.byref(p), 1) > 64 * 2 ** 20
+    assert lib.attn_bwd_noalloc(ctypes.byref(p), *([fake] * 10), None) == abi.ATTN_ERR_WORKSPACE
+    assert b"built-in scratch" in lib.attn_last_error()
