@@ -19,6 +19,7 @@ _FP8 = getattr(torch, "float8_e4m3fn", None)
 if _FP8 is not None:
     _DTYPES[_FP8] = _abi.ATTN_FP8_E4M3
 _workspaces = {}
+_retired = {}
 
 
 def workspace(device, nbytes):
@@ -26,12 +27,19 @@ def workspace(device, nbytes):
 
     The cached buffer is shared by every call on that device that does not
     pass its own workspace, so calls that overlap on different streams must
-    pass separate workspaces.
+    pass separate workspaces.  When a call needs more, the cache grows to at
+    least twice its size; the buffer it replaces stays allocated for the life
+    of the process, because a CUDA graph captured earlier still holds its
+    address.
     """
-    key = torch.device(device).index
+    dev = torch.device(device)
+    key = (dev.type, dev.index)
     t = _workspaces.get(key)
     if t is None or t.numel() < nbytes:
-        t = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+        size = max(int(nbytes), 256, 0 if t is None else 2 * t.numel())
+        if t is not None:
+            _retired.setdefault(key, []).append(t)
+        t = torch.zeros(size, dtype=torch.uint8, device=dev)
         _workspaces[key] = t
     return t
 

@@ -1,5 +1,6 @@
-"""The bench's host bookkeeping on CPU: the graph-replay plan and the FLOP
-accounting that turns times into TFLOP/s."""
+"""Host bookkeeping on CPU: the bench's graph-replay plan and the FLOP
+accounting that turns times into TFLOP/s, and the Python binding's shared
+workspace cache."""
 
 import pytest
 import torch
@@ -49,3 +50,24 @@ def test_block_sparse_flops_count_kept_blocks_only():
     bm[3, 7] = 1
     assert bench.fwd_flops(w, block_mask=bm) == pytest.approx(
         4 * w.d * w.B * w.H * 2 * 128 * 128)
+
+
+def test_cached_workspace_grows_and_keeps_what_it_replaced():
+    # the binding's shared workspace (exercised on the CPU device): replaced
+    # buffers stay referenced, since a captured CUDA graph may still use them
+    from exact_attention_12_gb300 import api
+    dev = torch.device("cpu")
+    key = (dev.type, dev.index)
+    api._workspaces.pop(key, None)
+    api._retired.pop(key, None)
+    a = api.workspace(dev, 1000)
+    assert a.numel() == 1000 and not a.any()
+    assert api.workspace(dev, 600) is a                 # big enough: reused
+    b = api.workspace(dev, 1500)
+    assert b.numel() == 2000                            # grows at least twofold
+    assert len(api._retired[key]) == 1 and api._retired[key][0] is a
+    c = api.workspace(dev, 10 ** 5)
+    assert c.numel() == 10 ** 5
+    assert [id(t) for t in api._retired[key]] == [id(a), id(b)]
+    api._workspaces.pop(key, None)
+    api._retired.pop(key, None)
