@@ -27,9 +27,10 @@ Modules
                 OFP8 format), and the terms of the error bound for a kernel
                 that rounds the probabilities to E4M3.
 
-Parity status: the Philox constants are not pinned to published known-answer
-vectors (none are available here); "parity partly unpinned" for `philox`.
-Everything else is pinned by tests under tests/test_oracle_*.py.
+Parity status: every function is pinned by tests under tests/test_oracle_*.py;
+`philox` against cuRAND's host-side Philox4x32-10 generator, an independent
+implementation of the same published generator (no published known-answer
+vector file is available here).
 """
 
 from .attention import (  # noqa: F401

@@ -16,8 +16,10 @@ applies ten rounds (nine key bumps).
 
 Two implementations live here: `philox4x32_10` (vectorised numpy, uint64
 arithmetic masked to 32 bits) and `philox4x32_10_scalar` (Python integers).
-Tests require them to agree.  Parity partly unpinned: no published known-answer
-vectors are available to check the constants against.
+Tests require them to agree, and pin both to cuRAND's host-side Philox4x32-10
+generator (an independent implementation of the same published generator,
+run on the CPU): its first output blocks are the counters (0, 0, i, 0) under
+the key (seed low word, seed high word).
 """
 
 import numpy as np

@@ -443,6 +443,54 @@ def test_philox_output_bits_are_balanced():
     assert abs(flips - 0.5) < 0.01
 
 
+def _curand_host_philox(seed, nwords):
+    """`nwords` 32-bit outputs of cuRAND's host-side Philox4x32-10 generator
+    (CURAND_RNG_PSEUDO_PHILOX4_32_10 = 161 in curand.h), which runs on the
+    CPU without a device.  None if the library cannot be loaded."""
+    import ctypes
+    import ctypes.util
+    names = [ctypes.util.find_library("curand"), "/usr/local/cuda/lib64/libcurand.so",
+             "/usr/local/cuda/lib64/libcurand.so.10", "libcurand.so.10"]
+    lib = None
+    for n in names:
+        if not n:
+            continue
+        try:
+            lib = ctypes.CDLL(n)
+            break
+        except OSError:
+            continue
+    if lib is None:
+        return None
+    gen = ctypes.c_void_p()
+    if lib.curandCreateGeneratorHost(ctypes.byref(gen), 161) != 0:
+        return None
+    try:
+        assert lib.curandSetPseudoRandomGeneratorSeed(gen, ctypes.c_ulonglong(seed)) == 0
+        buf = (ctypes.c_uint * nwords)()
+        assert lib.curandGenerate(gen, buf, ctypes.c_size_t(nwords)) == 0
+        return np.array(list(buf), dtype=np.uint64)
+    finally:
+        lib.curandDestroyGenerator(gen)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 0x123456789ABCDEF0, 2 ** 64 - 1])
+def test_philox_matches_an_independent_implementation(seed):
+    # cuRAND's host generator implements the same published Philox4x32-10.
+    # Its first 64 output blocks of four words come from counters
+    # (0, 0, i, 0), i = 0..63 (the subsequence index in counter word 2), with
+    # the seed's low and high 32 bits as the key.  A wrong multiplier, Weyl
+    # constant, word order or round count changes every block.
+    words = _curand_host_philox(seed, 4 * 64)
+    if words is None:
+        pytest.skip("cuRAND's host generator is not available")
+    k0, k1 = seed & 0xFFFFFFFF, seed >> 32
+    i = np.arange(64, dtype=np.uint64)
+    got = philox4x32_10(np.zeros(64, dtype=np.uint64), 0, i, 0, k0, k1)
+    assert np.array_equal(np.stack(got, axis=1).reshape(-1), words)
+    assert philox4x32_10_scalar((0, 0, 5, 0), (k0, k1)) == tuple(int(x) for x in words[20:24])
+
+
 # ------------------------------------------------------ grouped-query heads --
 # "3.3 Hiểu sâu cơ chế Self-Attention", §9.2-9.3: groups of query heads share
 # one key/value head; one group per head is MHA, a single group is MQA.
