@@ -9,6 +9,10 @@ O_MAX_ABS = 1e-2      # forward output: max |O_gpu - O_oracle| beyond the output
 BF16_HALF_ULP_REL = 2.0 ** -8   # one round-to-nearest into bf16, relative
 L_MAX_ABS = 1e-3      # logsumexp, max |L_gpu - L_oracle|
 GRAD_REL_L2 = 1e-2    # dQ, dK, dV: ||g_gpu - g_oracle|| / ||g_oracle||
+# Below this magnitude half a bf16 ulp of the output (<= 2^-8 |O|) stays at
+# or under half of O_MAX_ABS, so there the plain bound |O_gpu - O_oracle| <=
+# O_MAX_ABS is checked as well, with nothing subtracted.
+O_PLAIN_BELOW = 1.28
 
 
 def np64(t):
@@ -45,6 +49,34 @@ def o_err(got, want, out_bf16=True):
     slack = BF16_HALF_ULP_REL * np.abs(want) if out_bf16 else 0.0
     d = np.abs(got - want) - slack
     return float(np.max(np.where(np.isnan(d), np.inf, d)))
+
+
+def o_plain_err(got, want):
+    """Max |got - want| over the elements with |want| < O_PLAIN_BELOW (no slack)."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    sel = np.abs(want) < O_PLAIN_BELOW
+    return max_abs(got[sel], want[sel]) if sel.any() else 0.0
+
+
+def assert_o(got, want, out_bf16=True, what=""):
+    """The forward-output bar: within O_MAX_ABS beyond the output's own bf16
+    rounding everywhere, and within plain O_MAX_ABS where |O| < O_PLAIN_BELOW."""
+    e1 = o_err(got, want, out_bf16)
+    e2 = o_plain_err(got, want)
+    assert e1 <= O_MAX_ABS and e2 <= O_MAX_ABS, (what, e1, e2)
+    return e1, e2
+
+
+def tile_samples(N, seed, tile=128):
+    """Row (or key) indices that reach every 128-row tile of a length-N
+    sequence: one random index inside each tile, plus the first and last
+    index of the sequence and of its first and last tiles."""
+    rng = np.random.default_rng(seed)
+    nb = (N + tile - 1) // tile
+    idx = {min(N - 1, tile * t + int(rng.integers(tile))) for t in range(nb)}
+    idx |= {0, min(tile - 1, N - 1), tile * (nb - 1), N - 1}
+    return np.array(sorted(idx))
 
 
 def rel_l2(a, b):

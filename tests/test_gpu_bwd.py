@@ -6,7 +6,7 @@ import torch
 
 import workloads
 from oracle import attention as oracle
-from tests.helpers import GRAD_REL_L2, api_kwargs, np64, oracle_kwargs, rel_l2
+from tests.helpers import GRAD_REL_L2, api_kwargs, np64, oracle_kwargs, rel_l2, tile_samples
 
 pytestmark = pytest.mark.gpu
 
@@ -20,10 +20,13 @@ def ea():
 
 
 def _run(ea, inp):
+    """Forward and backward; the gradients go into buffers pre-filled with
+    NaN, so that an element the kernels never write shows up as NaN."""
     q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
     kw = api_kwargs(inp)
     o, lse = ea.attention_fwd(q, k, v, **kw)
-    dq, dk, dv = ea.attention_bwd(do, q, k, v, o, lse, **kw)
+    dq, dk, dv = (torch.full_like(t, float("nan")) for t in (q, k, v))
+    ea.attention_bwd(do, q, k, v, o, lse, dq=dq, dk=dk, dv=dv, **kw)
     torch.cuda.synchronize()
     ea.check()
     return o.cpu(), lse.cpu(), dq.cpu(), dk.cpu(), dv.cpu()
@@ -103,29 +106,82 @@ def test_repeatable(ea):
     assert rel_l2(np64(a[2]), np64(b[2])) < 1e-3
 
 
-def _sample(N, seed, k=10):
-    rng = np.random.default_rng(seed)
-    fixed = {0, 127, 128, N // 2, N - 1}
-    return np.array(sorted({x for x in fixed if 0 <= x < N} | set(rng.integers(0, N, k).tolist())))
-
-
-@pytest.mark.parametrize("name", ["bert-large", "gpt2-1k", "gpt2-4k", "long-causal-4096",
+@pytest.mark.parametrize("name", ["bert-large", "gpt2-1k", "gpt2-4k", "long-causal-512",
+                                  "long-causal-1024", "long-causal-2048", "long-causal-4096",
                                   "long-causal-8192", "long-causal-16384", "block-sparse-64k"])
 def test_full_size_workload_sampled(ea, name):
+    """The bench's workloads at full size: in three heads, dQ of one row in
+    every query tile and dK, dV of one key in every key tile (each key tile
+    is a unit of the persistent backward, claimed by different CTAs in
+    different orders) against the oracle; every gradient element written
+    (the outputs start as NaN)."""
     w = workloads.get(name)
     inp = workloads.make_inputs(w)
     _, _, dq, dk, dv = _run(ea, inp)
+    for t in (dq, dk, dv):
+        assert not torch.isnan(t).any(), name
     q, k, v, do = (np64(inp[n]) for n in ("q", "k", "v", "do"))
     kw = oracle_kwargs(inp)
-    for b, h in {(0, 0), (w.B - 1, w.H - 1)}:
-        rows = _sample(w.N, 7 + b * 31 + h)
+    rng = np.random.default_rng(7)
+    heads = {(0, 0), (w.B - 1, w.H - 1)}
+    while len(heads) < min(3, w.B * w.H):
+        heads.add((int(rng.integers(w.B)), int(rng.integers(w.H))))
+    for b, h in sorted(heads):
+        rows = tile_samples(w.N, 7 + b * 31 + h)
+        keys = tile_samples(w.N, 1000 + b * 31 + h)
         dQ = oracle.backward_rows(q, k, v, do, b, h, rows, **kw)
-        dK, dV = oracle.backward_keys(q, k, v, do, b, h, rows, **kw)
-        errs = (rel_l2(np64(dq[b, h, rows]), dQ), rel_l2(np64(dk[b, h, rows]), dK),
-                rel_l2(np64(dv[b, h, rows]), dV))
+        dK, dV = oracle.backward_keys(q, k, v, do, b, h, keys, **kw)
+        errs = (rel_l2(np64(dq[b, h, rows]), dQ), rel_l2(np64(dk[b, h, keys]), dK),
+                rel_l2(np64(dv[b, h, keys]), dV))
         assert max(errs) <= GRAD_REL_L2, (name, b, h, errs)
-    for t in (dq, dk, dv):
-        assert torch.isfinite(t.float()).all()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_keep_bits_are_exact(ea, d, causal):
+    """The backward's own dropout keep mask, bit-exactly through the public API.
+
+    The backward regenerates Z by its own route (one Philox call shared by
+    eight lanes, then a bit transpose), so it is checked on its own.  With
+    Q = K = 0 every allowed score is 0, so P_ij = 1 / n_allowed(i), and
+    dV = P~^T dO with P~_ij = Z_ij P_ij / (1 - p').  Making dO the indicator
+    of query row q0 + c in column c turns dV[j, c] into P~[q0 + c, j]:
+    nonzero exactly where key j is allowed for, and kept at, query q0 + c.
+    One call per block of d query rows reads the whole pattern, which must
+    equal the oracle's allowed mask AND keep mask element for element, with
+    key padding, a block mask and (parametrised) the causal mask.
+    """
+    B, H, N = 2, 2, 384
+    key_lens = torch.tensor([384, 250], dtype=torch.int32)
+    bm = torch.tensor([[1, 0, 1], [1, 1, 0], [0, 1, 1]], dtype=torch.uint8)
+    p, seed, offset = 0.25, 0xDEADBEEF12345, 9
+    kw = dict(scale=0.1, causal=causal, key_lens=key_lens.cuda(), block_mask=bm.cuda(),
+              dropout_p=p, seed=seed, offset=offset)
+    z = torch.zeros(B, H, N, d, dtype=torch.bfloat16, device="cuda")
+    g = torch.Generator().manual_seed(d)
+    v = torch.randn(B, H, N, d, generator=g).to(torch.bfloat16).cuda()
+    o, lse = ea.attention_fwd(z, z, v, **kw)
+    got = np.zeros((B, H, N, N), dtype=bool)      # [b, h, query, key]
+    idx = torch.arange(d)
+    for q0 in range(0, N, d):
+        do = torch.zeros(B, H, N, d, dtype=torch.bfloat16)
+        do[:, :, q0 + idx, idx] = 1.0
+        dq, dk, dv = ea.attention_bwd(do.cuda(), z, z, v, o, lse, **kw)
+        torch.cuda.synchronize()
+        ea.check()
+        # dv[b, h, j, c] = P~[q0 + c, j]
+        got[:, :, q0:q0 + d, :] = (dv.cpu().float().numpy() != 0).transpose(0, 1, 3, 2)
+        # Q = K = 0: dQ = c dS K and dK = c dS^T Q vanish
+        assert not dq.any() and not dk.any()
+    want = np.zeros_like(got)
+    for b in range(B):
+        for h in range(H):
+            allowed = oracle.allowed_mask(np.arange(N), np.arange(N), causal, int(key_lens[b]),
+                                          bm.numpy())
+            keep = oracle.keep_mask(np.arange(N), np.arange(N), b * H + h, seed, offset, p)
+            want[b, h] = allowed & keep
+    assert want.any() and not want.all()
+    assert np.array_equal(got, want), int((got != want).sum())
 
 
 def test_strided_bnhd_layout(ea):

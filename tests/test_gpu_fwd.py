@@ -6,8 +6,8 @@ import torch
 
 import workloads
 from oracle import attention as oracle
-from tests.helpers import (L_MAX_ABS, O_MAX_ABS, api_kwargs, max_abs, np64, o_err,
-                           oracle_kwargs)
+from tests.helpers import (L_MAX_ABS, api_kwargs, assert_o, max_abs, np64, oracle_kwargs,
+                           tile_samples)
 
 pytestmark = pytest.mark.gpu
 
@@ -22,8 +22,12 @@ def ea():
 
 
 def _run_fwd(ea, inp):
+    """The forward into outputs pre-filled with NaN, so that an element the
+    kernels never write shows up as NaN."""
     q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
-    o, lse = ea.attention_fwd(q, k, v, **api_kwargs(inp))
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device=q.device)
+    ea.attention_fwd(q, k, v, out=o, lse=lse, **api_kwargs(inp))
     torch.cuda.synchronize()
     ea.check()
     return o.cpu(), lse.cpu()
@@ -42,9 +46,9 @@ def _check_full(ea, inp):
     o, lse = _run_fwd(ea, inp)
     O, L = oracle.attention_forward(np64(inp["q"]), np64(inp["k"]), np64(inp["v"]),
                                     **oracle_kwargs(inp))
-    eo = o_err(np64(o), O, out_bf16=o.dtype == torch.bfloat16)
+    eo = assert_o(np64(o), O, out_bf16=o.dtype == torch.bfloat16)
     el = max_abs(lse.numpy(), L)
-    assert eo <= O_MAX_ABS and el <= L_MAX_ABS, (eo, el)
+    assert el <= L_MAX_ABS, el
     return eo, el
 
 
@@ -134,7 +138,7 @@ def test_strided_bnhd_layout(ea):
     o, lse = ea.attention_fwd(qd.transpose(1, 2), kd.transpose(1, 2), vd.transpose(1, 2),
                               scale=0.125, causal=True)
     O, L = oracle.attention_forward(np64(q), np64(k), np64(v), **oracle_kwargs(inp))
-    assert o_err(np64(o.cpu()), O) <= O_MAX_ABS
+    assert_o(np64(o.cpu()), O)
     assert max_abs(lse.cpu().numpy(), L) <= L_MAX_ABS
 
 
@@ -180,29 +184,27 @@ def test_empty_problem_sizes(ea):
 
 # ------------------------------------------------- full-size workloads ----
 
-def _sampled_rows(N, seed):
-    rng = np.random.default_rng(seed)
-    fixed = {0, 1, 127, 128, 129, N // 2, N - 129, N - 128, N - 1}
-    rows = sorted({r for r in fixed if 0 <= r < N} | set(rng.integers(0, N, 12).tolist()))
-    return np.array(rows)
-
-
 @pytest.mark.parametrize("name", ["bert-large", "gpt2-1k", "gpt2-4k", "long-causal-512",
                                   "long-causal-1024", "long-causal-2048", "long-causal-4096",
                                   "long-causal-8192", "long-causal-16384", "block-sparse-64k"])
 def test_full_size_workload_sampled(ea, name):
+    """The bench's workloads at full size: in four heads, one row in every
+    query tile (the persistent scheduler hands the tiles to different CTAs
+    in different orders) against the oracle; every element of O and L
+    written (the outputs start as NaN)."""
     w = workloads.get(name)
     inp = workloads.make_inputs(w)
     o, lse = _run_fwd(ea, inp)
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any(), name
     q, k, v = np64(inp["q"]), np64(inp["k"]), np64(inp["v"])
     kw = oracle_kwargs(inp)
     rng = np.random.default_rng(5)
-    heads = {(0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))}
-    for b, h in heads:
-        rows = _sampled_rows(w.N, b * 100 + h)
+    heads = {(0, 0), (w.B - 1, w.H - 1)}
+    while len(heads) < min(4, w.B * w.H):
+        heads.add((int(rng.integers(w.B)), int(rng.integers(w.H))))
+    for b, h in sorted(heads):
+        rows = tile_samples(w.N, b * 100 + h)
         O, L = oracle.forward_rows(q, k, v, b, h, rows, **kw)
-        eo = o_err(np64(o[b, h, rows]), O)
+        assert_o(np64(o[b, h, rows]), O, what=(name, b, h))
         el = max_abs(lse[b, h, rows].numpy(), L)
-        assert eo <= O_MAX_ABS and el <= L_MAX_ABS, (name, b, h, eo, el)
-    # every row of the output is finite (no unwritten or NaN rows)
-    assert torch.isfinite(o.float()).all()
+        assert el <= L_MAX_ABS, (name, b, h, el)
