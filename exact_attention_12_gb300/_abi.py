@@ -20,6 +20,10 @@ ATTN_BF16 = 0
 ATTN_FP32 = 1
 ATTN_FP8_E4M3 = 2
 
+ATTN_STALL_NONE = 0
+ATTN_STALL_FWD_SOFTMAX = 1
+ATTN_STALL_BWD_COMPUTE = 2
+
 # every function the header declares, with its ctypes signature
 EXPORTS = {
     "attn_workspace_size": (ctypes.c_size_t, [ctypes.c_void_p, ctypes.c_int]),
@@ -33,6 +37,7 @@ EXPORTS = {
     "attn_decode": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32] + [ctypes.c_void_p] * 6
                     + [ctypes.c_size_t, ctypes.c_void_p]),
     "attn_selftest_timeout": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]),
+    "attn_debug_stall": (ctypes.c_int, [ctypes.c_int32, ctypes.c_uint64]),
     "attn_check": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_last_error": (ctypes.c_char_p, []),

@@ -17,6 +17,22 @@ using attn::kTile;
 
 thread_local std::string g_last_error;
 
+// A test stall armed by attn_debug_stall for the next launch of the named
+// kernel on this host thread, and the wait limit that launch gets.
+thread_local int g_stall = attn::kStallNone;
+thread_local uint64_t g_stall_limit_ns = 0;
+
+// Takes the armed stall if it names `which`: sets the launch's stall and
+// wait limit, and disarms it.
+template <typename Args>
+void take_stall(int which, Args* a) {
+  if (g_stall == which && which != attn::kStallNone) {
+    a->stall = which;
+    a->timeout_ns = g_stall_limit_ns;
+    g_stall = attn::kStallNone;
+  }
+}
+
 attn_status fail(attn_status s, const char* fmt, ...) {
   char buf[512];
   va_list ap;
@@ -378,6 +394,7 @@ attn_status attn_fwd(const attn_params* p, const void* q, const void* k, const v
                                   reinterpret_cast<uint16_t*>(w + L.list_idx), s);
     if (e != cudaSuccess) return cuda_fail(e, "block-mask compaction launch");
   }
+  take_stall(attn::kStallFwdSoftmax, &a);
   e = fp8 ? attn::launch_fwd_fp8(tm, a, s) : attn::launch_fwd_bf16(tm, a, s);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "forward launch");
 }
@@ -465,6 +482,7 @@ attn_status attn_bwd_main(const attn_params* p, const void* q, const void* k, co
                                   reinterpret_cast<uint16_t*>(w + L.list_idx), s);
     if (e != cudaSuccess) return cuda_fail(e, "block-mask compaction launch");
   }
+  take_stall(attn::kStallBwdCompute, &a);
   e = attn::launch_bwd_bf16(tm, a, s);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "backward launch");
 }
@@ -602,8 +620,22 @@ attn_status attn_decode(const attn_params* p, int32_t n_q, const void* q, const 
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "decode launch");
 }
 
+attn_status attn_debug_stall(int32_t which, uint64_t limit_ns) {
+  if (which != ATTN_STALL_NONE && which != ATTN_STALL_FWD_SOFTMAX &&
+      which != ATTN_STALL_BWD_COMPUTE)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown stall %d", which);
+  if (limit_ns < 1000000ull) limit_ns = 1000000ull;          // 1 ms
+  if (limit_ns > kTimeoutNs) limit_ns = kTimeoutNs;          // 2 s
+  g_stall = which;
+  g_stall_limit_ns = limit_ns;
+  return ATTN_OK;
+}
+
 attn_status attn_check(void* ws, void* stream) {
-  if (ws == nullptr) return fail(ATTN_ERR_WORKSPACE, "workspace is NULL");
+  if (ws == nullptr) {   // the built-in scratch of attn_bwd_noalloc on this device
+    const attn_status st = static_cast<attn_status>(attn::builtin_scratch(&ws));
+    if (st != ATTN_OK) return st;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");

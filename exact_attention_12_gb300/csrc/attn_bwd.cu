@@ -649,7 +649,10 @@ __global__ void __launch_bounds__(384, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.pfull);
+      // (an armed test stall: warp 0 withholds its first arrive, so the MMA
+      // warp's wait runs out and the CTA takes its time-out path)
+      if (lane == 0 && !(a.stall == kStallBwdCompute && warp == 0 && it == 0))
+        mbar_arrive(&ctl.pfull);
 
       if (i >= 1) {   // dQ of the previous query tile: its dS^T is consumed
         ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dqfull, (it - 1) & 1, wc, kSiteBwdDq));

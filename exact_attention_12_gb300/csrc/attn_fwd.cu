@@ -686,7 +686,10 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.pfull[x]);
+        // (an armed test stall: warp 0 withholds its first arrive, so the MMA
+        // warp's wait runs out and the CTA takes its time-out path)
+        if (lane == 0 && !(a.stall == kStallFwdSoftmax && warp == 0 && cs == 0))
+          mbar_arrive(&ctl.pfull[x]);
       }
       if (!ok) break;
       if (any) {   // every warp takes every phase of `done`, so none falls two behind

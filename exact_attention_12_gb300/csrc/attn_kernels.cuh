@@ -47,6 +47,11 @@ enum WaitSite : int {
   kSiteDecode = 40
 };
 
+// One-shot stalls armed by attn_debug_stall (a test of the kernels' own
+// time-out path): the named role withholds one barrier arrive in its first
+// tile, so the wait on that barrier runs out.
+enum StallSite : int { kStallNone = 0, kStallFwdSoftmax = 1, kStallBwdCompute = 2 };
+
 // Device status code for a kernel that found its shared memory misaligned
 // and returned without doing anything (equals ATTN_ERR_CUDA in attn.h).
 constexpr int kStatusSmemAlign = 3;
@@ -94,6 +99,7 @@ struct FwdArgs {
   // the sequences in descending key length (ties by index), each head's
   // query-tile pairs together (key padding, not causal, B <= kLenOrderMaxB)
   int len_order;
+  int stall;                      // kStallFwdSoftmax: softmax warp 0 withholds its first P-ready arrive
 };
 
 // Largest batch whose sequences the forward orders by key length (one warp
@@ -118,6 +124,7 @@ struct BwdArgs {
   int* status;
   int* sched;                     // workspace scheduler words: next unit, CTAs finished
   uint64_t timeout_ns;
+  int stall;                      // kStallBwdCompute: compute warp 0 withholds its first P-ready arrive
 };
 
 // Decode step: query rows per CTA (the key/value group's heads x n_q) at most.
@@ -171,5 +178,9 @@ cudaError_t launch_decode(const TensorMaps& tm, void* o, float* lse, const Decod
 // Records `msg` as the calling thread's last error (what attn_last_error()
 // returns) and passes `status` through.
 int record_error(int status, const char* msg);
+
+// Device address of attn_bwd_noalloc's built-in scratch on the current
+// device (looked up once per device); an attn_status.
+int builtin_scratch(void** out);
 
 }  // namespace attn

@@ -32,9 +32,12 @@ constexpr int kMaxDevices = 64;
 void* g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mutex;
 
+}  // namespace
+
 // Device address of the scratch on the current device; looked up once per
-// device (with that device current) and cached.
-attn_status scratch_address(void** out) {
+// device (with that device current) and cached.  attn_check(NULL, ...)
+// reads the status words at its start through it.
+int attn::builtin_scratch(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) {
@@ -61,8 +64,6 @@ attn_status scratch_address(void** out) {
   return ATTN_OK;
 }
 
-}  // namespace
-
 extern "C" attn_status attn_bwd_noalloc(const attn_params* p, const void* q, const void* k,
                                         const void* v, const void* o, const float* lse,
                                         const void* dout, void* dq, void* dk, void* dv,
@@ -79,7 +80,7 @@ extern "C" attn_status attn_bwd_noalloc(const attn_params* p, const void* q, con
     return static_cast<attn_status>(attn::record_error(ATTN_ERR_WORKSPACE, msg));
   }
   void* ws = nullptr;
-  attn_status st = scratch_address(&ws);
+  const attn_status st = static_cast<attn_status>(attn::builtin_scratch(&ws));
   if (st != ATTN_OK) return st;
   // the status words must start at zero; a previous call may have left a
   // time-out recorded there (every other part of the scratch is rewritten)

@@ -197,8 +197,9 @@ attn_status attn_bwd_dq(const attn_params* p, void* dq, void* ws,
  *     contents: calls that overlap on the GPU (other streams, other host
  *     threads) race with each other.  The call clears the status words and
  *     rewrites everything else it reads.
- *   - A device-side time-out is recorded in the built-in array's status words,
- *     which callers cannot pass to attn_check; it is cleared by the next call. */
+ *   - A device-side time-out is recorded in the built-in array's status
+ *     words: attn_check(NULL, stream) reports it (and clears it).  The next
+ *     attn_bwd_noalloc call clears it too, so check before the next call. */
 attn_status attn_bwd_noalloc(const attn_params* p, const void* q,
                              const void* k, const void* v, const void* o,
                              const float* lse, const void* dout, void* dq,
@@ -235,8 +236,34 @@ attn_status attn_decode(const attn_params* p, int32_t n_q, const void* q, const 
  * attn_check returns ATTN_ERR_TIMEOUT.  `ws` needs 256 bytes. */
 attn_status attn_selftest_timeout(void* ws, uint64_t limit_ns, void* stream);
 
+/* Test hook for the time-out path of the attention kernels themselves (the
+ * pages have no counterpart: this checks this library's failure detection).
+ * Arms a one-shot stall for the next launch of the named kernel made by a
+ * call on the calling host thread:
+ *   ATTN_STALL_FWD_SOFTMAX  the forward (attn_fwd, bf16 or fp8): in every CTA,
+ *                           softmax warp 0 withholds its "P ready" arrive for
+ *                           its first key tile;
+ *   ATTN_STALL_BWD_COMPUTE  the backward main kernel (attn_bwd, attn_bwd_main,
+ *                           attn_bwd_noalloc): in every CTA, compute warp 0
+ *                           withholds its "P ready" arrive for its first
+ *                           query tile.
+ * The MMA warp's wait on that barrier then runs out; every wait of that launch
+ * gives up after `limit_ns` (clamped to [1 ms, 2 s]).  The kernel drains its
+ * copies and MMAs, frees its tensor memory and returns, and the status words
+ * of the call's workspace hold ATTN_ERR_TIMEOUT and the wait site, which
+ * attn_check reports.  That call's outputs are undefined; later calls are
+ * unaffected.  Nothing faults, traps or hangs.  ATTN_STALL_NONE disarms;
+ * other values give ATTN_ERR_INVALID_ARG. */
+typedef enum {
+  ATTN_STALL_NONE = 0,
+  ATTN_STALL_FWD_SOFTMAX = 1,
+  ATTN_STALL_BWD_COMPUTE = 2
+} attn_stall;
+attn_status attn_debug_stall(int32_t which, uint64_t limit_ns);
+
 /* Synchronises `stream`, returns the workspace's device status (ATTN_OK or
- * ATTN_ERR_TIMEOUT) and clears it. */
+ * ATTN_ERR_TIMEOUT) and clears it.  ws = NULL: the status of
+ * attn_bwd_noalloc's built-in scratch on the current device. */
 attn_status attn_check(void* ws, void* stream);
 
 /* Static description of a status code. */

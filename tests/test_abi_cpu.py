@@ -218,3 +218,12 @@ def test_noalloc_backward_checks_on_the_host(abi):
     assert lib.attn_workspace_size(ctypes.byref(p), 1) > 64 * 2 ** 20
     assert lib.attn_bwd_noalloc(ctypes.byref(p), *([fake] * 10), None) == abi.ATTN_ERR_WORKSPACE
     assert b"built-in scratch" in lib.attn_last_error()
+
+
+def test_debug_stall_is_checked_on_the_host(abi):
+    # arming touches no device: unknown kernels are refused, NONE disarms
+    lib = abi.lib()
+    assert lib.attn_debug_stall(7, 20_000_000) == abi.ATTN_ERR_INVALID_ARG
+    assert b"unknown stall" in lib.attn_last_error()
+    assert lib.attn_debug_stall(abi.ATTN_STALL_FWD_SOFTMAX, 0) == abi.ATTN_OK
+    assert lib.attn_debug_stall(abi.ATTN_STALL_NONE, 0) == abi.ATTN_OK
