@@ -34,14 +34,29 @@ import workloads  # noqa: E402
 METRIC = "attention fwd+bwd TFLOPS (bf16, causal/non-causal) & % of GB300 dense BF16 peak"
 SPEC_BF16_TFLOPS = 2250.0
 L2_BYTES = 129 * 2 ** 20
-SECONDARY = ("long-causal-16384",)
-# DRAM bytes (read + write) per launch of the backward main kernel, from the
-# ncu capture summarised in profiles/bwd_bf16_kernel_bert-large.md; absent
-# (reported as null) for other workloads or once the kernel has changed
-BWD_MAIN_TRAFFIC = {"bert-large": 113.3e6}
+# the headline: causal, d = 128, the longest sequence of the long-context
+# sweep (the largest configuration that fits one GPU)
+DEFAULT_WORKLOAD = "long-causal-16384"
+# measured beside it, each with its own clocks and roofline
+SECONDARY = ("bert-large", "gpt2-1k", "long-causal-4096")
+# sequences up to this length sit below the ridge point of the roofline
+# (about N / 2 FLOP per byte in the forward): their HBM GB/s is reported too
+SHORT_N = 1024
 # buffer sets of the e2e leg: step k uploads into set k mod E2E_SETS while
 # step k-1 computes and step k-2 downloads, so the three overlap fully
 E2E_SETS = 3
+# the sources each kernel is built from: a traffic figure taken by ncu
+# counts only while their hash is the one recorded beside it
+CSRC = os.path.join(ROOT, "exact_attention_12_gb300", "csrc")
+KERNEL_SOURCES = {
+    "fwd_bf16_kernel": ("attn_fwd.cu", "attn_kernels.cuh", "sm103.cuh", "philox.cuh"),
+    "bwd_bf16_kernel": ("attn_bwd.cu", "attn_kernels.cuh", "sm103.cuh", "philox.cuh"),
+    "bwd_preprocess_kernel": ("attn_bwd.cu", "attn_kernels.cuh"),
+    "dq_convert_kernel": ("attn_bwd.cu", "attn_kernels.cuh"),
+}
+STAGE_KERNELS = ("fwd_bf16_kernel", "bwd_preprocess_kernel", "bwd_bf16_kernel",
+                 "dq_convert_kernel")
+PROFILES = os.path.join(ROOT, "profiles")
 
 
 # ----------------------------------------------------------------- FLOPs --
@@ -68,6 +83,70 @@ def fwd_flops(w, key_lens=None, block_mask=None):
     return 4.0 * d * pairs
 
 
+def stage_bytes(w):
+    """Algorithmic HBM bytes of the four kernels of a step, in the order
+    fwd, bwd preprocess, bwd main, dQ conversion.
+
+    fwd reads Q, K, V and writes O, L; the preprocess reads O, dO, L and
+    writes D and L*log2(e) (rows padded to whole tiles) and the zeroed fp32
+    dQ accumulator; the main kernel reads Q, K, V, dO and the two row
+    statistics, writes dK, dV and adds into the accumulator (counted once,
+    the adds themselves resolve in L2); the conversion reads the accumulator
+    and writes dQ.  bf16 tensors, fp32 statistics and accumulator.
+    """
+    e = 2
+    q = w.B * w.H * w.N * w.d
+    kv = w.B * w.kv_heads * w.N * w.d
+    rows = w.B * w.H * w.N
+    pad = w.B * w.H * ((w.N + 127) // 128 * 128)
+    fwd = e * (q + 2 * kv + q) + 4 * rows
+    pre = e * 2 * q + 4 * rows + 4 * 2 * pad + 4 * q
+    main = e * (q + 2 * kv + q) + 4 * 2 * pad + e * 2 * kv + 4 * q
+    dq = 4 * q + e * q
+    return fwd, pre, main, dq
+
+
+def kernel_source_hash(kernel):
+    """First 16 hex digits of the SHA-256 of the kernel's source files."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` as an
+    ncu capture recorded them under profiles/, in lines of the form
+
+        traffic-per-launch | <kernel> | <workload> | <bytes> | src <hash>
+
+    Returns (bytes, note); bytes is None when no capture is recorded or when
+    the kernel's sources have changed since (their hash differs)."""
+    want = kernel_source_hash(kernel)
+    stale = None
+    try:
+        names = sorted(os.listdir(PROFILES))
+    except OSError:
+        return None, "no profiles directory"
+    for name in names:
+        if not name.endswith(".md"):
+            continue
+        with open(os.path.join(PROFILES, name)) as f:
+            for line in f:
+                parts = [x.strip() for x in line.strip().strip("`").split("|")]
+                if len(parts) != 5 or parts[0] != "traffic-per-launch":
+                    continue
+                if parts[1] != kernel or parts[2] != workload:
+                    continue
+                src = parts[4].split()[-1]
+                if src == want:
+                    return float(parts[3]), f"ncu capture, profiles/{name}"
+                stale = f"the capture in profiles/{name} predates the current sources"
+    return None, stale or "no ncu capture recorded for this kernel and workload"
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -87,16 +166,17 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, period_ms=50):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
-        self.lines = []
+        self.lines = []      # (host monotonic time, csv line)
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -106,7 +186,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -116,10 +196,16 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, window=None):
+        """Median SM clock and the throttle reasons seen: over the samples
+        taken inside `window` (host monotonic start, end) when there are
+        any, else over every sample (all taken while the step ran)."""
         sm, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in self.lines:
+        lines = self.lines
+        inside = [x for x in lines if window and window[0] <= x[0] <= window[1]]
+        scope = "timed region" if inside else "step loop around the timed region"
+        for _, line in (inside or lines):
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 7:
                 continue
@@ -134,7 +220,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "sampled": scope}
 
 
 # --------------------------------------------------------------- GPU arm --
@@ -251,8 +337,12 @@ def _max_over_ranks(dist, x, dev):
     return float(t.item())
 
 
-def measure_device(ea, w, dev, steps, warmup, dist=None, sample_clocks=True):
-    """Device-resident timing of `steps` steps; returns a dict of results."""
+def measure_device(ea, w, dev, steps, warmup, dist=None):
+    """Device-resident timing of `steps` steps; returns a dict of results.
+
+    Clocks are sampled from the start of the per-kernel event pass to the end
+    of the timed region; the summary takes the samples inside the timed
+    region (all of them when it is shorter than the sampling period)."""
     inp = workloads.make_inputs(w)
     first = Step(ea, inp, dev)
     # rotate input sets so consecutive steps do not find their data in L2
@@ -262,6 +352,12 @@ def measure_device(ea, w, dev, steps, warmup, dist=None, sample_clocks=True):
     for i in range(warmup):
         sets[i % nsets].run(stream)
     torch.cuda.synchronize(dev)
+    graphs = StepGraphs(lambda k, s: sets[k].run(s), nsets, dev)
+    graphs.replay(nsets)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.__enter__()
+    time.sleep(0.2)       # let the sampler start before the loaded window
     # kernel times: the same steps launched one by one, an event around each
     # launch (the events cost ~10 us per step, so the step itself is timed
     # below without them)
@@ -273,30 +369,89 @@ def measure_device(ea, w, dev, steps, warmup, dist=None, sample_clocks=True):
              for j in range(4)]
     # the step: replayed from CUDA graphs (the host launch cost of four ctypes
     # calls is not the kernels'), input sets in rotation as above
-    graphs = StepGraphs(lambda k, s: sets[k].run(s), nsets, dev)
-    graphs.replay(nsets)
-    torch.cuda.synchronize(dev)
-    sampler = ClockSampler(dev.index if dev.index is not None else 0)
     _barrier(dist)
     torch.cuda.synchronize(dev)
-    if sample_clocks:
-        sampler.__enter__()
-        time.sleep(0.3)       # let the sampler start before the timed region
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.monotonic()
     start.record(stream)
     graphs.replay(steps)
     end.record(stream)
     torch.cuda.synchronize(dev)
+    t1 = time.monotonic()
     _barrier(dist)
-    if sample_clocks:
-        sampler.__exit__()
+    time.sleep(0.06)
+    sampler.__exit__()
     ea.check(first.ws, dev)
     total_ms = _max_over_ranks(dist, start.elapsed_time(end), dev)
     flops_f = fwd_flops(w, inp["key_lens"], inp["block_mask"])
     return dict(inp=inp, total_ms=total_ms, ms_per_step=total_ms / steps, stage_ms=stage,
                 fwd_flops=flops_f, bwd_flops=2.5 * flops_f, nsets=nsets,
                 resident_bytes=first.bytes_resident(), launches=first.launches * steps,
-                clocks=sampler.summary() if sample_clocks else None)
+                clocks=sampler.summary((t0, t1)))
+
+
+def roofline(w, r):
+    """The roofline of the step's dominant kernel (the longest of the four
+    stages in the event pass): its algorithmic FLOPs and bytes over its
+    measured time, against the measured burst bf16 peak (the kernel is timed
+    launch by launch) and the measured HBM bandwidth; `bound` is whichever
+    of the two it is closer to."""
+    burst, _, hbm, src = peaks()
+    stage = r["stage_ms"]
+    k = max(range(4), key=lambda i: stage[i])
+    flops = (r["fwd_flops"], 0.0, r["bwd_flops"], 0.0)[k]
+    nbytes = stage_bytes(w)[k]
+    t = stage[k] * 1e-3
+    tf, gbs = flops / t / 1e12, nbytes / t / 1e9
+    tensor_frac, hbm_frac = tf / burst, gbs / hbm
+    kernel = STAGE_KERNELS[k]
+    traffic, note = profiled_traffic(kernel, w.name)
+    if tensor_frac >= hbm_frac:
+        bound, achieved, peak, unit = "tensor", tf, burst, "TFLOP/s"
+        psrc = f"bf16_tflops, burst ({src})"
+    else:
+        bound, achieved, peak, unit = "hbm", gbs, hbm, "GB/s"
+        psrc = f"hbm_gbs ({src})"
+    return {"kernel": kernel, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "peak_source": psrc, "kernel_ms": stage[k],
+            "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
+            "tensor_frac": tensor_frac, "hbm_frac": hbm_frac,
+            "traffic": traffic, "traffic_unit": "DRAM bytes read + written per launch (ncu)",
+            "traffic_source": note}
+
+
+def hbm_rates(w, r):
+    """Achieved HBM GB/s of the whole step and of each kernel, algorithmic
+    bytes (stage_bytes) over measured time, against the measured copy
+    bandwidth; reported for the short sequences that sit below the ridge."""
+    _, _, hbm, src = peaks()
+    nb = stage_bytes(w)
+    per = {k: b / (ms * 1e-3) / 1e9 for k, b, ms in zip(STAGE_KERNELS, nb, r["stage_ms"])}
+    step = sum(nb) / (r["ms_per_step"] * 1e-3) / 1e9
+    return {"achieved_gbs": step, "peak_gbs": hbm, "frac": step / hbm,
+            "peak_source": f"hbm_gbs ({src})", "bytes_per_step": sum(nb),
+            "kernel_gbs": per}
+
+
+def workload_result(w, r, world=1):
+    """The figures of one measured workload (measure_device's result)."""
+    burst, sustained, _, _ = peaks()
+    ms = r["ms_per_step"]
+    value = world * (r["fwd_flops"] + r["bwd_flops"]) / (ms * 1e-3) / 1e12
+    fwd_ms, pre_ms, main_ms, dq_ms = r["stage_ms"]
+    out = {"value": value, "ms_per_step": ms,
+           "fwd_tflops": r["fwd_flops"] / (fwd_ms * 1e-3) / 1e12,
+           "bwd_tflops": r["bwd_flops"] / ((pre_ms + main_ms + dq_ms) * 1e-3) / 1e12,
+           "stage_ms": {"fwd": fwd_ms, "bwd_preprocess": pre_ms, "bwd_main": main_ms,
+                        "bwd_dq": dq_ms},
+           "pct_of_peak": {"of_spec_2250": 100 * value / world / SPEC_BF16_TFLOPS,
+                           "of_measured_burst": 100 * value / world / burst,
+                           "of_measured_sustained": 100 * value / world / sustained},
+           "roofline": roofline(w, r),
+           "clocks": r["clocks"]}
+    if w.N <= SHORT_N:
+        out["hbm"] = hbm_rates(w, r)
+    return out
 
 
 def measure_e2e(ea, w, dev, steps, warmup):
@@ -376,58 +531,101 @@ def _blas_threads():
         return os.cpu_count()
 
 
-def oracle_sample(w, inp, budget_s, max_heads=None):
-    """Time the oracle's fwd+bwd on (b, h) heads until `budget_s` has passed."""
+ORACLE_ROWS = 256     # query rows per oracle timing unit (the oracle's own chunk)
+
+
+def oracle_units(w, seed=0):
+    """The oracle's timing units of a workload, in a seeded random order:
+    (b, h, rows) with rows a whole head when N <= SHORT_N, else one block of
+    ORACLE_ROWS consecutive query rows."""
     import numpy as np
-    from oracle import attention as oracle
-    q, k, v, do = (inp[n] for n in ("q", "k", "v", "do"))
+    if w.N <= SHORT_N:
+        blocks = [np.arange(w.N)]
+    else:
+        blocks = [np.arange(s0, min(w.N, s0 + ORACLE_ROWS)) for s0 in range(0, w.N, ORACLE_ROWS)]
+    units = [(b, h, r) for b in range(w.B) for h in range(w.H) for r in blocks]
+    order = np.random.default_rng(seed).permutation(len(units))
+    return [units[i] for i in order]
+
+
+def rows_flops(w, inp, b, rows):
+    """fwd+bwd FLOPs of query rows `rows` of batch b: 3.5 x 4 d per allowed
+    (query, key) pair, with the workload's causal, padding and block masks."""
+    import numpy as np
+    rows = np.asarray(rows, dtype=np.int64)
     kl = inp["key_lens"]
+    key_len = w.N if kl is None else min(w.N, max(0, int(kl[b])))
+    lim = np.minimum(key_len, rows + 1 if w.causal else np.full(rows.shape, w.N))
     bm = inp["block_mask"]
+    if bm is None:
+        pairs = float(np.maximum(lim, 0).sum())
+    else:
+        m = bm.numpy().astype(bool)[rows // 128]                       # [R, nb]
+        starts = 128 * np.arange(m.shape[1])
+        overlap = np.clip(lim[:, None] - starts[None, :], 0, 128)
+        pairs = float((m * overlap).sum())
+    return 3.5 * 4.0 * w.d * pairs
+
+
+def oracle_inputs(inp):
+    """The workload's tensors as numpy fp32 (exact for bf16 values; the
+    oracle takes each head to fp64 itself) and its oracle keyword arguments."""
+    arr = {n: inp[n].float().numpy() for n in ("q", "k", "v", "do")}
+    kl, bm = inp["key_lens"], inp["block_mask"]
     kw = dict(scale=inp["scale"], causal=inp["causal"],
               key_lens=None if kl is None else kl.numpy(),
               block_mask=None if bm is None else bm.numpy(),
               dropout_p=inp["dropout_p"], seed=inp["seed"], offset=inp["offset"])
-    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    return arr, kw
+
+
+def oracle_sample(w, inp, units, arrays, budget_s, start=0):
+    """Time the oracle's fwd+bwd on `units` (from oracle_units) starting at
+    index `start`, until `budget_s` has passed (at least one unit).  Each
+    unit's rows go through oracle.backward_rows, which evaluates O, L, dQ and
+    the rows' dK, dV contributions.  Returns (flops, seconds, units done)."""
+    from oracle import attention as oracle
+    arr, kw = arrays
     done, flops = 0, 0.0
     t0 = time.perf_counter()
-    grp = w.H // w.kv_heads
-    for b, h in heads:
-        sl = (slice(b, b + 1), slice(h, h + 1))
-        skv = (slice(b, b + 1), slice(h // grp, h // grp + 1))   # the head's key/value head
-        qs, dos = (x[sl].double().numpy() for x in (q, do))
-        ks, vs = (x[skv].double().numpy() for x in (k, v))
-        kws = dict(kw)
-        if kl is not None:
-            kws["key_lens"] = np.asarray(kw["key_lens"])[b:b + 1]
-        oracle.attention_backward(qs, ks, vs, dos, **kws)
+    while True:
+        b, h, rows = units[(start + done) % len(units)]
+        oracle.backward_rows(arr["q"], arr["k"], arr["v"], arr["do"], b, h, rows, **kw)
+        flops += rows_flops(w, inp, b, rows)
         done += 1
-        wh = workloads.get(w.name, B=1, H=1, H_kv=1)
-        flops += 3.5 * fwd_flops(wh, None if kl is None else kl[b:b + 1],
-                                 None if bm is None else bm)
-        if time.perf_counter() - t0 > budget_s or (max_heads and done >= max_heads):
+        if time.perf_counter() - t0 > budget_s or done >= len(units):
             break
-    dt = time.perf_counter() - t0
-    return flops, dt, done
+    return flops, time.perf_counter() - t0, done
+
+
+def oracle_unit_name(w):
+    return "(b, h) heads" if w.N <= SHORT_N else f"blocks of {ORACLE_ROWS} query rows"
 
 
 def run_reference(args, w):
-    """The reference arm: the fp64 CPU oracle, as it stands, on host cores."""
+    """The reference arm: the fp64 CPU oracle, as it stands, on host cores.
+    Each step is a bounded sample of the workload: timing units (whole
+    heads, or blocks of query rows at long N) for about half a second."""
     inp = workloads.make_inputs(w)
+    units = oracle_units(w)
+    arrays = oracle_inputs(inp)
+    pos = 0
     for _ in range(args.warmup):
-        oracle_sample(w, inp, 0.0, max_heads=1)
-    times, flops = [], 0.0
+        _, _, n = oracle_sample(w, inp, units, arrays, 0.5, pos)
+        pos += n
+    total_f, total_t, total_n = 0.0, 0.0, 0
     for _ in range(args.steps):
-        f, dt, _ = oracle_sample(w, inp, 0.0, max_heads=1)
-        times.append(dt)
-        flops = f
-    per = sum(times) / len(times)
-    value = flops / per / 1e12
+        f, dt, n = oracle_sample(w, inp, units, arrays, 0.5, pos)
+        pos += n
+        total_f, total_t, total_n = total_f + f, total_t + dt, total_n + n
+    value = total_f / total_t / 1e12
     cores = _blas_threads()
-    sample = f"one (b, h) head of {w.name} per step, fp64 numpy fwd+bwd"
+    sample = (f"{total_n} timing units ({oracle_unit_name(w)}, about 0.5 s per step) of "
+              f"{w.name}, fp64 numpy fwd+bwd")
     line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "impl": "reference",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "ms_per_step": total_t / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": describe(w), "parallelism": "none (host cores)"},
             "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
                              "sample": sample},
@@ -760,9 +958,9 @@ def profile_steps(w, n):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="bert-large")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing")
@@ -804,11 +1002,12 @@ def main():
     cpu = None
     if rank == 0 and world == 1:
         inp_cpu = workloads.make_inputs(w)
-        f, dt, heads = oracle_sample(w, inp_cpu, args.cpu_budget)
+        units = oracle_units(w)
+        f, dt, n = oracle_sample(w, inp_cpu, units, oracle_inputs(inp_cpu), args.cpu_budget)
         cpu = {"value": f / dt / 1e12, "unit": "TFLOPS", "cores": _blas_threads(),
                "kind": "oracle",
-               "sample": f"{heads} of {w.B * w.H} (b, h) heads of {w.name}, fp64 numpy fwd+bwd, "
-                         f"{dt:.1f} s"}
+               "sample": f"{n} of {len(units)} {oracle_unit_name(w)} of {w.name} (seeded "
+                         f"random order), fp64 numpy fwd+bwd, {dt:.1f} s"}
         del inp_cpu
 
     dist = None
@@ -827,17 +1026,10 @@ def main():
         dist.barrier()
 
     r = measure_device(ea, w, dev, args.steps, args.warmup, dist)
-    ms = r["ms_per_step"]
-    flops_step = r["fwd_flops"] + r["bwd_flops"]
-    value = world * flops_step / (ms * 1e-3) / 1e12
-    burst, sustained, hbm, src = peaks()
-    fwd_ms, pre_ms, main_ms, dq_ms = r["stage_ms"]
-    main_tflops = r["bwd_flops"] / (main_ms * 1e-3) / 1e12
-    traffic = BWD_MAIN_TRAFFIC.get(w.name)
-
+    res = workload_result(w, r, world)
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "metric": METRIC, "value": res.pop("value"), "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": res.pop("ms_per_step"),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": describe(w), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
@@ -849,35 +1041,23 @@ def main():
                              "the K steps; stage_ms and the roofline kernel time from a "
                              "separate pass of K steps launched one by one with an event "
                              "around each launch"},
-        "fwd_tflops": r["fwd_flops"] / (fwd_ms * 1e-3) / 1e12,
-        "bwd_tflops": r["bwd_flops"] / ((pre_ms + main_ms + dq_ms) * 1e-3) / 1e12,
-        "stage_ms": {"fwd": fwd_ms, "bwd_preprocess": pre_ms, "bwd_main": main_ms,
-                     "bwd_dq": dq_ms},
-        "pct_of_peak": {"of_measured_sustained": 100 * value / world / sustained,
-                        "of_spec_2250": 100 * value / world / SPEC_BF16_TFLOPS},
-        "roofline": {"kernel": "bwd_bf16_kernel", "bound": "tensor", "achieved": main_tflops,
-                     "peak": sustained, "unit": "TFLOP/s", "frac": main_tflops / sustained,
-                     "peak_source": f"bf16_tflops_sustained ({src})", "traffic": traffic,
-                     "traffic_unit": "bytes per launch (DRAM read + write, ncu)"},
         "gpu_launches": r["launches"],
-        "clocks": r["clocks"],
     }
+    line.update(res)
     if cpu is not None:
         line["cpu_baseline"] = cpu
     line["e2e"] = measure_e2e(ea, w, dev, max(3, min(args.steps, 100)), 3)
     if not args.no_secondary and world == 1:
         sec = []
         for name in SECONDARY:
+            if name == w.name:
+                continue
             ws = workloads.get(name)
-            rs = measure_device(ea, ws, dev, max(10, args.steps // 20), 5, None,
-                                sample_clocks=False)
-            f_ms, p_ms, m_ms, d_ms = rs["stage_ms"]
-            tot = rs["fwd_flops"] + rs["bwd_flops"]
-            sec.append({"workload": describe(ws),
-                        "fwd_bwd_tflops": tot / (rs["ms_per_step"] * 1e-3) / 1e12,
-                        "fwd_tflops": rs["fwd_flops"] / (f_ms * 1e-3) / 1e12,
-                        "bwd_tflops": rs["bwd_flops"] / ((p_ms + m_ms + d_ms) * 1e-3) / 1e12,
-                        "ms_per_step": rs["ms_per_step"]})
+            rs = measure_device(ea, ws, dev, max(10, args.steps // 10), 5, None)
+            entry = {"workload": describe(ws)}
+            entry.update(workload_result(ws, rs))
+            entry["fwd_bwd_tflops"] = entry.pop("value")
+            sec.append(entry)
         line["secondary"] = sec
     if rank == 0:
         print(json.dumps(line), flush=True)

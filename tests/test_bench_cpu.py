@@ -71,3 +71,81 @@ def test_cached_workspace_grows_and_keeps_what_it_replaced():
     assert [id(t) for t in api._retired[key]] == [id(a), id(b)]
     api._workspaces.pop(key, None)
     api._retired.pop(key, None)
+
+
+@pytest.mark.parametrize("name,over", [("long-causal-512", {}), ("bert-large", {}),
+                                       ("block-sparse-64k", {"N": 1000, "H": 2}),
+                                       ("gqa-4k", {"N": 700, "B": 1})])
+def test_oracle_units_cover_the_workload_and_count_its_flops(name, over):
+    # the oracle's timing units (whole heads or row blocks) partition the
+    # workload, and their FLOPs add up to the step's fwd+bwd FLOPs
+    w = workloads.get(name, **over)
+    inp = workloads.make_inputs(w)
+    if w.block_density is not None:
+        nb = (w.N + 127) // 128
+        inp["block_mask"] = workloads.make_block_mask(nb, 0.3, seed=3)
+    units = bench.oracle_units(w)
+    seen = {}
+    for b, h, rows in units:
+        for r in rows.tolist():
+            seen[(b, h, r)] = seen.get((b, h, r), 0) + 1
+    assert len(seen) == w.B * w.H * w.N and set(seen.values()) == {1}
+    total = sum(bench.rows_flops(w, inp, b, rows) for b, h, rows in units)
+    want = 3.5 * bench.fwd_flops(w, inp["key_lens"], inp["block_mask"])
+    # the metric counts causal work as N^2 / 2; the rows' exact count of
+    # allowed pairs is N (N + 1) / 2
+    assert total == pytest.approx(want * ((w.N + 1) / w.N if w.causal else 1.0), rel=1e-12)
+
+
+def test_oracle_sample_runs_and_counts_what_it_did():
+    w = workloads.get("long-causal-512", H=2)
+    inp = workloads.make_inputs(w)
+    units = bench.oracle_units(w)
+    f, dt, n = bench.oracle_sample(w, inp, units, bench.oracle_inputs(inp), 0.0)
+    assert n == 1 and dt > 0
+    assert f == bench.rows_flops(w, inp, units[0][0], units[0][2])
+
+
+def test_stage_bytes_of_a_plain_head():
+    w = workloads.get("long-causal-4096", H=1)
+    fwd, pre, main, dq = bench.stage_bytes(w)
+    nd = w.N * w.d
+    assert fwd == 2 * 4 * nd + 4 * w.N                 # Q, K, V read; O, L written
+    assert dq == 6 * nd                                # fp32 accumulator in, bf16 dQ out
+    assert main > 2 * 6 * nd and pre > 2 * 2 * nd
+
+
+def _profile(tmp_path, line):
+    (tmp_path / "x.md").write_text("# summary\n\n    " + line + "\n")
+
+
+def test_traffic_is_read_from_profiles_while_the_sources_match(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "PROFILES", str(tmp_path))
+    h = bench.kernel_source_hash("bwd_bf16_kernel")
+    _profile(tmp_path, f"traffic-per-launch | bwd_bf16_kernel | long-causal-16384 | 123456 | src {h}")
+    got, note = bench.profiled_traffic("bwd_bf16_kernel", "long-causal-16384")
+    assert got == 123456.0 and "x.md" in note
+    assert bench.profiled_traffic("bwd_bf16_kernel", "bert-large")[0] is None
+    assert bench.profiled_traffic("fwd_bf16_kernel", "long-causal-16384")[0] is None
+
+
+def test_traffic_of_changed_sources_is_not_reported(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "PROFILES", str(tmp_path))
+    _profile(tmp_path, "traffic-per-launch | bwd_bf16_kernel | long-causal-16384 | 99 | src 0123")
+    got, note = bench.profiled_traffic("bwd_bf16_kernel", "long-causal-16384")
+    assert got is None and "predates" in note
+
+
+def test_roofline_takes_the_longest_stage_and_the_nearer_bound():
+    w = workloads.get("long-causal-16384")
+    f = bench.fwd_flops(w)
+    r = dict(stage_ms=[0.8, 0.05, 2.4, 0.03], fwd_flops=f, bwd_flops=2.5 * f)
+    roof = bench.roofline(w, r)
+    assert roof["kernel"] == "bwd_bf16_kernel" and roof["bound"] == "tensor"
+    assert roof["achieved"] == pytest.approx(2.5 * f / 2.4e-3 / 1e12)
+    assert roof["frac"] == pytest.approx(roof["achieved"] / bench.peaks()[0])
+    # a memory-bound stage dominating
+    r = dict(stage_ms=[0.01, 0.5, 0.02, 0.01], fwd_flops=f, bwd_flops=2.5 * f)
+    roof = bench.roofline(w, r)
+    assert roof["kernel"] == "bwd_preprocess_kernel" and roof["bound"] == "hbm"
+    assert roof["unit"] == "GB/s"
