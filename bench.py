@@ -955,6 +955,23 @@ def profile_steps(w, n):
 
 # -------------------------------------------------------------------- main --
 
+def parse_overrides(items):
+    """FIELD=VALUE strings -> a dict of workload fields (ints where they parse)."""
+    out = {}
+    for item in items:
+        key, sep, val = item.partition("=")
+        if not sep or key not in workloads.Workload.__dataclass_fields__:
+            raise SystemExit(f"--set wants FIELD=VALUE with a workload field, got {item!r}")
+        try:
+            out[key] = int(val)
+        except ValueError:
+            try:
+                out[key] = float(val)
+            except ValueError:
+                out[key] = val
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -967,8 +984,10 @@ def main():
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="run this many untimed steps of one input set and exit (a short, "
                          "fixed launch sequence for ncu captures; no oracle, no JSON line)")
+    ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
+                    help="replace a field of the workload, e.g. --set H=2 (repeatable)")
     args = ap.parse_args()
-    w = workloads.get(args.workload)
+    w = workloads.get(args.workload, **parse_overrides(args.set))
 
     if args.profile_steps > 0:
         profile_steps(w, args.profile_steps)

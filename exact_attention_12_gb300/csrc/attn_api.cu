@@ -56,12 +56,52 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct WsLayout {
   size_t list_cnt = 0, list_idx = 0;   // compacted block mask (0 = none)
   size_t vt = 0;                       // FP8 forward: V^T [B * H_kv][d][nb * 128]
+  size_t part_o = 0, part_l = 0;       // forward of split pairs: partial O, L
+  int splits = 1;
   size_t lse2 = 0, dsum = 0, dq_acc = 0;   // backward only
   size_t total = 0;
 };
 
 int num_masks(const attn_params* p) {
   return p->block_mask_head_stride != 0 ? p->B * p->H : 1;
+}
+
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    sms = 148;
+  return sms;
+}
+
+// Key padding without the causal mask, up to kLenOrderMaxB sequences: the
+// forward numbers its units longest sequence first (ranked in the kernel).
+bool fwd_len_order(const attn_params* p) {
+  return p->key_lens != nullptr && !p->causal && p->B <= attn::kLenOrderMaxB;
+}
+
+// Key tiles a piece of a split pair keeps at least.  A unit has fixed
+// costs (claim, Q load, pipeline fill, epilogue) of a few key steps, and the
+// pieces' partials must be merged afterwards, so short pieces lose more
+// than the fuller GPU gains (measured: causal d = 128 with 16 heads at
+// N = 1024, cut into pieces of 1-2 key tiles, took 41 us against 24 us
+// unsplit).
+constexpr long long kMinPieceTiles = 8;
+
+// Pieces per query-tile pair in the forward.  With fewer pairs than SMs and
+// long rows (few heads, long sequences) the pairs are cut along the keys
+// into pieces merged afterwards: about two units per SM, each piece at least
+// kMinPieceTiles key tiles of the longest pair, at most 16; otherwise 1.
+int fwd_splits(const attn_params* p) {
+  if (p->dtype == ATTN_FP32 || fwd_len_order(p)) return 1;
+  const long long nb = (static_cast<long long>(p->N) + kTile - 1) / kTile;
+  const long long units = (nb + 1) / 2 * p->B * p->H;
+  const long long sms = sm_count();
+  if (units <= 0 || units >= sms) return 1;
+  long long k = (2 * sms + units - 1) / units;
+  if (k > nb / kMinPieceTiles) k = nb / kMinPieceTiles;
+  if (k > 16) k = 16;
+  return k < 1 ? 1 : static_cast<int>(k);
 }
 
 WsLayout layout(const attn_params* p, bool bwd) {
@@ -80,6 +120,13 @@ WsLayout layout(const attn_params* p, bool bwd) {
     L.vt = off;
     const size_t H_kv = static_cast<size_t>(p->H_kv == 0 ? p->H : p->H_kv);
     off = round_up(off + static_cast<size_t>(p->B) * H_kv * p->d * nb * kTile, 256);
+  }
+  if (!bwd && (L.splits = fwd_splits(p)) > 1) {
+    const size_t prows = static_cast<size_t>(L.splits) * p->B * p->H * ((nb + 1) / 2) * 2 * kTile;
+    L.part_o = off;
+    off = round_up(off + prows * p->d * sizeof(float), 256);
+    L.part_l = off;
+    off = round_up(off + prows * sizeof(float), 256);
   }
   if (bwd) {
     const size_t bhpad = static_cast<size_t>(p->B) * p->H * nb * kTile;
@@ -333,7 +380,7 @@ attn_status attn_fwd(const attn_params* p, const void* q, const void* k, const v
   a.m.head_group = head_group(p, p->B * p->H, 4.0 * p->N * p->d);   // K and V, bf16
   // key padding makes the units' costs differ by sequence: claim the
   // longest first so that the last claims are short
-  a.len_order = (p->key_lens != nullptr && !p->causal && p->B <= attn::kLenOrderMaxB) ? 1 : 0;
+  a.len_order = fwd_len_order(p) ? 1 : 0;
   if (a.len_order) a.m.head_group = 1;   // each head's pairs together, heads in ranked order
   a.d = p->d;
   a.scale = p->scale;
@@ -348,6 +395,12 @@ attn_status attn_fwd(const attn_params* p, const void* q, const void* k, const v
   a.status = reinterpret_cast<int*>(w);
   a.sched = reinterpret_cast<int*>(w + kSchedOffset);
   a.timeout_ns = kTimeoutNs;
+  a.splits = L.splits;
+  a.part_rows = (a.m.nb + 1) / 2 * 2 * kTile;
+  if (L.splits > 1) {
+    a.part_o = reinterpret_cast<float*>(w + L.part_o);
+    a.part_l = reinterpret_cast<float*>(w + L.part_l);
+  }
 
   cudaError_t e;
   if (p->dtype == ATTN_FP32) {

@@ -84,9 +84,12 @@ struct FwdCfg {
 
 // A claimed unit as the producer publishes it to the other roles.
 struct UnitInfo {
-  const uint16_t* idx[2];   // block-mask rows of query tiles A, B (null: dense)
+  const uint16_t* idx[2];   // block-mask rows of query tiles A, B from their first
+                            // visited entry (null: dense)
+  int base[2];              // dense: first key tile A, B visit
   int n[2];                 // key tiles A and B visit
   int pair, bh, b, h, limit;
+  int piece;                // key-range piece of a split pair (0 when unsplit)
   int w;                    // unit index; -1: no more units
 };
 
@@ -113,10 +116,13 @@ struct FwdCtl {
 constexpr int kBarLenOrder = 1;
 
 // One unit of work: a pair of query tiles of one (b, h) and their key-tile
-// lists.  Units are numbered in head groups of G consecutive (b, h), within
-// a group heaviest pair first; CTAs take units round-robin.
+// lists, or, when the pairs are split along the keys (too few pairs to
+// fill the GPU), one of `splits` pieces of a pair, each over a contiguous
+// range of key-tile indices.  Units are numbered in head groups of G
+// consecutive (b, h), within a group heaviest pair first, a pair's pieces
+// together; CTAs take units round-robin.
 struct FwdUnit {
-  int pair, bh, b, h, limit;
+  int pair, bh, b, h, limit, piece;
 };
 
 
@@ -132,9 +138,10 @@ struct FwdUnit {
 
 // The key tiles query tile `qt` of head `bh` visits, in ascending order.
 struct TileList {
-  const uint16_t* idx;   // compacted block-mask row, or null (dense)
+  const uint16_t* idx;   // compacted block-mask row from the first visited entry, or null (dense)
+  int base;              // dense: the first visited key tile
   int n;
-  __device__ __forceinline__ int operator[](int t) const { return idx ? int(idx[t]) : t; }
+  __device__ __forceinline__ int operator[](int t) const { return idx ? int(idx[t]) : base + t; }
 };
 
 __device__ __forceinline__ int key_limit(const MaskArgs& m, int b) {
@@ -143,23 +150,41 @@ __device__ __forceinline__ int key_limit(const MaskArgs& m, int b) {
   return limit;
 }
 
-__device__ __forceinline__ TileList fwd_tiles(const MaskArgs& m, int qt, int bh, int limit) {
-  if (qt >= m.nb) return TileList{nullptr, 0};   // past the last query tile
+// First position in the sorted list p[0, n) whose tile index is >= j.
+__device__ __forceinline__ int lower_bound_tile(const uint16_t* p, int n, int j) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (int(p[mid]) < j) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// The key tiles with index in [jlo, jhi) that query tile qt may attend.
+__device__ __forceinline__ TileList fwd_tiles(const MaskArgs& m, int qt, int bh, int limit,
+                                              int jlo, int jhi) {
+  if (qt >= m.nb) return TileList{nullptr, 0, 0};   // past the last query tile
   int cap = (limit + kTile - 1) / kTile;
   if (m.causal) cap = min(cap, qt + 1);
-  TileList t{nullptr, cap};
-  if (m.list_idx != nullptr) {
-    const size_t row = static_cast<size_t>(m.mask_per_head ? bh : 0) * m.nb + qt;
-    const uint16_t* p = m.list_idx + row * m.nb;
-    int lo = 0, hi = m.list_cnt[row];
-    while (lo < hi) {   // the list is sorted: the usable part is a prefix
-      const int mid = (lo + hi) >> 1;
-      if (int(p[mid]) < cap) lo = mid + 1; else hi = mid;
-    }
-    t.idx = p;
-    t.n = lo;
-  }
-  return t;
+  const int end = min(cap, jhi);
+  if (m.list_idx == nullptr) return TileList{nullptr, jlo, max(0, end - jlo)};
+  const size_t row = static_cast<size_t>(m.mask_per_head ? bh : 0) * m.nb + qt;
+  const uint16_t* p = m.list_idx + row * m.nb;
+  const int cnt = m.list_cnt[row];
+  const int lo = lower_bound_tile(p, cnt, jlo);
+  const int hi = lower_bound_tile(p, cnt, end);
+  return TileList{p + lo, 0, max(0, hi - lo)};
+}
+
+// The key-tile range [jlo, jhi) of piece `piece` of `splits` of a query-tile
+// pair: the pair's key tiles [0, J) cut into equal parts (J: the tiles below
+// the key limit and, causal, at or below the pair's second tile).
+__device__ __forceinline__ void piece_range(const MaskArgs& m, int pair, int limit, int piece,
+                                            int splits, int& jlo, int& jhi) {
+  int J = min((limit + kTile - 1) / kTile, m.nb);
+  if (m.causal) J = min(J, 2 * pair + 2);
+  jlo = piece * J / splits;
+  jhi = (piece + 1) * J / splits;
 }
 
 // Walks the union of two sorted key-tile lists in ascending order.
@@ -241,15 +266,18 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
   const MaskArgs& m = a.m;
   const int BH = m.B * m.H;
   const int npairs = (m.nb + 1) / 2;
-  const int total = npairs * BH;
+  const int K = a.splits;   // pieces per pair
+  const int total = npairs * BH * K;
   auto unit_of = [&](int w) {
-    const int G = m.head_group, per = G * npairs, nfull = BH / G;
+    const int G = m.head_group, per = G * npairs * K, nfull = BH / G;
     const int g = w < nfull * per ? w / per : nfull;
     const int gs = g < nfull ? G : BH - nfull * G;
     const int rem = w - g * per;
     FwdUnit u;
-    u.pair = npairs - 1 - rem / gs;
-    u.bh = g * G + rem % gs;
+    u.pair = npairs - 1 - rem / (gs * K);
+    const int r2 = rem % (gs * K);
+    u.bh = g * G + r2 / K;
+    u.piece = r2 % K;
     u.b = u.bh / m.H;
     u.h = u.bh - u.b * m.H;
     if (a.len_order) {   // (groups of one head) the sequences in their ranked order
@@ -322,9 +350,12 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
         ui.w = -1;
         if (w < total) {
           const FwdUnit u = unit_of(w);
-          const TileList la = fwd_tiles(m, 2 * u.pair, u.bh, u.limit);
-          const TileList lb = fwd_tiles(m, 2 * u.pair + 1, u.bh, u.limit);
-          ui = UnitInfo{{la.idx, lb.idx}, {la.n, lb.n}, u.pair, u.bh, u.b, u.h, u.limit, w};
+          int jlo, jhi;
+          piece_range(m, u.pair, u.limit, u.piece, K, jlo, jhi);
+          const TileList la = fwd_tiles(m, 2 * u.pair, u.bh, u.limit, jlo, jhi);
+          const TileList lb = fwd_tiles(m, 2 * u.pair + 1, u.bh, u.limit, jlo, jhi);
+          ui = UnitInfo{{la.idx, lb.idx}, {la.base, lb.base}, {la.n, lb.n}, u.pair, u.bh,
+                        u.b, u.h, u.limit, u.piece, w};
         }
         const int r = pub % kUnitRing;
         if (pub >= kUnitRing &&
@@ -333,8 +364,8 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
         ctl.unit[r] = ui;
         mbar_arrive(&ctl.unitfull[r]);   // release: the consumers' wait acquires unit[r]
         if (ui.w < 0) break;
-        const FwdUnit u{ui.pair, ui.bh, ui.b, ui.h, ui.limit};
-        const TileList listA{ui.idx[0], ui.n[0]}, listB{ui.idx[1], ui.n[1]};
+        const FwdUnit u{ui.pair, ui.bh, ui.b, ui.h, ui.limit, ui.piece};
+        const TileList listA{ui.idx[0], ui.base[0], ui.n[0]}, listB{ui.idx[1], ui.base[1], ui.n[1]};
         if (listA.n == 0 && listB.n == 0) continue;
         // the previous unit's score MMAs are done with Q
         if (kw >= 1 && !(ok = mbar_wait(&ctl.qempty, (kw - 1) & 1, wc, kSiteFwdQ))) break;
@@ -407,7 +438,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
         const UnitInfo ui = ctl.unit[r];
         mbar_arrive(&ctl.unitempty[r]);
         if (ui.w < 0) break;
-        const TileList listA{ui.idx[0], ui.n[0]}, listB{ui.idx[1], ui.n[1]};
+        const TileList listA{ui.idx[0], ui.base[0], ui.n[0]}, listB{ui.idx[1], ui.base[1], ui.n[1]};
         if (listA.n == 0 && listB.n == 0) continue;
         if (!(ok = mbar_wait(&ctl.qfull, kw & 1, wc, kSiteFwdQ))) break;
         PairWalk walk{listA, listB};
@@ -558,7 +589,8 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.unitempty[r]);
       if (ui.w < 0) break;
-      const TileList tiles{x ? ui.idx[1] : ui.idx[0], x ? ui.n[1] : ui.n[0]};
+      const TileList tiles{x ? ui.idx[1] : ui.idx[0], x ? ui.base[1] : ui.base[0],
+                           x ? ui.n[1] : ui.n[0]};
       const bool any = ui.n[0] > 0 || ui.n[1] > 0;
       const int bh = ui.bh, b = ui.b, h = ui.h, limit = ui.limit;
       const int q0 = (2 * ui.pair + x) * kTile;
@@ -697,7 +729,34 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
         if (!ok) break;
         tc_fence_after();
       }
-      if (q0 < m.N) {
+      if (q0 < m.N && K > 1) {
+        // a piece of a split pair: O normalised over the piece's keys (fp32)
+        // and its logsumexp, merged with the other pieces' afterwards
+        const bool live = l_sum > 0.f;
+        const float inv = live ? a.o_scale * (m.drop_scale / l_sum) : 0.f;
+        const float L = live ? (m_used * c2 + __log2f(l_sum)) * kLn2 : -INFINITY;
+        const int64_t prow = (static_cast<int64_t>(ui.piece) * BH + bh) * a.part_rows + qi;
+        float* po = a.part_o + prow * D;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          if (n > 0) {
+            tmem_ld32(oc + c, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) o[t] = 0u;
+          }
+          if (qi < m.N) {
+            float4* dst = reinterpret_cast<float4*>(po + c);
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              dst[t] = make_float4(__uint_as_float(o[4 * t]) * inv, __uint_as_float(o[4 * t + 1]) * inv,
+                                   __uint_as_float(o[4 * t + 2]) * inv, __uint_as_float(o[4 * t + 3]) * inv);
+          }
+        }
+        if (qi < m.N) a.part_l[prow] = L;
+      } else if (q0 < m.N) {
         const bool live = l_sum > 0.f;
         const float inv = live ? a.o_scale * (m.drop_scale / l_sum) : 0.f;
         const float L = live ? (m_used * c2 + __log2f(l_sum)) * kLn2 : -INFINITY;
@@ -780,9 +839,71 @@ cudaError_t launch_one(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const long long units = static_cast<long long>((a.m.nb + 1) / 2) * a.m.B * a.m.H;
+  const long long units = static_cast<long long>((a.m.nb + 1) / 2) * a.m.B * a.m.H * a.splits;
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
   return launch_pdl(kernel, dim3(grid), dim3(C::kThreads), C::kSmem, s, tm.q, tm.k, tm.v, a);
+}
+
+// The pieces of split query-tile pairs merged by the incremental-softmax
+// rule (the paper summary's running statistics, "Theo dõi Softmax tăng dần";
+// the online-softmax update of the azimuth.plus explainer): with pieces s
+// holding O_s normalised over their keys and L_s = logsumexp of their
+// scores, L = log sum_s e^{L_s} and O = sum_s e^{L_s - L} O_s.  A piece with
+// no allowed key has L_s = -inf and weight 0; a row with none at all gets
+// O = 0, L = -inf.  One thread per eight columns of a row.
+template <int D>
+__global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
+  constexpr int kLanes = D / 8;
+  const MaskArgs& m = a.m;
+  const int64_t rows = static_cast<int64_t>(m.B) * m.H * m.N;
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = gtid / kLanes;
+  if (row >= rows) return;
+  const int part = static_cast<int>(gtid % kLanes);
+  const int64_t n = row % m.N, bh = row / m.N;
+  const int64_t piece_stride = static_cast<int64_t>(m.B) * m.H * a.part_rows;
+  const int64_t prow = bh * a.part_rows + n;
+  float lmax = -INFINITY;
+  for (int s = 0; s < a.splits; ++s) lmax = fmaxf(lmax, a.part_l[s * piece_stride + prow]);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float L = -INFINITY;
+  if (lmax > -INFINITY) {
+    float wsum = 0.f;
+    for (int s = 0; s < a.splits; ++s) {
+      const float ls = a.part_l[s * piece_stride + prow];
+      if (ls == -INFINITY) continue;
+      const float w = __expf(ls - lmax);
+      wsum += w;
+      const float4* src = reinterpret_cast<const float4*>(a.part_o + (s * piece_stride + prow) * D + part * 8);
+      const float4 x = src[0], y = src[1];
+      acc[0] = fmaf(w, x.x, acc[0]); acc[1] = fmaf(w, x.y, acc[1]);
+      acc[2] = fmaf(w, x.z, acc[2]); acc[3] = fmaf(w, x.w, acc[3]);
+      acc[4] = fmaf(w, y.x, acc[4]); acc[5] = fmaf(w, y.y, acc[5]);
+      acc[6] = fmaf(w, y.z, acc[6]); acc[7] = fmaf(w, y.w, acc[7]);
+    }
+    L = lmax + __logf(wsum);
+    const float inv = 1.f / wsum;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) acc[t] *= inv;
+  }
+  const int64_t b = bh / m.H, h = bh % m.H;
+  uint4 out;
+  out.x = pack_bf16x2(acc[0], acc[1]);
+  out.y = pack_bf16x2(acc[2], acc[3]);
+  out.z = pack_bf16x2(acc[4], acc[5]);
+  out.w = pack_bf16x2(acc[6], acc[7]);
+  *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + b * a.stride_b + h * a.stride_h +
+                            n * a.stride_n + part * 8) = out;
+  if (part == 0) a.lse[row] = L;
+}
+
+template <int D>
+cudaError_t launch_merge(const FwdArgs& a, cudaStream_t s) {
+  const int64_t threads = static_cast<int64_t>(a.m.B) * a.m.H * a.m.N * (D / 8);
+  const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
+  return launch_pdl(fwd_merge_kernel<D>, dim3(grid), dim3(256), 0, s, a);
 }
 
 // V [B, H_kv, N, d] E4M3 -> V^T [B * H_kv][d][npad]: one CTA per 64 keys of
@@ -830,9 +951,13 @@ __global__ void __launch_bounds__(256) fp8_transpose_v_kernel(const uint8_t* __r
 
 cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
   const bool drop = a.m.drop_threshold != 0;
+  cudaError_t e;
   if (a.d == 64)
-    return drop ? launch_one<64, true, false>(tm, a, s) : launch_one<64, false, false>(tm, a, s);
-  return drop ? launch_one<128, true, false>(tm, a, s) : launch_one<128, false, false>(tm, a, s);
+    e = drop ? launch_one<64, true, false>(tm, a, s) : launch_one<64, false, false>(tm, a, s);
+  else
+    e = drop ? launch_one<128, true, false>(tm, a, s) : launch_one<128, false, false>(tm, a, s);
+  if (e != cudaSuccess || a.splits <= 1) return e;
+  return a.d == 64 ? launch_merge<64>(a, s) : launch_merge<128>(a, s);
 }
 
 cudaError_t launch_fp8_transpose_v(const uint8_t* v, int64_t sb, int64_t sh, int64_t sn, int B,
@@ -846,7 +971,9 @@ cudaError_t launch_fp8_transpose_v(const uint8_t* v, int64_t sb, int64_t sh, int
 
 cudaError_t launch_fwd_fp8(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
   if (a.d != 128 || a.m.drop_threshold != 0) return cudaErrorInvalidValue;
-  return launch_one<128, false, true>(tm, a, s);
+  const cudaError_t e = launch_one<128, false, true>(tm, a, s);
+  if (e != cudaSuccess || a.splits <= 1) return e;
+  return launch_merge<128>(a, s);
 }
 
 }  // namespace attn

@@ -100,6 +100,13 @@ struct FwdArgs {
   // query-tile pairs together (key padding, not causal, B <= kLenOrderMaxB)
   int len_order;
   int stall;                      // kStallFwdSoftmax: softmax warp 0 withholds its first P-ready arrive
+  // split pairs (too few query-tile pairs to fill the GPU): each pair's key
+  // tiles are cut into `splits` pieces whose normalised O (fp32) and
+  // logsumexp go to the workspace, then merged into o, lse; 1 = unsplit
+  int splits;
+  int part_rows;                  // rows per (b, h) in the partial arrays: pairs x 256
+  float* part_o;                  // [splits][B*H][part_rows][d]
+  float* part_l;                  // [splits][B*H][part_rows]
 };
 
 // Largest batch whose sequences the forward orders by key length (one warp

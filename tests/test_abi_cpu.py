@@ -142,7 +142,7 @@ def test_misaligned_tensor_is_rejected(abi):
     p = _params(abi)
     ok = ctypes.c_void_p(0x1000)
     bad = ctypes.c_void_p(0x1008)
-    st = lib.attn_fwd(ctypes.byref(p), ok, bad, ok, ok, ok, ok, 4096, None)
+    st = lib.attn_fwd(ctypes.byref(p), ok, bad, ok, ok, ok, ok, 1 << 24, None)
     assert st == abi.ATTN_ERR_INVALID_ARG
 
 
@@ -227,3 +227,26 @@ def test_debug_stall_is_checked_on_the_host(abi):
     assert b"unknown stall" in lib.attn_last_error()
     assert lib.attn_debug_stall(abi.ATTN_STALL_FWD_SOFTMAX, 0) == abi.ATTN_OK
     assert lib.attn_debug_stall(abi.ATTN_STALL_NONE, 0) == abi.ATTN_OK
+
+
+def test_forward_splits_pairs_only_for_few_long_heads(abi):
+    # pieces keep at least 8 key tiles: one head of N = 4096 (16 pairs of
+    # 32 key tiles) is cut along the keys into 4 pieces; 16 heads x 64 pairs at
+    # N = 16384 fill any GPU, and short rows are never cut
+    lib = abi.lib()
+
+    def ws(**kw):
+        N = kw.get("N", 256)
+        d = kw.get("d", 64)
+        H = kw.get("H", 3)
+        p = _params(abi, stride_b=H * N * d, stride_h=N * d, stride_n=d, **kw)
+        return lib.attn_workspace_size(ctypes.byref(p), 0)
+
+    assert ws(B=1, H=16, N=16384, d=128) == 256
+    assert ws(B=2, H=3, N=1000) == 256
+    nb, pieces = 32, 4
+    rows = pieces * 1 * 1 * (nb // 2) * 256
+    assert ws(B=1, H=1, N=4096, d=128) == 256 + rows * 128 * 4 + rows * 4
+    # key padding without the causal mask keeps its longest-first order unsplit
+    assert ws(B=1, H=1, N=4096, d=128, key_lens=0x3000) == 256
+    assert ws(B=1, H=1, N=4096, d=128, key_lens=0x3000, causal=1) > 256

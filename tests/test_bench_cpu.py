@@ -149,3 +149,12 @@ def test_roofline_takes_the_longest_stage_and_the_nearer_bound():
     roof = bench.roofline(w, r)
     assert roof["kernel"] == "bwd_preprocess_kernel" and roof["bound"] == "hbm"
     assert roof["unit"] == "GB/s"
+
+
+def test_workload_overrides_parse_into_fields():
+    assert bench.parse_overrides(["H=2", "dropout_p=0.25", "dtype=fp8"]) == \
+        {"H": 2, "dropout_p": 0.25, "dtype": "fp8"}
+    with pytest.raises(SystemExit):
+        bench.parse_overrides(["heads=2"])
+    w = workloads.get("long-causal-16384", **bench.parse_overrides(["H=2"]))
+    assert (w.H, w.N, w.d, w.causal) == (2, 16384, 128, True)

@@ -110,6 +110,13 @@ def test_multi_query_heads_and_large_scores(ea):
 
 
 @pytest.mark.skipif(FP8 is None, reason="torch without float8_e4m3fn")
+def test_split_pairs_of_a_long_single_head(ea):
+    # one head of 4096 keys: 16 query-tile pairs, each cut into pieces along
+    # the keys whose (O, L) are merged by the logsumexp rule
+    _check_full(ea, 1, 1, 1, 4096, seed=8, causal=True)
+
+
+@pytest.mark.skipif(FP8 is None, reason="torch without float8_e4m3fn")
 def test_descale_factors_are_applied(ea):
     (q, _), (k, _), (v, _) = workloads.random_case_fp8(1, 2, 256, 128, 6)
     o1, l1 = _run(ea, q, k, v, (0.5, 0.25, 2.0), scale=0.125)

@@ -182,6 +182,51 @@ def test_empty_problem_sizes(ea):
         assert o.shape == q.shape and tuple(lse.shape) == shape[:3]
 
 
+# ------------------------------------------- split pairs (few heads) ----
+
+@pytest.mark.parametrize("B,H,N,d,kw", [
+    (1, 1, 4096, 128, dict(causal=True)),                     # 16 pairs, 4 pieces each
+    (1, 2, 2100, 64, dict(causal=False)),                     # a ragged last tile
+    (1, 2, 3000, 128, dict(causal=True, key_lens=[2555])),
+    (2, 1, 2500, 64, dict(causal=True, key_lens=[2500, 0])),  # an empty sequence
+    (1, 3, 2048, 64, dict(dropout_p=0.2)),
+    (1, 2, 2400, 128, dict(block=True)),
+])
+def test_split_pairs_match_the_oracle(ea, B, H, N, d, kw):
+    """Few heads, long rows: too few query-tile pairs to fill the GPU, so the
+    forward cuts each pair's keys into pieces of at least eight key tiles
+    and merges their (O, L) by the logsumexp rule."""
+    kw = dict(kw)
+    bm = workloads.make_block_mask((N + 127) // 128, 0.4, seed=N) if kw.pop("block", False) \
+        else None
+    inp = _inputs(B, H, N, d, seed=N + d, block_mask=bm, **kw)
+    q = inp["q"].cuda()
+    inp_dev = dict(inp, q=q, k=inp["k"].cuda(),
+                   key_lens=None if inp["key_lens"] is None else inp["key_lens"].cuda(),
+                   block_mask=None if bm is None else bm.cuda())
+    p = ea.make_params(q, k=inp_dev["k"], causal=inp["causal"], key_lens=inp_dev["key_lens"],
+                       block_mask=inp_dev["block_mask"])
+    assert ea.workspace_size(p, False) > 256 + (1 << 16)   # the partials are there
+    _check_full(ea, inp)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_unsplit_pairs_with_every_mask(ea, d):
+    # enough query-tile pairs to fill the GPU (10 x 20 heads x 2 pairs): the
+    # pieces are whole pairs and O, L are written directly
+    B, H, N = 10, 20, 480
+    bm = workloads.make_block_mask(4, 0.6, seed=d)
+    lens = [480, 1, 129, 300, 0, 480, 256, 255, 400, 77]
+    inp = _inputs(B, H, N, d, seed=d + 1, causal=True, key_lens=lens, block_mask=bm,
+                  dropout_p=0.1)
+    p = ea.make_params(inp["q"].cuda(), k=inp["k"].cuda(), causal=True,
+                       key_lens=inp["key_lens"].cuda(), block_mask=bm.cuda())
+    nb = 4
+    assert ea.workspace_size(p, False) == 256 + (nb * 4 + 255) // 256 * 256 + \
+        (nb * nb * 2 + 255) // 256 * 256
+    _check_full(ea, inp)
+
+
 # ------------------------------------------------- full-size workloads ----
 
 @pytest.mark.parametrize("name", ["bert-large", "gpt2-1k", "gpt2-4k", "long-causal-512",

@@ -87,6 +87,12 @@ def test_grouped_heads_with_per_head_block_mask(ea):
     _check(ea, _inputs(B, H, H_kv, N, 64, seed=13, block_mask=bm, causal=True))
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_grouped_heads_with_split_pairs(ea, d):
+    # few heads and long rows: the forward's pairs are cut along the keys
+    _check(ea, _inputs(1, 4, 1, 2048, d, seed=21 + d, causal=True, dropout_p=0.1))
+
+
 def test_multi_query_fp32_forward(ea):
     _check(ea, _inputs(1, 4, 1, 200, 64, seed=3, dtype=torch.float32), backward=False)
 
