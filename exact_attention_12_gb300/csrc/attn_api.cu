@@ -58,6 +58,7 @@ struct WsLayout {
   size_t vt = 0;                       // FP8 forward: V^T [B * H_kv][d][nb * 128]
   size_t part_o = 0, part_l = 0;       // forward of split pairs: partial O, L
   int splits = 1;
+  size_t qhi = 0, qlo = 0, khi = 0, klo = 0, vt32 = 0;   // fp32 forward: TF32 parts
   size_t lse2 = 0, dsum = 0, dq_acc = 0;   // backward only
   size_t total = 0;
 };
@@ -120,6 +121,21 @@ WsLayout layout(const attn_params* p, bool bwd) {
     L.vt = off;
     const size_t H_kv = static_cast<size_t>(p->H_kv == 0 ? p->H : p->H_kv);
     off = round_up(off + static_cast<size_t>(p->B) * H_kv * p->d * nb * kTile, 256);
+  }
+  if (p->dtype == ATTN_FP32 && !bwd) {
+    const size_t H_kv = static_cast<size_t>(p->H_kv == 0 ? p->H : p->H_kv);
+    const size_t qn = static_cast<size_t>(p->B) * p->H * p->N * p->d * sizeof(float);
+    const size_t kn = static_cast<size_t>(p->B) * H_kv * p->N * p->d * sizeof(float);
+    L.qhi = off;
+    off = round_up(off + qn, 256);
+    L.qlo = off;
+    off = round_up(off + qn, 256);
+    L.khi = off;
+    off = round_up(off + kn, 256);
+    L.klo = off;
+    off = round_up(off + kn, 256);
+    L.vt32 = off;
+    off = round_up(off + static_cast<size_t>(p->B) * H_kv * p->d * nb * kTile * sizeof(float), 256);
   }
   if (!bwd && (L.splits = fwd_splits(p)) > 1) {
     const size_t prows = static_cast<size_t>(L.splits) * p->B * p->H * ((nb + 1) / 2) * 2 * kTile;
@@ -404,9 +420,35 @@ attn_status attn_fwd(const attn_params* p, const void* q, const void* k, const v
 
   cudaError_t e;
   if (p->dtype == ATTN_FP32) {
-    e = attn::launch_fwd_fp32(static_cast<const float*>(q), static_cast<const float*>(k),
-                              static_cast<const float*>(v), a, s);
-    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "forward (fp32) launch");
+    // TF32 hi / lo parts of q, k and TF32 V^T into the workspace, then the
+    // tensor-core forward on them
+    const int H_kv = kv_heads(p);
+    const int npad = a.m.nb * kTile;
+    const int64_t d64 = p->d;
+    attn::Tf32Buffers buf{reinterpret_cast<float*>(w + L.qhi), reinterpret_cast<float*>(w + L.qlo),
+                          reinterpret_cast<float*>(w + L.khi), reinterpret_cast<float*>(w + L.klo),
+                          reinterpret_cast<float*>(w + L.vt32), npad};
+    attn::Tf32Maps tm{};
+    const int64_t qsh = static_cast<int64_t>(p->N) * d64, ksh = qsh;
+    if ((st = make_map(&tm.qhi, buf.qhi, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->B, p->H, p->N,
+                       p->d, p->H * qsh, qsh, d64, 32, kTile, CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK ||
+        (st = make_map(&tm.qlo, buf.qlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->B, p->H, p->N,
+                       p->d, p->H * qsh, qsh, d64, 32, kTile, CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK ||
+        (st = make_map(&tm.khi, buf.khi, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->B, H_kv, p->N,
+                       p->d, H_kv * ksh, ksh, d64, 32, kTile, CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK ||
+        (st = make_map(&tm.klo, buf.klo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->B, H_kv, p->N,
+                       p->d, H_kv * ksh, ksh, d64, 32, kTile, CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK)
+      return st;
+    // V^T [B, H_kv, d, N]: rows of npad keys, N of them valid (the rest read as 0)
+    const int64_t dn = d64 * npad;
+    if ((st = make_map(&tm.vt, buf.vt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->B, H_kv, p->d, p->N,
+                       H_kv * dn, dn, npad, 32, p->d, CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK)
+      return st;
+    e = attn::launch_tf32_split(static_cast<const float*>(q), static_cast<const float*>(k),
+                                static_cast<const float*>(v), a, buf, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fp32 split launch");
+    e = attn::launch_fwd_tf32(tm, a, s);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "forward (fp32, tf32 tensor cores) launch");
   }
   attn::TensorMaps tm{};
   const bool fp8 = p->dtype == ATTN_FP8_E4M3;

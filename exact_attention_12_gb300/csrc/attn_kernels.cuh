@@ -44,7 +44,8 @@ enum WaitSite : int {
   kSiteFwdPFull, kSiteFwdPvDone, kSiteFwdUnit,
   kSiteBwdLoad = 20, kSiteBwdKV, kSiteBwdQ, kSiteBwdMma, kSiteBwdSoft, kSiteBwdDq,
   kSiteBwdEmpty, kSiteBwdFree, kSiteBwdSmem,
-  kSiteDecode = 40
+  kSiteDecode = 40,
+  kSiteTf32Load = 50, kSiteTf32Mma, kSiteTf32Soft
 };
 
 // One-shot stalls armed by attn_debug_stall (a test of the kernels' own
@@ -170,8 +171,22 @@ cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdArgs& a, cudaStream_t
 cudaError_t launch_fwd_fp8(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_fp8_transpose_v(const uint8_t* v, int64_t sb, int64_t sh, int64_t sn, int B,
                                    int H_kv, int N, int d, int npad, uint8_t* vt, cudaStream_t s);
-cudaError_t launch_fwd_fp32(const float* q, const float* k, const float* v, const FwdArgs& a,
-                            cudaStream_t s);
+// fp32 inputs on the tensor cores (kind::tf32): the split kernel writes the
+// TF32 hi and lo parts of q, k and the TF32 V^T into the workspace, the
+// forward reads them through these maps (fp32, 32-column x 128-row boxes;
+// V^T: 32-key x d-row boxes, 128-byte swizzle).
+struct Tf32Maps {
+  CUtensorMap qhi, qlo, khi, klo, vt;
+};
+struct Tf32Buffers {
+  float *qhi, *qlo;               // [B*H][N][d]
+  float *khi, *klo;               // [B*H_kv][N][d]
+  float* vt;                      // [B*H_kv][d][npad]
+  int npad;                       // keys per V^T row: N rounded up to 128
+};
+cudaError_t launch_tf32_split(const float* q, const float* k, const float* v, const FwdArgs& a,
+                              const Tf32Buffers& buf, cudaStream_t s);
+cudaError_t launch_fwd_tf32(const Tf32Maps& tm, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_compact_mask(const uint8_t* mask, int64_t head_stride, int masks, int nb,
                                 int by_column, int32_t* cnt, uint16_t* idx, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const void* o, const void* dout, const BwdArgs& a,
