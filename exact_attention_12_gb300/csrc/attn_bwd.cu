@@ -19,8 +19,8 @@
 //                      S^T  = K_j Q_i^T      (TMEM)
 //                      dP^T = V_j dO_i^T     (TMEM)
 //                      dV  += P~^T dO_i      (A = P~^T in TMEM, bf16)
-//                      dK  += dS^T Q_i       (A = dS^T in shared memory)
-//                      dQ_i = dS K_j         (A = the same dS^T buffer read
+//                      dK  += dS^T Q_i       (A = dS^T in TMEM, bf16)
+//                      dQ_i = dS K_j         (A = dS^T in shared memory, read
 //                                             as an MN-major operand)
 //                    dK and dV stay in TMEM for the whole loop; each dQ_i is
 //                    staged through shared memory and added into the fp32
@@ -32,15 +32,18 @@
 //              query columns 64*(w/4) .. +63 of the S^T / dP^T tiles.  The
 //              backward needs no row reduction, so the 128 columns of a row
 //              split freely between two warps.  Per query tile: P^T and the
-//              dropout mask, P~^T into TMEM, dS^T into shared memory, and the
-//              drain of the previous dQ tile; epilogue writes dK, dV.
+//              dropout mask, P~^T into TMEM, dS^T into TMEM and shared
+//              memory, and the drain of the previous dQ tile; epilogue
+//              writes dK, dV.
 //   warp 8     TMA producer (K_j, V_j once; Q_i, dO_i per query tile).
 //   warp 9     MMA issuer, TMEM owner.  (warps 10-11 idle: they complete the
 //              third warpgroup, whose registers go to the compute warps.)
 // TMEM columns: S^T [0,128) -- P~^T (bf16 pairs) overwrites columns [0,32)
 //   and [64,96), each half by the warps that read that half of S^T --,
-//   dP^T [128,256), dV [256,256+d), dK [256+d,256+2d), dQ [384,448) for
-//   d = 64 and over the dP^T columns for d = 128.
+//   dP^T [128,256) -- dS^T (bf16 pairs) overwrites [128,160) and [192,224)
+//   the same way --, dV [256,256+d), dK [256+d,256+2d), dQ [384,448) for
+//   d = 64 and over the dP^T columns for d = 128 (issued after dK, which
+//   has read dS^T: the MMAs of one thread execute in order).
 #include <cuda_bf16.h>
 
 #include "attn_kernels.cuh"
@@ -491,18 +494,16 @@ __global__ void __launch_bounds__(384, 1)
                            smem_u32(sQ + ((it + 1) % QS) * C::kTileBytes));
               mma_commit(&ctl.sfull);
             }
-            // dK += dS^T Q_i
+            // dK += dS^T Q_i; dS^T pairs of query rows 0..63 sit in columns
+            // [128,160), those of rows 64..127 in [192,224)
             if (!(ok = mbar_wait(&ctl.dsfull, ph, wc, kSiteBwdMma))) break;
             tc_fence_after();
             {
-              const uint64_t dds = smem_desc(ds_base, 16, 1024);
               const uint64_t dq = smem_desc(q_base, C::kBoxBytes, 1024);
 #pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-                mma_ss(tmem + C::kDKCol, desc_plus(dds, off), desc_plus(dq, kk * 2048), kIdKN,
-                       (i > 0 || kk > 0) ? 1u : 0u);
-              }
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                mma_ts(tmem + C::kDKCol, tmem + C::kDPCol + kk * 8 + (kk >= 4 ? 32 : 0),
+                       desc_plus(dq, kk * 2048), kIdKN, (i > 0 || kk > 0) ? 1u : 0u);
             }
             // dQ_i = dS K_j (its columns: drained copy of the previous dQ read out)
             if (!C::kDqAliasesDp && it >= 1) {
@@ -705,7 +706,10 @@ __global__ void __launch_bounds__(384, 1)
         for (int u = 0; u < 4; ++u)
           *reinterpret_cast<uint4*>(region + swz(lane, cc * 4 + u)) =
               make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        // the dK MMA's A operand: over this warp's dP^T half, already read
+        tmem_st16(tl + C::kDPCol + half * 64 + cc * 16, pk);
       }
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
