@@ -60,6 +60,8 @@ struct WsLayout {
   int splits = 1;
   size_t qhi = 0, qlo = 0, khi = 0, klo = 0, vt32 = 0;   // fp32 forward: TF32 parts
   size_t lse2 = 0, dsum = 0, dq_acc = 0;   // backward only
+  size_t part_dk = 0, part_dv = 0;         // backward of split key tiles: partial dK, dV
+  int bwd_splits = 1;
   size_t total = 0;
 };
 
@@ -101,6 +103,24 @@ int fwd_splits(const attn_params* p) {
   if (units <= 0 || units >= sms) return 1;
   long long k = (2 * sms + units - 1) / units;
   if (k > nb / kMinPieceTiles) k = nb / kMinPieceTiles;
+  if (k > 16) k = 16;
+  return k < 1 ? 1 : static_cast<int>(k);
+}
+
+// Pieces per key tile in the backward, by the same rule: with fewer key
+// tiles (of all key/value heads) than SMs, each key tile's query tiles are
+// cut into pieces of at least kMinPieceTiles (counted over the longest walk:
+// nb query tiles of each of the H / H_kv query heads), about two units per
+// SM, at most 16; otherwise 1.
+int bwd_splits(const attn_params* p) {
+  const long long nb = (static_cast<long long>(p->N) + kTile - 1) / kTile;
+  const long long H_kv = p->H_kv == 0 ? p->H : p->H_kv;
+  const long long units = nb * p->B * H_kv;
+  const long long sms = sm_count();
+  if (units <= 0 || units >= sms) return 1;
+  const long long walk = nb * (H_kv > 0 ? p->H / H_kv : 1);
+  long long k = (2 * sms + units - 1) / units;
+  if (k > walk / kMinPieceTiles) k = walk / kMinPieceTiles;
   if (k > 16) k = 16;
   return k < 1 ? 1 : static_cast<int>(k);
 }
@@ -152,6 +172,14 @@ WsLayout layout(const attn_params* p, bool bwd) {
     off = round_up(off + bhpad * sizeof(float), 256);
     L.dq_acc = off;
     off = round_up(off + bhn * p->d * sizeof(float), 256);
+    if ((L.bwd_splits = bwd_splits(p)) > 1) {
+      const size_t prows =
+          static_cast<size_t>(L.bwd_splits) * p->B * (p->H_kv == 0 ? p->H : p->H_kv) * nb * kTile;
+      L.part_dk = off;
+      off = round_up(off + prows * p->d * sizeof(float), 256);
+      L.part_dv = off;
+      off = round_up(off + prows * p->d * sizeof(float), 256);
+    }
   }
   L.total = off;
   return L;
@@ -525,6 +553,12 @@ attn_status bwd_setup(const attn_params* p, void* ws, size_t ws_bytes, attn::Bwd
   a->status = reinterpret_cast<int*>(w);
   a->sched = reinterpret_cast<int*>(w + kSchedOffset);
   a->timeout_ns = kTimeoutNs;
+  a->splits = L->bwd_splits;
+  a->part_rows = a->npad;
+  if (L->bwd_splits > 1) {
+    a->part_dk = reinterpret_cast<float*>(w + L->part_dk);
+    a->part_dv = reinterpret_cast<float*>(w + L->part_dv);
+  }
   return ATTN_OK;
 }
 

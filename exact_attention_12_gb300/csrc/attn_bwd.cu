@@ -89,11 +89,11 @@ struct BwdCfg {
 constexpr int kBwdUnitRing = 4;   // claimed units not yet handed to every role
 constexpr int kBwdClaimAhead = 2;  // claim the next unit this many query tiles early
 
-// A claimed unit (one key tile of one (b, key/value head)) as the producer
-// publishes it.
+// A claimed unit (one key tile of one (b, key/value head), or one piece of
+// its query tiles when key tiles are split) as the producer publishes it.
 struct BwdUnit {
   int w;      // unit index; -1: no more units
-  int kt, bhk;
+  int kt, bhk, piece;
   int n;      // (query head, query tile) pairs it visits
 };
 
@@ -120,26 +120,38 @@ struct QList {
   }
 };
 
-__device__ __forceinline__ QList bwd_tiles(const MaskArgs& m, int kt, int bh, int limit) {
+// First position in the sorted list p[0, n) whose tile index is >= q.
+__device__ __forceinline__ int lower_bound_q(const uint16_t* p, int n, int q) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (int(p[mid]) < q) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// The query tiles key tile kt of head bh is visited by, within piece `piece`
+// of `splits`: the tiles [first, nb) (first = kt when causal) are cut into
+// equal index ranges.
+__device__ __forceinline__ QList bwd_tiles(const MaskArgs& m, int kt, int bh, int limit,
+                                           int piece, int splits) {
   QList t{nullptr, 0, 0};
   if (kt * kTile >= limit) return t;   // every key of the tile is masked
   const int first = m.causal ? kt : 0;
+  const int span = m.nb - first;
+  const int qlo = first + piece * span / splits;
+  const int qhi = first + (piece + 1) * span / splits;
   if (m.list_idx == nullptr) {
-    t.first = first;
-    t.n = m.nb - first;
+    t.first = qlo;
+    t.n = qhi - qlo;
     return t;
   }
   const size_t col = static_cast<size_t>(m.mask_per_head ? bh : 0) * m.nb + kt;
   const uint16_t* p = m.list_idx + col * m.nb;
   const int cnt = m.list_cnt[col];
-  int lo = 0, hi = cnt;   // first entry >= first (the list is sorted)
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (int(p[mid]) < first) lo = mid + 1; else hi = mid;
-  }
   t.idx = p;
-  t.first = lo;
-  t.n = cnt - lo;
+  t.first = lower_bound_q(p, cnt, qlo);
+  t.n = lower_bound_q(p, cnt, qhi) - t.first;
   return t;
 }
 
@@ -154,14 +166,14 @@ __device__ __forceinline__ int key_limit(const MaskArgs& m, int b) {
 // query-tile list (the block mask may differ per head).
 struct QHeadWalk {
   const MaskArgs* m;
-  int kt, b, h0, g, limit;
+  int kt, b, h0, g, limit, piece, splits;
   int qh = -1;
   QList list{nullptr, 0, 0};
   int i = 0;
   __device__ __forceinline__ bool next(int& h, int& qtile) {
     while (qh < 0 || i >= list.n) {
       if (++qh >= g) return false;
-      list = bwd_tiles(*m, kt, b * m->H + h0 + qh, limit);
+      list = bwd_tiles(*m, kt, b * m->H + h0 + qh, limit, piece, splits);
       i = 0;
     }
     h = h0 + qh;
@@ -241,17 +253,20 @@ __device__ __forceinline__ void mma_kt_qt(uint32_t d_tmem, uint32_t a_base, uint
   }
 }
 
-// Unit w -> (key tile, b * H_kv + key/value head): head groups of G
+// Unit w -> (key tile, b * H_kv + key/value head, piece): head groups of G
 // consecutive (b, hk); within a group, key tiles in ascending order (heaviest
-// first for causal).
-__device__ __forceinline__ void bwd_unit_of(const MaskArgs& m, int w, int& kt, int& bhk) {
+// first for causal), a key tile's K pieces together.
+__device__ __forceinline__ void bwd_unit_of(const MaskArgs& m, int K, int w, int& kt, int& bhk,
+                                            int& piece) {
   const int BHk = m.B * m.H_kv;
-  const int G = m.head_group, per = G * m.nb, nfull = BHk / G;
+  const int G = m.head_group, per = G * m.nb * K, nfull = BHk / G;
   const int g = w < nfull * per ? w / per : nfull;
   const int gs = g < nfull ? G : BHk - nfull * G;
   const int rem = w - g * per;
-  kt = rem / gs;
-  bhk = g * G + rem % gs;
+  kt = rem / (gs * K);
+  const int r2 = rem % (gs * K);
+  bhk = g * G + r2 / K;
+  piece = r2 % K;
 }
 
 template <int D, bool DROPOUT>
@@ -281,7 +296,8 @@ __global__ void __launch_bounds__(384, 1)
   const MaskArgs& m = a.m;
   // persistent: CTA i starts with unit i (one key tile of one (b, key/value
   // head)); later units are claimed from the scheduler counter
-  const int total = m.nb * m.B * m.H_kv;
+  const int K = a.splits;   // pieces per key tile
+  const int total = m.nb * m.B * m.H_kv * K;
 
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
@@ -341,14 +357,14 @@ __global__ void __launch_bounds__(384, 1)
           if (kw >= 1 && !(ok = mbar_wait(&ctl.claim, (kw - 1) & 1, wc, kSiteBwdLoad))) break;
           const int w = pub == 0 ? static_cast<int>(blockIdx.x)
                                  : static_cast<int>(gridDim.x) + atomicAdd(a.sched, 1);
-          BwdUnit u{-1, 0, 0, 0};
+          BwdUnit u{-1, 0, 0, 0, 0};
           if (w < total) {
             u.w = w;
-            bwd_unit_of(m, w, u.kt, u.bhk);
+            bwd_unit_of(m, K, w, u.kt, u.bhk, u.piece);
             const int ub = u.bhk / m.H_kv, uhk = u.bhk - ub * m.H_kv;
             const int ulim = key_limit(m, ub);
             for (int qh = 0; qh < m.kv_group; ++qh)
-              u.n += bwd_tiles(m, u.kt, ub * m.H + uhk * m.kv_group + qh, ulim).n;
+              u.n += bwd_tiles(m, u.kt, ub * m.H + uhk * m.kv_group + qh, ulim, u.piece, K).n;
           }
           const int r = pub % kBwdUnitRing;
           if (pub >= kBwdUnitRing &&
@@ -370,7 +386,7 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_4d(sV + x * C::kBoxBytes, &tv, &ctl.kvfull, x * 64, k0, hk, b);
           }
           ++kw;
-          QHeadWalk walk{&m, u.kt, b, hk * m.kv_group, m.kv_group, key_limit(m, b)};
+          QHeadWalk walk{&m, u.kt, b, hk * m.kv_group, m.kv_group, key_limit(m, b), u.piece, K};
           int h, qtile;
           for (int i = 0; ok && walk.next(h, qtile); ++i) {
             const int q0 = qtile * kTile;
@@ -574,7 +590,7 @@ __global__ void __launch_bounds__(384, 1)
     const int kj = k0 + r;                 // global key index
     const bool key_ok = kj < limit;
     const bool tile_keys_ok = k0 + kTile <= limit;   // no key of the tile is masked
-    QHeadWalk walk{&m, kt, b, hk * m.kv_group, m.kv_group, limit};
+    QHeadWalk walk{&m, kt, b, hk * m.kv_group, m.kv_group, limit, u.piece, K};
     int h = 0, qtile = 0;
     int prev_h = 0, prev_q0 = 0;   // the pair whose dQ is drained next
     for (int i = 0; i < n && walk.next(h, qtile); ++i, ++it) {
@@ -730,7 +746,34 @@ __global__ void __launch_bounds__(384, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl.done, kw & 1, wc, kSiteBwdSoft));
       if (ok) tc_fence_after();
     }
-    if (ok) {
+    if (ok && K > 1) {
+      // a piece of a split key tile: its dV and (unscaled) dK sums in fp32,
+      // added up with the other pieces' afterwards
+      const int64_t prow = (static_cast<int64_t>(u.piece) * m.B * m.H_kv + u.bhk) * a.part_rows + kj;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        float* dst = (which ? a.part_dk : a.part_dv) + prow * D + half * C::kHalf;
+#pragma unroll
+        for (int c = 0; c < C::kHalf; c += 32) {
+          uint32_t o[32];
+          if (n > 0) {
+            tmem_ld32(tl + (which ? C::kDKCol : C::kDVCol) + half * C::kHalf + c, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) o[t] = 0u;
+          }
+          if (kj < m.N) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              d4[t] = key_ok ? make_float4(__uint_as_float(o[4 * t]), __uint_as_float(o[4 * t + 1]),
+                                           __uint_as_float(o[4 * t + 2]), __uint_as_float(o[4 * t + 3]))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+      }
+    } else if (ok) {
       const int64_t row_off = b * a.kv_stride_b + hk * a.kv_stride_h +
                               static_cast<int64_t>(kj) * a.kv_stride_n + half * C::kHalf;
 #pragma unroll
@@ -853,6 +896,44 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(__nv_bfloat16* __restri
   *reinterpret_cast<uint4*>(dq + b * a.stride_b + h * a.stride_h + n * a.stride_n + part * 8) = out;
 }
 
+// dK, dV of split key tiles: the pieces' fp32 sums added up, dK scaled by c,
+// converted to bf16.  One thread per eight columns of a key row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_merge_kernel(const BwdArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
+  constexpr int kLanes = D / 8;
+  const MaskArgs& m = a.m;
+  const int64_t rows = static_cast<int64_t>(m.B) * m.H_kv * m.N;
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = gtid / kLanes;
+  if (row >= rows) return;
+  const int part = static_cast<int>(gtid % kLanes);
+  const int64_t n = row % m.N, bhk = row / m.N;
+  const int64_t piece_stride = static_cast<int64_t>(m.B) * m.H_kv * a.part_rows * D;
+  const int64_t off = (bhk * a.part_rows + n) * D + part * 8;
+  float dk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, dv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < a.splits; ++s) {
+    const float4* pk = reinterpret_cast<const float4*>(a.part_dk + s * piece_stride + off);
+    const float4* pv = reinterpret_cast<const float4*>(a.part_dv + s * piece_stride + off);
+    const float4 k0 = pk[0], k1 = pk[1], v0 = pv[0], v1 = pv[1];
+    dk[0] += k0.x; dk[1] += k0.y; dk[2] += k0.z; dk[3] += k0.w;
+    dk[4] += k1.x; dk[5] += k1.y; dk[6] += k1.z; dk[7] += k1.w;
+    dv[0] += v0.x; dv[1] += v0.y; dv[2] += v0.z; dv[3] += v0.w;
+    dv[4] += v1.x; dv[5] += v1.y; dv[6] += v1.z; dv[7] += v1.w;
+  }
+  const int64_t b = bhk / m.H_kv, hk = bhk % m.H_kv;
+  const int64_t dst = b * a.kv_stride_b + hk * a.kv_stride_h + n * a.kv_stride_n + part * 8;
+  const float c = a.scale;
+  uint4 ko, vo;
+  ko.x = pack_bf16x2(dk[0] * c, dk[1] * c); ko.y = pack_bf16x2(dk[2] * c, dk[3] * c);
+  ko.z = pack_bf16x2(dk[4] * c, dk[5] * c); ko.w = pack_bf16x2(dk[6] * c, dk[7] * c);
+  vo.x = pack_bf16x2(dv[0], dv[1]); vo.y = pack_bf16x2(dv[2], dv[3]);
+  vo.z = pack_bf16x2(dv[4], dv[5]); vo.w = pack_bf16x2(dv[6], dv[7]);
+  *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dk) + dst) = ko;
+  *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dv) + dst) = vo;
+}
+
 template <int D, bool DROP>
 cudaError_t launch_main(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s) {
   using C = BwdCfg<D>;
@@ -873,10 +954,14 @@ cudaError_t launch_main(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s) 
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const long long units = static_cast<long long>(a.m.nb) * a.m.B * a.m.H_kv;
+  const long long units = static_cast<long long>(a.m.nb) * a.m.B * a.m.H_kv * a.splits;
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
-  return launch_pdl(bwd_bf16_kernel<D, DROP>, dim3(grid), dim3(C::kThreads), C::kSmem, s, tm.q,
-                    tm.k, tm.v, tm.dout, tm.dq_acc, a);
+  e = launch_pdl(bwd_bf16_kernel<D, DROP>, dim3(grid), dim3(C::kThreads), C::kSmem, s, tm.q,
+                 tm.k, tm.v, tm.dout, tm.dq_acc, a);
+  if (e != cudaSuccess || a.splits <= 1) return e;
+  const int64_t threads = static_cast<int64_t>(a.m.B) * a.m.H_kv * a.m.N * (D / 8);
+  return launch_pdl(bwd_merge_kernel<D>, dim3(static_cast<unsigned>((threads + 255) / 256)),
+                    dim3(256), 0, s, a);
 }
 
 unsigned blocks_for(int64_t threads) {

@@ -133,6 +133,13 @@ struct BwdArgs {
   int* sched;                     // workspace scheduler words: next unit, CTAs finished
   uint64_t timeout_ns;
   int stall;                      // kStallBwdCompute: compute warp 0 withholds its first P-ready arrive
+  // split key tiles (too few key tiles to fill the GPU): each key tile's
+  // query tiles are cut into `splits` pieces whose dK, dV sums (fp32, dK
+  // unscaled) go to the workspace, then added into dk, dv; 1 = unsplit
+  int splits;
+  int part_rows;                  // rows per (b, key/value head) in the partials: nb x 128
+  float* part_dk;                 // [splits][B*H_kv][part_rows][d]
+  float* part_dv;
 };
 
 // Decode step: query rows per CTA (the key/value group's heads x n_q) at most.

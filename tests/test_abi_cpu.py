@@ -250,3 +250,21 @@ def test_forward_splits_pairs_only_for_few_long_heads(abi):
     # key padding without the causal mask keeps its longest-first order unsplit
     assert ws(B=1, H=1, N=4096, d=128, key_lens=0x3000) == 256
     assert ws(B=1, H=1, N=4096, d=128, key_lens=0x3000, causal=1) > 256
+
+
+def test_backward_splits_key_tiles_only_for_few_long_heads(abi):
+    # one head of 4096 keys has 32 key tiles for any GPU's SMs: each key
+    # tile's 32 query tiles are cut into 4 pieces of 8, and the pieces' dK,
+    # dV partials (fp32, [pieces][B*H_kv][nb*128][d] each) join the workspace
+    lib = abi.lib()
+
+    def ws(**kw):
+        N, d, H = kw.get("N", 256), kw.get("d", 64), kw.get("H", 3)
+        p = _params(abi, stride_b=H * N * d, stride_h=N * d, stride_n=d, **kw)
+        return lib.attn_workspace_size(ctypes.byref(p), 1)
+
+    N, d, nb = 4096, 128, 32
+    base = 256 + 2 * N * 4 + N * d * 4          # row statistics + fp32 dQ accumulator
+    assert ws(B=1, H=1, N=N, d=d) == base + 2 * 4 * nb * 128 * d * 4
+    assert ws(B=1, H=16, N=16384, d=128) == 256 + 2 * 16 * 16384 * 4 + 16 * 16384 * 128 * 4
+    assert ws(B=2, H=3, N=700) == 256 + 2 * 6 * 768 * 4 + 6 * 700 * 64 * 4   # short: unsplit

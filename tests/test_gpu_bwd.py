@@ -184,6 +184,28 @@ def test_bwd_keep_bits_are_exact(ea, d, causal):
     assert np.array_equal(got, want), int((got != want).sum())
 
 
+@pytest.mark.parametrize("B,H,N,d,kw", [
+    (1, 1, 4096, 128, dict(causal=True)),                     # 32 key tiles, 4 pieces each
+    (1, 2, 2100, 64, dict(dropout_p=0.2)),                    # a ragged last tile
+    (2, 1, 2500, 128, dict(causal=True, key_lens=[2500, 0])),
+    (1, 2, 2400, 64, dict(block=True)),
+])
+def test_split_key_tiles_match_the_oracle(ea, B, H, N, d, kw):
+    """Few heads, long rows: too few key tiles to fill the GPU, so the
+    backward cuts each key tile's query tiles into pieces and adds up their
+    dK, dV afterwards."""
+    kw = dict(kw)
+    bm = workloads.make_block_mask((N + 127) // 128, 0.4, seed=N) if kw.pop("block", False) \
+        else None
+    inp = _inputs(B, H, N, d, seed=N + d, block_mask=bm, **kw)
+    p = ea.make_params(inp["q"].cuda(), causal=inp["causal"],
+                       key_lens=None if inp["key_lens"] is None else inp["key_lens"].cuda(),
+                       block_mask=None if bm is None else bm.cuda())
+    nb = (N + 127) // 128
+    assert ea.workspace_size(p, True) > 256 + B * H * nb * 128 * 8 + B * H * N * d * 4 + (1 << 16)
+    _check(ea, inp)
+
+
 def test_strided_bnhd_layout(ea):
     # [B, N, H, d] storage viewed as [B, H, N, d], backward included
     B, H, N, d = 2, 3, 300, 64

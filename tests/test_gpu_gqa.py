@@ -89,7 +89,8 @@ def test_grouped_heads_with_per_head_block_mask(ea):
 
 @pytest.mark.parametrize("d", [64, 128])
 def test_grouped_heads_with_split_pairs(ea, d):
-    # few heads and long rows: the forward's pairs are cut along the keys
+    # few heads and long rows: the forward's pairs are cut along the keys and
+    # the backward's key tiles along their (query head, query tile) walks
     _check(ea, _inputs(1, 4, 1, 2048, d, seed=21 + d, causal=True, dropout_p=0.1))
 
 
