@@ -81,6 +81,7 @@ def test_block_mask(ea, per_head):
     bm = (torch.rand(shape, generator=g) < 0.4).to(torch.uint8)
     if per_head:
         bm[1, 0, :, 3] = 0          # a key tile no query tile visits
+        bm[0, 1, 2, :] = 0          # a query tile no key tile visits: dQ = 0
     else:
         bm[:, 3] = 0
     _check(ea, _inputs(B, H, N, 64, seed=23, block_mask=bm))
@@ -95,6 +96,35 @@ def test_everything_at_once(ea, d):
 
 def test_long_rows_many_query_tiles(ea):
     _check(ea, _inputs(1, 2, 1100, 128, seed=25, causal=True, std=0.5))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_staged_calls_match_the_oracle(ea, d):
+    """attn_bwd_preprocess, attn_bwd_main and attn_bwd_dq called one by one
+    on one workspace (the bench times them so) give the oracle's gradients."""
+    import ctypes
+    from exact_attention_12_gb300 import _abi
+    inp = _inputs(2, 3, 700, d, seed=27 + d, causal=True, key_lens=[700, 433], dropout_p=0.1)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    kw = api_kwargs(inp)
+    o, lse = ea.attention_fwd(q, k, v, **kw)
+    p = ea.make_params(q, k=k, **kw)
+    ws = torch.zeros(ea.workspace_size(p, True), dtype=torch.uint8, device="cuda")
+    dq, dk, dv = (torch.full_like(t, float("nan")) for t in (q, k, v))
+    lib, s = _abi.lib(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    P, W = ctypes.byref(p), (ws.data_ptr(), ws.numel())
+    _abi.check_status(lib.attn_bwd_preprocess(P, o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                                              *W, s), "preprocess")
+    _abi.check_status(lib.attn_bwd_main(P, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                        do.data_ptr(), dk.data_ptr(), dv.data_ptr(), *W, s),
+                      "main")
+    _abi.check_status(lib.attn_bwd_dq(P, dq.data_ptr(), *W, s), "dq")
+    torch.cuda.synchronize()
+    ea.check(ws)
+    _, _, dQ, dK, dV = oracle.attention_backward(np64(inp["q"]), np64(inp["k"]), np64(inp["v"]),
+                                                 np64(inp["do"]), **oracle_kwargs(inp))
+    for got, want in ((dq, dQ), (dk, dK), (dv, dV)):
+        assert rel_l2(np64(got.cpu()), want) <= GRAD_REL_L2
 
 
 def test_repeatable(ea):
