@@ -269,7 +269,9 @@ __device__ __forceinline__ void bwd_unit_of(const MaskArgs& m, int K, int w, int
   piece = r2 % K;
 }
 
-template <int D, bool DROPOUT>
+// SPLIT: the key tiles are cut into pieces along their query tiles
+// (a.splits > 1); the unsplit kernel is compiled without the pieces' code.
+template <int D, bool DROPOUT, bool SPLIT>
 __global__ void __launch_bounds__(384, 1)
     bwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -296,7 +298,7 @@ __global__ void __launch_bounds__(384, 1)
   const MaskArgs& m = a.m;
   // persistent: CTA i starts with unit i (one key tile of one (b, key/value
   // head)); later units are claimed from the scheduler counter
-  const int K = a.splits;   // pieces per key tile
+  const int K = SPLIT ? a.splits : 1;   // pieces per key tile
   const int total = m.nb * m.B * m.H_kv * K;
 
   if (threadIdx.x == 0) {
@@ -746,7 +748,7 @@ __global__ void __launch_bounds__(384, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl.done, kw & 1, wc, kSiteBwdSoft));
       if (ok) tc_fence_after();
     }
-    if (ok && K > 1) {
+    if (ok && SPLIT) {
       // a piece of a split key tile: its dV and (unscaled) dK sums in fp32,
       // added up with the other pieces' afterwards
       const int64_t prow = (static_cast<int64_t>(u.piece) * m.B * m.H_kv + u.bhk) * a.part_rows + kj;
@@ -934,17 +936,17 @@ __global__ void __launch_bounds__(256) bwd_merge_kernel(const BwdArgs a) {
   *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dv) + dst) = vo;
 }
 
-template <int D, bool DROP>
+template <int D, bool DROP, bool SPLIT>
 cudaError_t launch_main(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s) {
   using C = BwdCfg<D>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_bf16_kernel<D, DROP>,
+    cudaError_t e = cudaFuncSetAttribute(bwd_bf16_kernel<D, DROP, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     // the register re-split inside the kernel assumes the launch allocation
     cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, bwd_bf16_kernel<D, DROP>)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, bwd_bf16_kernel<D, DROP, SPLIT>)) != cudaSuccess) return e;
     if (static_cast<uint32_t>(fa.numRegs) < C::kRegsLaunch) return cudaErrorInvalidConfiguration;
     attr_set = true;
   }
@@ -956,12 +958,17 @@ cudaError_t launch_main(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s) 
   if (e != cudaSuccess) return e;
   const long long units = static_cast<long long>(a.m.nb) * a.m.B * a.m.H_kv * a.splits;
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
-  e = launch_pdl(bwd_bf16_kernel<D, DROP>, dim3(grid), dim3(C::kThreads), C::kSmem, s, tm.q,
-                 tm.k, tm.v, tm.dout, tm.dq_acc, a);
-  if (e != cudaSuccess || a.splits <= 1) return e;
+  e = launch_pdl(bwd_bf16_kernel<D, DROP, SPLIT>, dim3(grid), dim3(C::kThreads), C::kSmem, s,
+                 tm.q, tm.k, tm.v, tm.dout, tm.dq_acc, a);
+  if (e != cudaSuccess || !SPLIT) return e;
   const int64_t threads = static_cast<int64_t>(a.m.B) * a.m.H_kv * a.m.N * (D / 8);
   return launch_pdl(bwd_merge_kernel<D>, dim3(static_cast<unsigned>((threads + 255) / 256)),
                     dim3(256), 0, s, a);
+}
+
+template <int D, bool DROP>
+cudaError_t launch_main(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s) {
+  return a.splits > 1 ? launch_main<D, DROP, true>(tm, a, s) : launch_main<D, DROP, false>(tm, a, s);
 }
 
 unsigned blocks_for(int64_t threads) {

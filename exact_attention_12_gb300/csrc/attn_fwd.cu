@@ -249,7 +249,9 @@ __device__ __forceinline__ void mma_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_
 
 // The forward of one CTA.  FP8: q, k are E4M3 [B,H,N,d] / [B,H_kv,N,d] maps
 // with 128 x 128-byte boxes and tv maps the transposed V^T [B,H_kv,d,N].
-template <int D, bool DROPOUT, bool FP8>
+// SPLIT: the pairs are cut into pieces along the keys (a.splits > 1); the
+// unsplit kernel is compiled without the pieces' code.
+template <int D, bool DROPOUT, bool FP8, bool SPLIT>
 __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMap& tk,
                                          const CUtensorMap& tv, const FwdArgs& a) {
   using C = FwdCfg<D, DROPOUT, FP8>;
@@ -266,7 +268,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
   const MaskArgs& m = a.m;
   const int BH = m.B * m.H;
   const int npairs = (m.nb + 1) / 2;
-  const int K = a.splits;   // pieces per pair
+  const int K = SPLIT ? a.splits : 1;   // pieces per pair
   const int total = npairs * BH * K;
   auto unit_of = [&](int w) {
     const int G = m.head_group, per = G * npairs * K, nfull = BH / G;
@@ -365,7 +367,8 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
         mbar_arrive(&ctl.unitfull[r]);   // release: the consumers' wait acquires unit[r]
         if (ui.w < 0) break;
         const FwdUnit u{ui.pair, ui.bh, ui.b, ui.h, ui.limit, ui.piece};
-        const TileList listA{ui.idx[0], ui.base[0], ui.n[0]}, listB{ui.idx[1], ui.base[1], ui.n[1]};
+        const TileList listA{ui.idx[0], SPLIT ? ui.base[0] : 0, ui.n[0]},
+            listB{ui.idx[1], SPLIT ? ui.base[1] : 0, ui.n[1]};
         if (listA.n == 0 && listB.n == 0) continue;
         // the previous unit's score MMAs are done with Q
         if (kw >= 1 && !(ok = mbar_wait(&ctl.qempty, (kw - 1) & 1, wc, kSiteFwdQ))) break;
@@ -438,7 +441,8 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
         const UnitInfo ui = ctl.unit[r];
         mbar_arrive(&ctl.unitempty[r]);
         if (ui.w < 0) break;
-        const TileList listA{ui.idx[0], ui.base[0], ui.n[0]}, listB{ui.idx[1], ui.base[1], ui.n[1]};
+        const TileList listA{ui.idx[0], SPLIT ? ui.base[0] : 0, ui.n[0]},
+            listB{ui.idx[1], SPLIT ? ui.base[1] : 0, ui.n[1]};
         if (listA.n == 0 && listB.n == 0) continue;
         if (!(ok = mbar_wait(&ctl.qfull, kw & 1, wc, kSiteFwdQ))) break;
         PairWalk walk{listA, listB};
@@ -589,7 +593,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.unitempty[r]);
       if (ui.w < 0) break;
-      const TileList tiles{x ? ui.idx[1] : ui.idx[0], x ? ui.base[1] : ui.base[0],
+      const TileList tiles{x ? ui.idx[1] : ui.idx[0], SPLIT ? (x ? ui.base[1] : ui.base[0]) : 0,
                            x ? ui.n[1] : ui.n[0]};
       const bool any = ui.n[0] > 0 || ui.n[1] > 0;
       const int bh = ui.bh, b = ui.b, h = ui.h, limit = ui.limit;
@@ -729,7 +733,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
         if (!ok) break;
         tc_fence_after();
       }
-      if (q0 < m.N && K > 1) {
+      if (SPLIT && q0 < m.N) {
         // a piece of a split pair: O normalised over the piece's keys (fp32)
         // and its logsumexp, merged with the other pieces' afterwards
         const bool live = l_sum > 0.f;
@@ -802,26 +806,26 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tq, const CUtensorMa
   }
 }
 
-template <int D, bool DROPOUT>
+template <int D, bool DROPOUT, bool SPLIT>
 __global__ void __launch_bounds__(FwdCfg<D, DROPOUT>::kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
-  fwd_body<D, DROPOUT, false>(tq, tk, tv, a);
+  fwd_body<D, DROPOUT, false, SPLIT>(tq, tk, tv, a);
 }
 
-template <int D>
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(FwdCfg<D, false, true>::kThreads, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tvt, const FwdArgs a) {
-  fwd_body<D, false, true>(tq, tk, tvt, a);
+  fwd_body<D, false, true, SPLIT>(tq, tk, tvt, a);
 }
 
-template <int D, bool DROP, bool FP8>
-cudaError_t launch_one(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
+template <int D, bool DROP, bool FP8, bool SPLIT>
+cudaError_t launch_split(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
   using C = FwdCfg<D, DROP, FP8>;
   auto kernel = [] {
-    if constexpr (FP8) return fwd_fp8_kernel<D>;
-    else return fwd_bf16_kernel<D, DROP>;
+    if constexpr (FP8) return fwd_fp8_kernel<D, SPLIT>;
+    else return fwd_bf16_kernel<D, DROP, SPLIT>;
   }();
   static bool attr_set = false;
   if (!attr_set) {
@@ -842,6 +846,12 @@ cudaError_t launch_one(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
   const long long units = static_cast<long long>((a.m.nb + 1) / 2) * a.m.B * a.m.H * a.splits;
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
   return launch_pdl(kernel, dim3(grid), dim3(C::kThreads), C::kSmem, s, tm.q, tm.k, tm.v, a);
+}
+
+template <int D, bool DROP, bool FP8>
+cudaError_t launch_one(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s) {
+  return a.splits > 1 ? launch_split<D, DROP, FP8, true>(tm, a, s)
+                      : launch_split<D, DROP, FP8, false>(tm, a, s);
 }
 
 // The pieces of split query-tile pairs merged by the incremental-softmax
