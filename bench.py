@@ -106,6 +106,16 @@ def stage_bytes(w):
     return fwd, pre, main, dq
 
 
+def nvtx(name):
+    """An NVTX range around a phase of the bench, named in nsys and ncu
+    timelines (--nvtx); without a profiler attached it costs a host call."""
+    import contextlib
+    try:
+        return torch.cuda.nvtx.range(f"bench: {name}")
+    except (AttributeError, RuntimeError):
+        return contextlib.nullcontext()
+
+
 def kernel_source_hash(kernel):
     """First 16 hex digits of the SHA-256 of the kernel's source files."""
     import hashlib
@@ -349,12 +359,14 @@ def measure_device(ea, w, dev, steps, warmup, dist=None):
     nsets = max(1, min(8, math.ceil(2 * L2_BYTES / max(1, first.bytes_resident()))))
     sets = [first] + [Step(ea, inp, dev) for _ in range(nsets - 1)]
     stream = torch.cuda.current_stream(dev)
-    for i in range(warmup):
-        sets[i % nsets].run(stream)
-    torch.cuda.synchronize(dev)
-    graphs = StepGraphs(lambda k, s: sets[k].run(s), nsets, dev)
-    graphs.replay(nsets)
-    torch.cuda.synchronize(dev)
+    with nvtx(f"{w.name} warm-up"):
+        for i in range(warmup):
+            sets[i % nsets].run(stream)
+        torch.cuda.synchronize(dev)
+    with nvtx(f"{w.name} graph capture"):
+        graphs = StepGraphs(lambda k, s: sets[k].run(s), nsets, dev)
+        graphs.replay(nsets)
+        torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.__enter__()
     time.sleep(0.2)       # let the sampler start before the loaded window
@@ -362,9 +374,10 @@ def measure_device(ea, w, dev, steps, warmup, dist=None):
     # launch (the events cost ~10 us per step, so the step itself is timed
     # below without them)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
-    for i in range(steps):
-        sets[i % nsets].run(stream, evs[i])
-    torch.cuda.synchronize(dev)
+    with nvtx(f"{w.name} per-kernel event pass"):
+        for i in range(steps):
+            sets[i % nsets].run(stream, evs[i])
+        torch.cuda.synchronize(dev)
     stage = [sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
              for j in range(4)]
     # the step: replayed from CUDA graphs (the host launch cost of four ctypes
@@ -373,10 +386,11 @@ def measure_device(ea, w, dev, steps, warmup, dist=None):
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.monotonic()
-    start.record(stream)
-    graphs.replay(steps)
-    end.record(stream)
-    torch.cuda.synchronize(dev)
+    with nvtx(f"{w.name} timed steps"):
+        start.record(stream)
+        graphs.replay(steps)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
     t1 = time.monotonic()
     _barrier(dist)
     time.sleep(0.06)
@@ -504,14 +518,16 @@ def measure_e2e(ea, w, dev, steps, warmup):
                 dst.copy_(src, non_blocking=True)
             ev_out[b].record(down)
 
-    for k in range(warmup):
-        step(k)
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    for k in range(steps):
-        step(k)
-    torch.cuda.synchronize(dev)
-    dt = (time.perf_counter() - t0) / steps
+    with nvtx(f"{w.name} e2e warm-up"):
+        for k in range(warmup):
+            step(k)
+        torch.cuda.synchronize(dev)
+    with nvtx(f"{w.name} e2e timed steps"):
+        t0 = time.perf_counter()
+        for k in range(steps):
+            step(k)
+        torch.cuda.synchronize(dev)
+        dt = (time.perf_counter() - t0) / steps
     flops = 3.5 * fwd_flops(w, inp["key_lens"], inp["block_mask"])
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     d2h = sum(t.numel() * t.element_size() for t in host_out[0])

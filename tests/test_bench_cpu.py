@@ -158,3 +158,11 @@ def test_workload_overrides_parse_into_fields():
         bench.parse_overrides(["heads=2"])
     w = workloads.get("long-causal-16384", **bench.parse_overrides(["H=2"]))
     assert (w.H, w.N, w.d, w.causal) == (2, 16384, 128, True)
+
+
+def test_nvtx_ranges_need_no_profiler():
+    # the bench's phases sit in NVTX ranges; entering one must work on a host
+    # without a GPU or a profiler attached
+    with bench.nvtx("phase"):
+        with bench.nvtx("nested"):
+            pass
