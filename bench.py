@@ -799,17 +799,33 @@ FP8_METRIC = "attention fwd TFLOPS (E4M3 Q, K, V; bf16 O) & % of GB300 dense FP8
 FP8_NOMINAL_RATIO = 2.0   # dense FP8 / dense BF16 tensor throughput (4.5 / 2.25 PFLOP/s)
 
 
+FP32_METRIC = "attention fwd TFLOPS (fp32 Q, K, V, O; tcgen05 kind::tf32) & % of GB300 TF32 peak"
+TF32_NOMINAL_RATIO = 1.1 / 2.25   # dense TF32 / dense BF16 tensor throughput (PFLOP/s)
+
+
 def _fp8_kw(inp):
     return dict(scale=inp["scale"], causal=inp["causal"], q_descale=inp["q_descale"],
                 k_descale=inp["k_descale"], v_descale=inp["v_descale"])
 
 
-def measure_fp8(ea, w, dev, steps, warmup):
-    """Device-timed forward steps (V transpose + fused forward, one attn_fwd
-    call) over input sets that rotate so each step misses the L2, then the
-    e2e leg: Q, K, V up from pinned host memory and O down, every step."""
+def _fwd_kw(w, inp, dev):
+    """attention_fwd keywords of a forward-only workload (FP8 or fp32)."""
+    if w.dtype == "fp8":
+        return _fp8_kw(inp)
+    kl, bm = inp["key_lens"], inp["block_mask"]
+    return dict(scale=inp["scale"], causal=inp["causal"], dropout_p=inp["dropout_p"],
+                seed=inp["seed"], offset=inp["offset"],
+                key_lens=None if kl is None else kl.to(dev),
+                block_mask=None if bm is None else bm.to(dev))
+
+
+def measure_fwd(ea, w, dev, steps, warmup):
+    """Device-timed forward steps (one attn_fwd call: for FP8 the V transpose
+    + fused forward, for fp32 the operand split + TF32 forward) over input
+    sets that rotate so each step misses the L2, then the e2e leg: Q, K, V up
+    from pinned host memory and O down, every step."""
     inp = workloads.make_inputs(w)
-    kw = _fp8_kw(inp)
+    kw = _fwd_kw(w, inp, dev)
 
     def make_set():
         q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
@@ -870,59 +886,81 @@ def measure_fp8(ea, w, dev, steps, warmup):
                 d2h=ho.numel() * ho.element_size())
 
 
-def run_fp8(args, w):
-    """The FP8 forward: fwd TFLOPS against the FP8 tensor peak (the measured
-    BF16 peak times the nominal FP8/BF16 ratio), oracle timed beside it."""
-    import numpy as np
-    from oracle import fp8 as oracle_fp8
-    inp_cpu = workloads.make_inputs(w)
-    ds = (inp_cpu["q_descale"], inp_cpu["k_descale"], inp_cpu["v_descale"])
-    t0 = time.perf_counter()
-    done, flops_cpu = 0, 0.0
+def fwd_only_oracle_sample(w, budget_s):
+    """Time the oracle's forward of a forward-only workload head by head (the
+    FP8 oracle for E4M3 inputs, the fp64 forward otherwise) until `budget_s`
+    has passed (at least one head).  Returns (flops, seconds, heads done)."""
+    fp8 = w.dtype == "fp8"
+    inp = workloads.make_inputs(w)
     grp = w.H // w.kv_heads
-    for h in range(w.H):
-        codes = [inp_cpu[n][:, sl].view(torch.uint8).numpy() for n, sl in
-                 (("q", slice(h, h + 1)), ("k", slice(h // grp, h // grp + 1)),
-                  ("v", slice(h // grp, h // grp + 1)))]
-        oracle_fp8.fp8_forward(*codes, *ds, inp_cpu["scale"], causal=w.causal)
-        flops_cpu += fwd_flops(workloads.get(w.name, H=1, H_kv=1))
+    per_head = fwd_flops(workloads.get(w.name, B=1, H=1, H_kv=1))
+    if fp8:
+        from oracle import fp8 as oracle_fp8
+        ds = (inp["q_descale"], inp["k_descale"], inp["v_descale"])
+    else:
+        import numpy as np
+        from oracle import attention as oracle
+        arr = {n: inp[n].float().numpy() for n in ("q", "k", "v")}
+        okw = dict(scale=inp["scale"], causal=inp["causal"], dropout_p=inp["dropout_p"],
+                   seed=inp["seed"], offset=inp["offset"])
+    t0 = time.perf_counter()
+    done, flops = 0, 0.0
+    for b, h in ((b, h) for b in range(w.B) for h in range(w.H)):
+        if fp8:
+            codes = [inp[n][b:b + 1, sl].view(torch.uint8).numpy() for n, sl in
+                     (("q", slice(h, h + 1)), ("k", slice(h // grp, h // grp + 1)),
+                      ("v", slice(h // grp, h // grp + 1)))]
+            oracle_fp8.fp8_forward(*codes, *ds, inp["scale"], causal=w.causal)
+        else:
+            oracle.forward_rows(arr["q"], arr["k"], arr["v"], b, h, np.arange(w.N), **okw)
+        flops += per_head
         done += 1
-        if time.perf_counter() - t0 > args.cpu_budget:
+        if time.perf_counter() - t0 > budget_s:
             break
-    dt_cpu = time.perf_counter() - t0
-    del inp_cpu
+    return flops, time.perf_counter() - t0, done
+
+
+def run_fwd_only(args, w):
+    """A forward-only workload (FP8, or fp32 on the TF32 tensor path): fwd
+    TFLOPS against that type's tensor peak (the measured BF16 peak times the
+    nominal FP8/BF16 or TF32/BF16 ratio), the oracle timed beside it."""
+    fp8 = w.dtype == "fp8"
+    flops_cpu, dt_cpu, done = fwd_only_oracle_sample(w, args.cpu_budget)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     import exact_attention_12_gb300 as ea
     from exact_attention_12_gb300 import build
     build.build()
-    r = measure_fp8(ea, w, dev, args.steps, args.warmup)
+    r = measure_fwd(ea, w, dev, args.steps, args.warmup)
     flops = fwd_flops(w)
     burst, _, _, src = peaks()
-    peak = FP8_NOMINAL_RATIO * burst
+    ratio = FP8_NOMINAL_RATIO if fp8 else TF32_NOMINAL_RATIO
+    peak = ratio * burst
     tflops = flops / (r["ms"] * 1e-3) / 1e12
     line = {
-        "metric": FP8_METRIC, "value": tflops, "unit": "TFLOPS", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
-        "data": "synthetic",
+        "metric": FP8_METRIC if fp8 else FP32_METRIC, "value": tflops, "unit": "TFLOPS",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if fp8 else "f32", "data": "synthetic",
         "config": {"workload": describe(w), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                    "causal": w.causal, "parallelism": "single GPU",
                    "l2": f"inputs rotate over {r['nsets']} resident sets of "
                          f"{r['resident'] / 2**20:.0f} MiB (> 2x the 129 MB L2)",
                    "timing": "attn_fwd calls captured in CUDA graphs, replayed; CUDA events"},
-        "roofline": {"kernel": "fwd_fp8_kernel", "bound": "tensor", "achieved": tflops,
-                     "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
-                     "peak_source": f"bf16_tflops ({src}) x {FP8_NOMINAL_RATIO} "
-                                    f"(nominal dense FP8 / BF16)",
-                     "timed": "the attn_fwd call: V transpose + fused forward",
+        "roofline": {"kernel": "fwd_fp8_kernel" if fp8 else "fwd_tf32_kernel", "bound": "tensor",
+                     "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                     "peak_source": f"bf16_tflops ({src}) x {ratio:.4g} "
+                                    f"(nominal dense {'FP8' if fp8 else 'TF32'} / BF16)",
+                     "timed": "the attn_fwd call: V transpose + fused forward" if fp8 else
+                              "the attn_fwd call: operand split + TF32 forward (the scores "
+                              "take three TF32 passes: the tensor work is 2x the counted FLOPs)",
                      "traffic": None},
         "gpu_launches": 2 * args.steps,
         "clocks": r["clocks"],
         "cpu_baseline": {"value": flops_cpu / dt_cpu / 1e12, "unit": "TFLOPS",
                          "cores": _blas_threads(), "kind": "oracle",
-                         "sample": f"{done} of {w.H} heads of {w.name}, fp64 numpy forward, "
-                                   f"{dt_cpu:.1f} s"},
+                         "sample": f"{done} of {w.B * w.H} heads of {w.name}, fp64 numpy "
+                                   f"forward, {dt_cpu:.1f} s"},
         "e2e": {"value": flops / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOPS",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "ms_per_step": r["e2e_ms"]},
@@ -951,11 +989,11 @@ def profile_steps(w, n):
         ea.check()
         print(f"profile-steps: {n} steps of {w.name} done")
         return
-    if w.dtype == "fp8":   # forward only: V transpose + fused forward per step
+    if w.fwd_only:   # forward only: one attn_fwd call per step
         inp = workloads.make_inputs(w)
         q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
         for _ in range(n):
-            ea.attention_fwd(q, k, v, **_fp8_kw(inp))
+            ea.attention_fwd(q, k, v, **_fwd_kw(w, inp, dev))
         torch.cuda.synchronize(dev)
         ea.check()
         print(f"profile-steps: {n} steps of {w.name} done")
@@ -1008,12 +1046,12 @@ def main():
     if args.profile_steps > 0:
         profile_steps(w, args.profile_steps)
         return
-    if w.dtype == "fp8":
+    if w.fwd_only and not w.decode_n_q:
         if args.impl == "reference":
             print(json.dumps({"impl": "reference",
                               "unavailable": "the reference arm times the bf16 training step"}))
         elif int(os.environ.get("RANK", "0")) == 0:
-            run_fp8(args, w)
+            run_fwd_only(args, w)
         return
     if w.decode_n_q:
         if args.impl == "reference":

@@ -244,6 +244,9 @@ def test_forward_splits_pairs_only_for_few_long_heads(abi):
 
     assert ws(B=1, H=16, N=16384, d=128) == 256
     assert ws(B=2, H=3, N=1000) == 256
+    # 128 pairs of 16 key tiles: more than half of any GPU's SMs, rows too
+    # short to be worth the merge
+    assert ws(B=1, H=16, N=2048, d=128) == 256
     nb, pieces = 32, 4
     rows = pieces * 1 * 1 * (nb // 2) * 256
     assert ws(B=1, H=1, N=4096, d=128) == 256 + rows * 128 * 4 + rows * 4

@@ -166,3 +166,13 @@ def test_nvtx_ranges_need_no_profiler():
     with bench.nvtx("phase"):
         with bench.nvtx("nested"):
             pass
+
+
+@pytest.mark.parametrize("name", ["single-head-fp32", "fp8-long-causal-512"])
+def test_forward_only_oracle_sample(name):
+    # forward-only workloads are timed on the oracle head by head; at least
+    # one head runs, and the FLOPs are whole heads' worth
+    w = workloads.get(name)
+    flops, dt, done = bench.fwd_only_oracle_sample(w, 0.0)
+    assert done == 1 and dt > 0
+    assert flops == bench.fwd_flops(workloads.get(name, B=1, H=1, H_kv=1))
