@@ -91,9 +91,12 @@ typedef struct attn_params {
   int32_t B, H, N, d;        /* batch, heads, sequence length, head dim.
                                 d in {64, 128}.  B, H or N = 0: no work. */
   int32_t dtype;             /* attn_dtype.  bf16: forward and backward;
-                                fp32: forward only; fp8 (E4M3 q, k, v with
-                                the de-scale factors below, bf16 o):
-                                forward only, d = 128, no dropout. */
+                                fp32: forward only, on the tensor cores in
+                                TF32 (the scores as three TF32 products of
+                                the operands' high and low parts, P V as
+                                one), fp32 o; fp8 (E4M3 q, k, v with the
+                                de-scale factors below, bf16 o): forward
+                                only, d = 128, no dropout. */
   float scale;               /* score scale, e.g. 1/sqrt(d); finite */
   int32_t causal;            /* nonzero: keep j <= i (top-left aligned) */
   float dropout_p;           /* drop probability in [0, 1); 0 = no dropout */
@@ -146,7 +149,9 @@ size_t attn_workspace_size(const attn_params* p, int for_backward);
 
 /* Forward: O [B,H,N,d] (same dtype as q; bf16 for fp8 inputs) and lse
  * [B,H,N] fp32.  For fp8 the workspace also holds a transposed copy of v
- * ([B, H_kv, d, N] padded to a multiple of 128 keys), written by the call. */
+ * ([B, H_kv, d, N] padded to a multiple of 128 keys), written by the call;
+ * for fp32 it holds the high and low TF32 parts of q and k and a transposed
+ * copy of v, written by the call. */
 attn_status attn_fwd(const attn_params* p, const void* q, const void* k,
                      const void* v, void* o, float* lse, void* ws,
                      size_t ws_bytes, void* stream);
