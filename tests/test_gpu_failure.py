@@ -48,8 +48,10 @@ def _site(lib):
     return int(msg.rsplit("wait site", 1)[1].split()[0])
 
 
-@pytest.mark.parametrize("which,d", [("fwd", 64), ("fwd", 128), ("bwd", 64), ("bwd", 128)])
-def test_attention_kernel_timeout_path(ea, which, d):
+@pytest.mark.parametrize("which,d,split", [("fwd", 64, False), ("fwd", 128, False),
+                                           ("bwd", 64, False), ("bwd", 128, False),
+                                           ("fwd", 128, True), ("bwd", 128, True)])
+def test_attention_kernel_timeout_path(ea, which, d, split):
     """A real attention kernel's bounded waits running out.
 
     attn_debug_stall arms a one-shot stall for the next launch: in every CTA
@@ -57,13 +59,16 @@ def test_attention_kernel_timeout_path(ea, which, d):
     it gives up after the armed 20 ms.  The CTA then drains its copies and
     MMAs, frees its tensor memory and returns; the call's workspace records
     ATTN_ERR_TIMEOUT with a wait site of that kernel, attn_check reports and
-    clears it, and the next calls on the same context match the oracle."""
+    clears it, and the next calls on the same context match the oracle.
+    `split`: one head of 4096 keys, which the forward cuts into pieces along
+    the keys and the backward along its key tiles' query tiles (the kernels
+    with the pieces' code, followed by their merge kernels)."""
     import numpy as np
     from exact_attention_12_gb300 import _abi
     from oracle import attention as oracle
     from tests.helpers import GRAD_REL_L2, assert_o, max_abs, np64, rel_l2, L_MAX_ABS
     lib = _abi.lib()
-    B, H, N = 2, 3, 700
+    B, H, N = (1, 1, 4096) if split else (2, 3, 700)
     qc, kc, vc, doc = workloads.random_case(B, H, N, d, seed=40 + d)
     q, k, v, do = (t.cuda() for t in (qc, kc, vc, doc))
     kw = dict(scale=d ** -0.5, causal=True)
