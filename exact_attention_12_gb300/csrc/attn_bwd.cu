@@ -24,7 +24,11 @@
 //                                             as an MN-major operand)
 //                    dK and dV stay in TMEM for the whole loop; each dQ_i is
 //                    staged through shared memory and added into the fp32
-//                    accumulator with TMA bulk reduce-adds.
+//                    accumulator with TMA bulk reduce-adds.  With fewer key
+//                    tiles than SMs (few, long heads) a key tile's walk is
+//                    cut into pieces, units of their own, each leaving fp32
+//                    dK, dV partials (the kernel's SPLIT instances).
+//   bwd_merge        the pieces' dK, dV added up -> bf16 (split key tiles only).
 //   dq_convert       dQ = c * accumulator -> bf16.
 //
 // Warp roles of bwd_kernel (384 threads; registers re-split with setmaxnreg):

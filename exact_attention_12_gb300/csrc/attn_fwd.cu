@@ -34,6 +34,11 @@
 //                MMA.
 //   * warps 10-11 idle (they complete the third warpgroup, whose registers
 //                go to the softmax warps).
+//   * With few, long heads (fewer pairs than SMs) each pair's key tiles are
+//     cut into pieces, units of their own; a piece leaves O normalised over
+//     its keys (fp32) and its L in the workspace, and fwd_merge_kernel
+//     combines the pieces.  That code is compiled only into the kernel's
+//     SPLIT instances.
 //   Because every tcgen05.commit covers all earlier MMAs of the issuing
 //   thread, "S_X(t+1) is complete" already implies "O_X += P_X V_t is
 //   complete": the softmax may then overwrite P_X and rescale O_X.
