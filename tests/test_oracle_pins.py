@@ -236,6 +236,34 @@ def test_blockwise_recurrence_matches_direct_statistics():
                 np.testing.assert_allclose(Ob, O, atol=1e-12)
 
 
+@pytest.mark.parametrize("causal,p", [(False, 0.0), (True, 0.0), (True, 0.3)])
+def test_key_pieces_merge_to_the_full_attention(causal, p):
+    # the merge rule the split forward and decode step use (a reading of the
+    # pages' running statistics): pieces of a row's keys, each with O_s
+    # normalised over its keys and L_s its logsumexp, combine as
+    # L = log sum_s e^{L_s} and O = sum_s e^{L_s - L} O_s, in any order.
+    # Each piece here is one 128-key block column, selected by a block mask
+    # in the oracle; the merge must give the unsplit attention.
+    B, H, N, d = 1, 2, 300, 8
+    rng = np.random.default_rng(7)
+    q, k, v = (rng.standard_normal((B, H, N, d)) for _ in range(3))
+    kw = dict(scale=0.4, causal=causal, dropout_p=p, seed=11, offset=3)
+    O, L = A.attention_forward(q, k, v, **kw)
+    nb = (N + 127) // 128
+    parts = []
+    for s in (2, 0, 1):                       # an arbitrary order
+        bm = np.zeros((nb, nb), dtype=np.uint8)
+        bm[:, s] = 1
+        parts.append(A.attention_forward(q, k, v, block_mask=bm, **kw))
+    Ls = np.stack([Lp for _, Lp in parts])                  # [pieces, B, H, N]
+    Lm = np.logaddexp.reduce(Ls, axis=0)
+    with np.errstate(invalid="ignore"):
+        w = np.where(np.isneginf(Ls), 0.0, np.exp(Ls - Lm))
+    Om = sum(w[i][..., None] * parts[i][0] for i in range(len(parts)))
+    np.testing.assert_allclose(Lm, L, atol=1e-12)
+    np.testing.assert_allclose(Om, O, atol=1e-12)
+
+
 def test_fully_masked_row_is_zero():
     N, d = 6, 4
     q, k, v, do = (_rand((N, d), s) for s in (50, 51, 52, 53))
