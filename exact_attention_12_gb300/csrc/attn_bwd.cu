@@ -943,22 +943,24 @@ __global__ void __launch_bounds__(256) bwd_merge_kernel(const BwdArgs a) {
 template <int D, bool DROP, bool SPLIT>
 cudaError_t launch_main(const TensorMaps& tm, const BwdArgs& a, cudaStream_t s) {
   using C = BwdCfg<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_bf16_kernel<D, DROP, SPLIT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  static std::atomic<uint64_t> set_up{0};
+  int dev = 0, sms = 0;
+  bool todo = false;
+  cudaError_t e = needs_setup(set_up, &dev, &todo);
+  if (e != cudaSuccess) return e;
+  if (todo) {
+    e = cudaFuncSetAttribute(bwd_bf16_kernel<D, DROP, SPLIT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     // the register re-split inside the kernel assumes the launch allocation
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, bwd_bf16_kernel<D, DROP, SPLIT>)) != cudaSuccess) return e;
     if (static_cast<uint32_t>(fa.numRegs) < C::kRegsLaunch) return cudaErrorInvalidConfiguration;
-    attr_set = true;
+    mark_done(set_up, dev);
   }
   // persistent: at most one CTA per SM, each claiming units (one key tile of
   // one (b, key/value head)) until none are left
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const long long units = static_cast<long long>(a.m.nb) * a.m.B * a.m.H_kv * a.splits;
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);

@@ -832,21 +832,22 @@ cudaError_t launch_split(const TensorMaps& tm, const FwdArgs& a, cudaStream_t s)
     if constexpr (FP8) return fwd_fp8_kernel<D, SPLIT>;
     else return fwd_bf16_kernel<D, DROP, SPLIT>;
   }();
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmem);
+  static std::atomic<uint64_t> set_up{0};
+  int dev = 0, sms = 0;
+  bool todo = false;
+  cudaError_t e = needs_setup(set_up, &dev, &todo);
+  if (e != cudaSuccess) return e;
+  if (todo) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     // the register re-split inside the kernel assumes the launch allocation
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, kernel)) != cudaSuccess) return e;
     if (static_cast<uint32_t>(fa.numRegs) < C::kRegsLaunch) return cudaErrorInvalidConfiguration;
-    attr_set = true;
+    mark_done(set_up, dev);
   }
   // persistent: at most one CTA per SM, each walking its share of the units
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const long long units = static_cast<long long>((a.m.nb + 1) / 2) * a.m.B * a.m.H * a.splits;
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);

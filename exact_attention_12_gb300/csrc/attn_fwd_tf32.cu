@@ -380,12 +380,16 @@ __global__ void __launch_bounds__(256) tf32_split_kernel(const float* __restrict
 template <int D, bool DROP>
 cudaError_t launch_tf32(const Tf32Maps& tm, const FwdArgs& a, cudaStream_t s) {
   using C = Tf32Cfg<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(fwd_tf32_kernel<D, DROP>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  static std::atomic<uint64_t> set_up{0};
+  int dev = 0;
+  bool todo = false;
+  cudaError_t e = needs_setup(set_up, &dev, &todo);
+  if (e != cudaSuccess) return e;
+  if (todo) {
+    e = cudaFuncSetAttribute(fwd_tf32_kernel<D, DROP>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    mark_done(set_up, dev);
   }
   const dim3 grid(static_cast<unsigned>(a.m.nb), static_cast<unsigned>(a.m.B * a.m.H));
   fwd_tf32_kernel<D, DROP><<<grid, C::kThreads, C::kSmem, s>>>(tm.qhi, tm.qlo, tm.khi, tm.klo,

@@ -7,6 +7,7 @@
 
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <utility>
 
 #include "philox.cuh"
@@ -33,6 +34,22 @@ inline cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
+
+// One-time set-up of a kernel instance (its shared-memory limit, the
+// register check) is per device: `done` remembers the devices it has run on
+// (up to 64; beyond that it runs on every call).  Returns the current device
+// in *dev and whether the set-up is still to do there; mark_done records it.
+inline cudaError_t needs_setup(const std::atomic<uint64_t>& done, int* dev, bool* todo) {
+  const cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (*dev >= 0 && *dev < 64) ? (uint64_t{1} << *dev) : 0;
+  *todo = bit == 0 || (done.load(std::memory_order_acquire) & bit) == 0;
+  return cudaSuccess;
+}
+
+inline void mark_done(std::atomic<uint64_t>& done, int dev) {
+  if (dev >= 0 && dev < 64) done.fetch_or(uint64_t{1} << dev, std::memory_order_release);
 }
 
 constexpr int kTile = 128;            // query/key tile rows == block-mask granularity
