@@ -468,6 +468,30 @@ def workload_result(w, r, world=1):
     return out
 
 
+def headline_line(w, r, steps, warmup, world):
+    """The JSON line of the training-step bench from a measure_device result
+    (the cpu_baseline, e2e and secondary entries are added by the caller)."""
+    res = workload_result(w, r, world)
+    line = {
+        "metric": METRIC, "value": res.pop("value"), "unit": "TFLOPS", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": res.pop("ms_per_step"),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": describe(w), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "dropout_p": w.dropout_p,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs rotate over {r['nsets']} resident sets of "
+                         f"{r['resident_bytes'] / 2**20:.0f} MiB (> 2x the 129 MB L2)",
+                   "timing": "steps captured in CUDA graphs and replayed, CUDA events around "
+                             "the K steps; stage_ms and the roofline kernel time from a "
+                             "separate pass of K steps launched one by one with an event "
+                             "around each launch"},
+        "gpu_launches": r["launches"],
+    }
+    line.update(res)
+    return line
+
+
 def measure_e2e(ea, w, dev, steps, warmup):
     """Same metric through the Python API with host (pinned) inputs and outputs.
 
@@ -1099,24 +1123,7 @@ def main():
         dist.barrier()
 
     r = measure_device(ea, w, dev, args.steps, args.warmup, dist)
-    res = workload_result(w, r, world)
-    line = {
-        "metric": METRIC, "value": res.pop("value"), "unit": "TFLOPS", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": res.pop("ms_per_step"),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": describe(w), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                   "causal": w.causal, "dropout_p": w.dropout_p,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"inputs rotate over {r['nsets']} resident sets of "
-                         f"{r['resident_bytes'] / 2**20:.0f} MiB (> 2x the 129 MB L2)",
-                   "timing": "steps captured in CUDA graphs and replayed, CUDA events around "
-                             "the K steps; stage_ms and the roofline kernel time from a "
-                             "separate pass of K steps launched one by one with an event "
-                             "around each launch"},
-        "gpu_launches": r["launches"],
-    }
-    line.update(res)
+    line = headline_line(w, r, args.steps, args.warmup, world)
     if cpu is not None:
         line["cpu_baseline"] = cpu
     line["e2e"] = measure_e2e(ea, w, dev, max(3, min(args.steps, 100)), 3)

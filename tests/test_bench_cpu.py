@@ -176,3 +176,26 @@ def test_forward_only_oracle_sample(name):
     flops, dt, done = bench.fwd_only_oracle_sample(w, 0.0)
     assert done == 1 and dt > 0
     assert flops == bench.fwd_flops(workloads.get(name, B=1, H=1, H_kv=1))
+
+
+def test_headline_line_carries_the_contract_keys():
+    # the training-step line from a measurement (made up here): every key the
+    # bench contract names, the roofline of the dominant stage with a traffic
+    # figure read from profiles/ when it is current, and value = the whole
+    # step's FLOPs over its time
+    w = workloads.get("long-causal-16384")
+    ff = bench.fwd_flops(w)
+    r = dict(ms_per_step=3.0, stage_ms=[0.75, 0.04, 2.2, 0.03], fwd_flops=ff, bwd_flops=2.5 * ff,
+             nsets=1, resident_bytes=643 << 20, launches=800,
+             clocks={"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []})
+    line = bench.headline_line(w, r, steps=200, warmup=20, world=1)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "gpu_launches", "roofline", "clocks"):
+        assert key in line, key
+    assert line["value"] == pytest.approx(3.5 * ff / 3.0e-3 / 1e12)
+    assert line["config"]["workload"].startswith("long-causal-16384")
+    roof = line["roofline"]
+    assert roof["kernel"] == "bwd_bf16_kernel" and roof["bound"] == "tensor"
+    assert roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"])
+    assert set(roof) >= {"bound", "achieved", "peak", "unit", "frac", "traffic"}
