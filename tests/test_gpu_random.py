@@ -7,8 +7,9 @@ The draws are fixed by the seed: a failing case keeps its id from run to run.
 Value std runs to 2 and dropout to 0.5, beyond the workloads' regime (std up
 to 1, dropout 0.1) for which the O bar of 1e-2 is stated; there the bar widens
 in proportion to |V| and 1 / (1 - p) (tests.helpers.o_magnitude_factor), the
-only two things the kernel's O error scales with.  L, dQ, dK and dV keep
-their bars unchanged.
+only two things the kernel's O error scales with.  L and dV keep their bars;
+dQ and dK add what forming D from the forward's bf16 O contributes (see
+d_rounding_terms), which only matters where they cancel to nearly nothing.
 """
 
 import numpy as np
@@ -88,6 +89,37 @@ def _to_dev(t, bnhd):
     return t.transpose(1, 2).contiguous().cuda().transpose(1, 2)
 
 
+def d_rounding_terms(q, k, do, O, o_gpu, c, kl):
+    """Norms of what the forward's O error carries into dQ and dK: the
+    backward forms D = rowsum(dO * O) from the O it is given (the forward's
+    bf16 output), so with e_i = rowsum(dO * (O_gpu - O)) the error of D_i,
+    dS_ij changes by -P_ij e_i (P the softmax probabilities before dropout),
+    dQ_i by -c e_i sum_j P_ij K_j and dK_j by -c sum_i P_ij e_i Q_i (summed
+    over a key/value head's query heads)."""
+    qn, kn, don = np64(q), np64(k), np64(do)
+    e = (don * (o_gpu - O)).sum(-1)                            # [B, H, N]
+    B, H, N, _ = qn.shape
+    grp = H // c["H_kv"]
+    eq = np.zeros_like(qn)
+    ek = np.zeros_like(kn)
+    bm = c["block_mask"]
+    for b in range(B):
+        for h in range(H):
+            hk = h // grp
+            head_bm = None if bm is None else (bm[b, h] if bm.ndim == 4 else bm)
+            allowed = oracle.allowed_mask(np.arange(N), np.arange(N), c["causal"],
+                                          None if kl is None else int(kl[b]), head_bm)
+            S = np.where(allowed, c["scale"] * qn[b, h] @ kn[b, hk].T, -np.inf)
+            m = S.max(axis=1, keepdims=True)
+            P = np.where(allowed, np.exp(S - np.where(np.isfinite(m), m, 0.0)), 0.0)
+            s = P.sum(axis=1, keepdims=True)
+            P = np.divide(P, s, out=np.zeros_like(P), where=s > 0)
+            Pe = P * e[b, h][:, None]
+            eq[b, h] = c["scale"] * Pe @ kn[b, hk]
+            ek[b, hk] += c["scale"] * Pe.T @ qn[b, h]
+    return float(np.linalg.norm(eq)), float(np.linalg.norm(ek))
+
+
 @pytest.mark.parametrize("i", range(N_SHORT + N_LONG), ids=_case_id)
 def test_random_configuration(ea, i):
     c = _draw(i)
@@ -115,18 +147,21 @@ def test_random_configuration(ea, i):
     assert_o(np64(o.cpu()), O, what=_case_id(i),
              factor=o_magnitude_factor(c["std"], c["dropout_p"]))
     assert max_abs(lse.cpu().numpy(), L) <= L_MAX_ABS
-    # rel-L2 as everywhere, plus a floor of 1e-4 per element (x std^2) for
-    # gradients that cancel to (nearly) nothing: with one key per row, say,
-    # dS = P (dP - D) is exactly 0, but the kernel's dP (tensor cores) and D
-    # (row sums of dO * O) add the same products in different orders, and
-    # ~1e-6 of rounding is left in dQ and dK
+    # rel-L2 as everywhere, plus what D adds where dQ and dK cancel to
+    # (nearly) nothing (one or two keys per row, say, where dS = P (dP - D)
+    # is exactly 0): D = rowsum(dO * O) is formed from the forward's bf16 O,
+    # so O's error (within the forward's bar) reaches dS and, through it, dQ
+    # and dK (d_rounding_terms: that term, exactly, from the oracle's values
+    # and the forward's O), and a floor of 1e-4 per element (x std^2) for dP
+    # and D adding the same products in different orders
+    eq, ek = d_rounding_terms(q, k, do, O, np64(o.cpu()), c, kl)
     floor = 1e-4 * max(1.0, c["std"] ** 2)
-    for name, got, want in (("dQ", dq, dQ), ("dK", dk, dK), ("dV", dv, dV)):
+    for name, got, want, extra in (("dQ", dq, dQ, eq), ("dK", dk, dK, ek), ("dV", dv, dV, 0.0)):
         g = np64(got.cpu())
         assert not np.isnan(g).any(), name
         err = np.linalg.norm(g - want)
-        bar = GRAD_REL_L2 * np.linalg.norm(want) + floor * np.sqrt(want.size)
-        assert err <= bar, (name, err, np.linalg.norm(want))
+        bar = GRAD_REL_L2 * np.linalg.norm(want) + extra + floor * np.sqrt(want.size)
+        assert err <= bar, (name, err, np.linalg.norm(want), extra)
 
 
 @pytest.mark.parametrize("i", range(N_SHORT + N_LONG, N_SHORT + N_LONG + N_FP32), ids=_case_id)
