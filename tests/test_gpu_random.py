@@ -1,6 +1,7 @@
 """Seeded random configurations, forward and backward through the public API
 against the fp64 oracle: shapes, head groups, layouts and every mask drawn
-together, so that combinations no hand-written case names are covered too.
+together, so that combinations no hand-written case names are covered too
+(and likewise for the fp32 forward, the decode step and the E4M3 forward).
 Outputs start as NaN (an element the kernels never write fails the check).
 
 The draws are fixed by the seed: a failing case keeps its id from run to run.
@@ -199,3 +200,95 @@ def test_random_fp32_forward(ea, i):
         A, _ = oracle_fp8.rounding_terms(qn, kn, vn, c["scale"], causal=c["causal"],
                                          key_lens=okw["key_lens"], block_mask=c["block_mask"])
         assert np.all(err <= 2.0 ** -9 * A + 1e-4), float((err - 2.0 ** -9 * A).max())
+
+
+N_DECODE = 40         # decode steps against random caches
+
+
+def _draw_decode(i):
+    r = np.random.default_rng(5000 + i)
+    B = int(r.integers(1, 5))
+    H_kv = int(r.integers(1, 5))
+    group = int(r.choice([1, 2, 4, 8]))
+    n_q = int(r.integers(1, 9))
+    while group * n_q > 64:
+        n_q //= 2
+    N = int(r.choice([1, 63, 64, 65, 700, 2049])) if r.random() < 0.3 else int(r.integers(1, 3001))
+    lens = [int(x) for x in r.integers(0, N + 1, size=B)]
+    if r.random() < 0.3:
+        lens[int(r.integers(0, B))] = int(r.choice([0, N]))
+    return dict(B=B, H=H_kv * group, H_kv=H_kv, n_q=n_q, N=N, d=int(r.choice([64, 128])),
+                lens=lens, causal=bool(r.random() < 0.7), bnhd=bool(r.random() < 0.3),
+                seed=int(r.integers(0, 2 ** 31)))
+
+
+def _decode_id(i):
+    c = _draw_decode(i)
+    return (f"{i}-B{c['B']}H{c['H']}/{c['H_kv']}q{c['n_q']}N{c['N']}d{c['d']}"
+            + ("-causal" if c["causal"] else "") + ("-bnhd" if c["bnhd"] else ""))
+
+
+@pytest.mark.parametrize("i", range(N_DECODE), ids=_decode_id)
+def test_random_decode_step(ea, i):
+    """attn_decode (the newest n_q positions of each sequence against its
+    cache, split into chunks merged by the logsumexp rule) against the
+    oracle's decode_forward: O within 1e-2 beyond its bf16 rounding, L within
+    1e-3; sequences with an empty cache give O = 0 and L = -inf."""
+    from tests.helpers import O_MAX_ABS, o_err
+    c = _draw_decode(i)
+    g = torch.Generator().manual_seed(c["seed"])
+    q = torch.randn(c["B"], c["H"], c["n_q"], c["d"], generator=g).to(torch.bfloat16)
+    k = torch.randn(c["B"], c["H_kv"], c["N"], c["d"], generator=g).to(torch.bfloat16)
+    v = torch.randn(c["B"], c["H_kv"], c["N"], c["d"], generator=g).to(torch.bfloat16)
+    lens = torch.tensor(c["lens"], dtype=torch.int32)
+    kd, vd = (_to_dev(t, c["bnhd"]) for t in (k, v))
+    scale = c["d"] ** -0.5
+    o, lse = ea.attention_decode(q.cuda(), kd, vd, lens.cuda(), scale=scale, causal=c["causal"])
+    torch.cuda.synchronize()
+    ea.check()
+    O, L = oracle.decode_forward(np64(q), np64(k), np64(v), scale=scale,
+                                 cache_lens=lens.numpy(), causal=c["causal"])
+    assert o_err(np64(o.cpu()), O) <= O_MAX_ABS, _decode_id(i)
+    assert max_abs(lse.cpu().numpy(), L) <= L_MAX_ABS, _decode_id(i)
+
+
+N_FP8 = 24            # E4M3 forwards (the last four few-head long cases on the split path)
+
+
+def _draw_fp8(i):
+    r = np.random.default_rng(7000 + i)
+    long = i >= N_FP8 - 4
+    B = 1 if long else int(r.integers(1, 4))
+    H_kv = 1 if long else int(r.integers(1, 4))
+    H = H_kv * (int(r.choice([1, 2])) if long else int(r.choice([1, 2, 4])))
+    N = int(r.integers(2048, 2600)) if long else (
+        int(r.choice(EDGE_N)) if r.random() < 0.4 else int(r.integers(1, 701)))
+    c = dict(B=B, H=H, H_kv=H_kv, N=N, causal=bool(r.random() < 0.5),
+             std=float(r.choice([0.5, 1.0, 2.0])), seed=int(r.integers(0, 2 ** 31)),
+             key_lens=None, block_mask=None)
+    if r.random() < 0.4:
+        c["key_lens"] = [int(x) for x in r.integers(0, N + 1, size=B)]
+    if not long and r.random() < 0.3:
+        nb = (N + 127) // 128
+        shape = (B, H, nb, nb) if r.random() < 0.5 else (nb, nb)
+        c["block_mask"] = torch.from_numpy((r.random(shape) < r.uniform(0.2, 0.8)).astype(np.uint8))
+    return c
+
+
+def _fp8_id(i):
+    c = _draw_fp8(i)
+    return (f"{i}-B{c['B']}H{c['H']}/{c['H_kv']}N{c['N']}-std{c['std']}"
+            + ("-causal" if c["causal"] else "") + ("-pad" if c["key_lens"] is not None else "")
+            + ("-block" if c["block_mask"] is not None else ""))
+
+
+@pytest.mark.parametrize("i", range(N_FP8), ids=_fp8_id)
+def test_random_fp8_forward(ea, i):
+    """The E4M3 forward (d = 128) against the oracle on the de-scaled inputs,
+    under the E4M3 rounding bound of tests/test_gpu_fp8.py."""
+    from tests.test_gpu_fp8 import FP8, _check_full
+    if FP8 is None:
+        pytest.skip("torch without float8_e4m3fn")
+    c = _draw_fp8(i)
+    _check_full(ea, c["B"], c["H"], c["H_kv"], c["N"], c["seed"], causal=c["causal"],
+                key_lens=c["key_lens"], block_mask=c["block_mask"], std=c["std"])
